@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Benchmark of the generalized paged-attention hot path on one GB300.
+
+One *step* is one pass of the whole path over one batch of synthetic input:
+  block_copy  (copy-on-write of shared blocks before they are written),
+  kv_append   (the step's new tokens into their slots),
+  pa_forward  (attention of every sequence's new tokens over its cached-plus-new context).
+
+Workloads (``--workload``):
+  decode13b   (default) 64 sequences, Llama-2-13B attention shape (40 MHA heads, d=128), bf16,
+              block 16, q_len 1, context U{512..4096}, blocks scattered in a pool with 10% free;
+              6 sequences fork (copy-on-write of their partially filled last block).
+              Metric: algorithmic HBM bytes / step time, GB/s.
+  mixed_gqa   32 resumed conversations (history U{1024..16384}, new turn U{16..512}) + 32 decode
+              sequences, GQA 32/8, d=128, bf16, block 32.  Metric: attention TFLOP/s (causal-exact).
+  longprefill 8 x (16384 cached + 2048 new), 40 MHA heads, d=128, bf16, block 16, ConvKV-style
+              turn segments.  Metric: attention TFLOP/s.
+  kvmove      40-layer 5120-hidden fp16 pool (8 layers resident), 64 sessions: append, 10%
+              copy-on-write copies, swap-in of 8 sessions from a pinned host pool, layer by
+              layer.  Metric: GB/s moved (read + write).
+
+``--impl reference`` times the float64 CPU oracle (the only reference implementation: the pages
+publish no code) on a bounded sample of the same workload and prints the same JSON line.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the path has no
+exchange step); the time is the max over ranks and ``value`` sums the ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_cache_generalized_gb300 import workloads as W  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# Workloads on the device
+# ------------------------------------------------------------------------------------------------
+def attn_flops(ctx, ql, hq, d):
+    """Causal-exact attention FLOPs: 4 * d * Hq per (query, visible key) pair (QK^T and PV)."""
+    c = ctx.astype(np.float64)
+    q = ql.astype(np.float64)
+    pairs = (q * c + q * (q + 1) / 2).sum()
+    return 4.0 * d * hq * pairs
+
+
+def _tc_enabled():
+    """Whether libpagedkv routes multi-token bf16/f16 turns to its tensor-core kernel."""
+    return False
+
+
+class AttnStep:
+    """block_copy + kv_append + pa_forward over one AttnBatch, all inputs resident on the GPU."""
+
+    def __init__(self, batch: W.AttnBatch, dev, cow_frac=0.0, seed=0):
+        import torch
+        import paged_kv_cache_generalized_gb300 as pkg
+
+        self.pkg, self.torch, self.b, self.dev = pkg, torch, batch, dev
+        tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[batch.dtype]
+        self.tdt = tdt
+
+        def up(x, dt=None):
+            t = torch.from_numpy(np.ascontiguousarray(x))
+            if dt is not None and dt != torch.float32:
+                t = t.view(torch.int16).view(dt)
+            return t
+
+        self.host = {
+            "q": up(batch.q, tdt).pin_memory(),
+            "k_new": up(batch.k_new, tdt).pin_memory(),
+            "v_new": up(batch.v_new, tdt).pin_memory(),
+            "slots": up(batch.slot_mapping).pin_memory(),
+            "bt": up(batch.block_tables).pin_memory(),
+            "ctx": up(batch.ctx_lens).pin_memory(),
+            "ql": up(batch.q_lens).pin_memory(),
+        }
+        # copy-on-write forks: a fraction of sequences copy their last block to a free block
+        B = batch.block_size
+        n = batch.seq_lens
+        used = np.zeros(batch.num_blocks, bool)
+        for i in range(batch.num_seqs):
+            used[batch.block_tables[i, :(n[i] + B - 1) // B]] = True
+        free = np.flatnonzero(~used)
+        rng = np.random.default_rng(seed)
+        k = min(int(round(cow_frac * batch.num_seqs)), len(free))
+        forks = rng.choice(batch.num_seqs, k, replace=False) if k else np.zeros(0, np.int64)
+        pairs = np.array([[batch.block_tables[i, (n[i] - 1) // B], free[j]] for j, i in enumerate(forks)],
+                         dtype=np.int64).reshape(-1, 2)
+        self.host["pairs"] = up(pairs).pin_memory()
+        self.dev_in = {k2: v.to(dev) for k2, v in self.host.items()}
+        # K and V caches are the two planes of one pool, so one block_copy moves both
+        self.pool = torch.empty((2,) + batch.k_cache.shape, dtype=tdt, device=dev)
+        self.pool[0].copy_(up(batch.k_cache, tdt))
+        self.pool[1].copy_(up(batch.v_cache, tdt))
+        self.k_cache, self.v_cache = self.pool[0], self.pool[1]
+        self.out = torch.empty_like(self.dev_in["q"])
+        self.out_host = torch.empty_like(self.host["q"]).pin_memory()
+        self.ws = torch.empty(max(256, pkg.forward_workspace_size(self.dev_in["q"], self.k_cache,
+                                                                 self.dev_in["bt"], self.dev_in["ctx"])),
+                              dtype=torch.uint8, device=dev)
+        es = 4 if batch.dtype == "f32" else 2
+        Hq, Hkv, d = batch.num_q_heads, batch.num_kv_heads, batch.head_dim
+        T = batch.total_q
+        nb = (n + B - 1) // B
+        self.bytes_attn = float(n.sum() * Hkv * d * es * 2 + 2 * T * Hq * d * es + nb.sum() * 4 + batch.num_seqs * 8)
+        self.bytes_append = float(2 * 2 * T * Hkv * d * es + 8 * T)
+        self.bytes_copy = float(len(pairs) * 2 * 2 * Hkv * B * d * es + pairs.size * 8)
+        self.flops = attn_flops(batch.ctx_lens, batch.q_lens, Hq, d)
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+        # block_copy (if any fork) + kv_append + pa_forward's plan, CUDA-core and combine kernels
+        # (+ the tensor-core kernel when the batch has multi-token turns it supports)
+        tc = T > batch.num_seqs and batch.dtype in ("bf16", "f16") and d == 128 and _tc_enabled()
+        self.launches_per_step = (1 if len(pairs) else 0) + 1 + 3 + (1 if tc else 0)
+
+    def _copy(self, inp):
+        if inp["pairs"].shape[0]:
+            self.pkg.block_copy(self.pool, self.pool, inp["pairs"])
+
+    def step(self, ev=None):
+        inp = self.dev_in
+        self._copy(inp)
+        self.pkg.kv_append(inp["k_new"], inp["v_new"], inp["slots"], self.k_cache, self.v_cache)
+        if ev is not None:
+            ev[0].record()
+        self.pkg.pa_forward(inp["q"], self.k_cache, self.v_cache, inp["bt"], inp["ctx"], inp["ql"],
+                            self.b.scale, out=self.out, workspace=self.ws)
+        if ev is not None:
+            ev[1].record()
+
+    def e2e_step(self):
+        for k2, v in self.host.items():
+            self.dev_in[k2].copy_(v, non_blocking=True)
+        self.step()
+        self.out_host.copy_(self.out, non_blocking=True)
+
+
+def build_attn_step(name, dev):
+    if name == "decode13b":
+        b = W.decode13b(seed=2, poison=False)
+        return AttnStep(b, dev, cow_frac=0.1, seed=2), b
+    if name == "mixed_gqa":
+        b = W.mixed_gqa(seed=3, poison=False)
+        return AttnStep(b, dev, cow_frac=0.0, seed=3), b
+    if name == "longprefill":
+        b = W.longprefill(seed=4, poison=False)
+        return AttnStep(b, dev, cow_frac=0.0, seed=4), b
+    raise ValueError(name)
+
+
+WORKLOAD_TEXT = {
+    "decode13b": "decode13b: 64 seqs, 40 MHA heads, head_dim 128, bf16, block 16, q_len 1, "
+                 "ctx U{512..4096}, pool +10% free, 6 copy-on-write forks per step",
+    "mixed_gqa": "mixed_gqa: 32 resumed turns (ctx U{1024..16384}, q U{16..512}) + 32 decode "
+                 "(ctx U{256..8192}), GQA 32/8, head_dim 128, bf16, block 32",
+    "longprefill": "longprefill: 8 seqs x (16384 cached + 2048 new), 40 MHA heads, head_dim 128, "
+                   "bf16, block 16, ConvKV turn segments 64..1024 tokens",
+}
+
+
+# ------------------------------------------------------------------------------------------------
+# Distributed helpers (independent replicas; timing barrier and max over ranks only)
+# ------------------------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, use_cuda):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    dist.init_process_group("nccl" if use_cuda else "gloo")
+    return dist
+
+
+def max_over_ranks(dist, value, device=None):
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample
+# ------------------------------------------------------------------------------------------------
+def oracle_sample(b: W.AttnBatch, budget_s: float, max_rows=None):
+    """Times the float64 oracle on rows of the workload (whole sequences, all heads, in order)
+    until about ``budget_s`` seconds of work; returns (seconds, kv_bytes, flops, rows, threads)."""
+    import oracle
+
+    threads = oracle.max_threads()
+    es = 4 if b.dtype == "f32" else 2
+    order = np.argsort(-b.seq_lens, kind="stable")  # one of the longest first, then the rest
+    rows, kv_bytes, flops = [], 0.0, 0.0
+    t_total = 0.0
+    done_rows = 0
+    for i in order:
+        seq_rows = [(i, j, h) for j in range(int(b.q_lens[i])) for h in range(b.num_q_heads)]
+        if max_rows is not None and done_rows + len(seq_rows) > max_rows and done_rows:
+            break
+        t0 = time.perf_counter()
+        oracle.paged_attention_batch(b, rows=np.array(seq_rows, np.int64), threads=threads)
+        t_total += time.perf_counter() - t0
+        done_rows += len(seq_rows)
+        c, q = int(b.ctx_lens[i]), int(b.q_lens[i])
+        kv_bytes += (c + q) * b.num_kv_heads * b.head_dim * es * 2
+        flops += attn_flops(np.array([c]), np.array([q]), b.num_q_heads, b.head_dim)
+        rows.append(i)
+        if t_total >= budget_s:
+            break
+    return t_total, kv_bytes, flops, rows, threads
+
+
+def metric_for(name):
+    if name in ("decode13b", "kvmove"):
+        return ("paged-attn decode KV GB/s (algorithmic HBM bytes per step / step time)", "GB/s", True)
+    return ("paged-attn mixed-prefill TFLOP/s (causal-exact attention FLOPs / step time)", "TFLOP/s", True)
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    name = args.workload
+    metric, unit, hib = metric_for(name)
+    b = {"decode13b": lambda: W.decode13b(seed=2, poison=False),
+         "mixed_gqa": lambda: W.mixed_gqa(seed=3, poison=False),
+         "longprefill": lambda: W.longprefill(seed=4, poison=False)}[name]()
+    total = args.steps + args.warmup
+    per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
+    vals, secs = [], 0.0
+    sample_desc = None
+    for s in range(total):
+        t, kvb, fl, rows, threads = oracle_sample(b, per_step)
+        if s >= args.warmup:
+            secs += t
+            vals.append((kvb, fl, t))
+        sample_desc = (f"float64 oracle rows of {len(rows)} sequence(s) (all heads, all new tokens) "
+                       f"of the {name} batch per step, ~{per_step:.2f}s each")
+    kvb = sum(v[0] for v in vals)
+    fl = sum(v[1] for v in vals)
+    value = (kvb / secs / 1e9) if unit == "GB/s" else (fl / secs / 1e12)
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / max(1, len(vals)) * 1e3, "higher_is_better": hib,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[name]},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                             "sample": sample_desc},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------
+# Native (CUDA) arm
+# ------------------------------------------------------------------------------------------------
+def run_native(args):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    peaks, peak_src = load_peaks()
+    name = args.workload
+    metric, unit, hib = metric_for(name)
+    step_obj, batch = build_attn_step(name, dev)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step_obj.step()
+    torch.cuda.synchronize()
+    flags = step_obj.pkg.device_status()
+    if flags:
+        raise RuntimeError(f"device status after warm-up: {step_obj.pkg.status_names(flags)}")
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record()
+        for i in range(K):
+            step_obj.step(evs[i])
+        stop.record()
+        torch.cuda.synchronize()
+    barrier(dist)
+    elapsed_ms = start.elapsed_time(stop)
+    attn_ms = sum(a.elapsed_time(b_) for a, b_ in evs) / K
+    elapsed_ms = max_over_ranks(dist, elapsed_ms, dev)
+    ms_step = elapsed_ms / K
+
+    step_bytes = step_obj.bytes_attn + step_obj.bytes_append + step_obj.bytes_copy
+    if unit == "GB/s":
+        value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    else:
+        value = step_obj.flops * world / (ms_step * 1e-3) / 1e12
+
+    # end to end through the public API: H2D of the step's inputs, the step, D2H of the output
+    Ke = min(K, max(20, K // 5))
+    for _ in range(3):
+        step_obj.e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(Ke):
+        step_obj.e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev) / Ke
+    e2e_val = (step_bytes if unit == "GB/s" else step_obj.flops) * world / (e2e_ms * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
+    flags = step_obj.pkg.device_status()
+
+    if rank != 0:
+        return
+    if unit == "GB/s":
+        achieved = step_obj.bytes_attn / (attn_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "kernel": "pa_forward (plan + split-KV CUDA-core attention + combine)",
+                "peak_source": f"hbm_gbs of {peak_src}"}
+    else:
+        achieved = step_obj.flops / (attn_ms * 1e-3) / 1e12
+        pk = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
+                "frac": achieved / pk, "traffic": None, "kernel": "pa_forward",
+                "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+
+    cpu = None
+    if world == 1 or rank == 0:
+        t, kvb, fl, rows, threads = oracle_sample(batch, args.cpu_seconds)
+        cval = kvb / t / 1e9 if unit == "GB/s" else fl / t / 1e12
+        cpu = {"value": cval, "unit": unit, "cores": threads, "kind": "oracle",
+               "sample": f"float64 oracle on {len(rows)} whole sequence(s) of the batch (all heads, "
+                         f"all new tokens), {t:.1f}s; attention only"}
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": hib,
+            "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype, "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[name],
+                       "l2": "inputs larger than L2 (KV pool %.2f GB resident)" % (
+                           (step_obj.pool.numel() * step_obj.pool.element_size()) / 1e9),
+                       "bytes_per_step": step_bytes, "attn_flops_per_step": step_obj.flops,
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": step_obj.h2d_bytes,
+                    "d2h_bytes_per_step": step_obj.d2h_bytes, "ms_per_step": e2e_ms},
+            "gpu_launches": step_obj.launches_per_step * K,
+            "attn_ms": attn_ms, "device_status": flags,
+            "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="decode13b", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

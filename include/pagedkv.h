@@ -1,0 +1,192 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: generalized paged attention, cache append and block
+ * copy on one GB300 (sm_103a).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensors are caller-owned, plain pointers; the library never allocates, never frees and
+ *    never copies between host and device on the caller's behalf.  Device pointers must belong to
+ *    the current CUDA device.  Host pointers are accepted only where a call says so (and must be
+ *    page-locked, e.g. cudaHostAlloc / torch pin_memory, so the GPU can address them).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *    and never synchronises, except pa_get_device_status.  No call falls back to the CPU.
+ *  - Shapes are described by small structs passed by pointer; element strides are given in
+ *    elements of the tensor's dtype, byte strides say so.
+ *  - Host-side validation (shapes, dtypes, alignment, supported sizes, workspace size) returns a
+ *    pa_status != PA_OK and launches nothing.  Data-dependent faults that only the device can see
+ *    (an out-of-range block id or slot, inconsistent lengths) are never trapped: the offending
+ *    work is skipped, and a bit is set in a per-device status word that pa_get_device_status
+ *    reads and clears.
+ *  - Calls that share a workspace must not run concurrently.
+ *
+ * Notation (as on the pages): B = block size in tokens; Hq / Hkv = query / KV heads,
+ * g = Hq / Hkv (GQA group); d = head_dim.  Sequence i has c_i = ctx_lens[i] tokens cached before
+ * this step and q_i = q_lens[i] >= 1 new tokens; n_i = c_i + q_i; T = sum_i q_i.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* a NULL pointer, a bad shape, stride or alignment */
+    PA_ERR_UNSUPPORTED = 2,  /* a valid request this build does not implement (e.g. head_dim) */
+    PA_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned */
+    PA_ERR_CUDA = 4,         /* a CUDA runtime call (launch, attribute query) failed */
+    PA_ERR_DEVICE = 5        /* pa_get_device_status found device-side error bits */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
+
+/* Bits of the device status word (pa_get_device_status). */
+#define PA_DEV_BAD_BLOCK_ID 0x1u  /* a block-table entry that had to be read was outside the pool */
+#define PA_DEV_BAD_LENGTHS 0x2u   /* q_len < 1, ctx_len < 0, n_i > max_blocks_per_seq * B, or
+                                     sum(q_lens) != total_q; that sequence's rows are not written */
+#define PA_DEV_BAD_SLOT 0x4u      /* kv_append: slot_mapping entry >= num_blocks * B (skipped) */
+#define PA_DEV_BAD_PAIR 0x8u      /* block_copy: a src or dst block id outside its pool (skipped) */
+#define PA_DEV_TIMEOUT 0x10u      /* a bounded wait inside a kernel gave up (internal error) */
+
+/* ------------------------------------------------------------------------------------------
+ * pa_forward: generalized paged attention.
+ *
+ * For every sequence i, new token j < q_i and query head h, with P = c_i + j the token's
+ * absolute position and kh = h / g its KV head:
+ *     out[cu_i + j, h, :] = sum_{p <= P} softmax_p(scale * q[cu_i + j, h, :] . K_i[p, kh, :]) V_i[p, kh, :]
+ * where K_i[p] lives in physical block block_tables[i][p / B] at slot p % B, and cu_i is the
+ * exclusive prefix sum of q_lens.  This is softmax(QK^T / sqrt(d_k)) V in the blockwise form
+ * A_j / o = sum_j A_j V_j of "SOSP 2023論文解説: PagedAttention" (section
+ * "PagedAttentionアルゴリズム"), generalized to ragged multi-token queries with a fused causal
+ * mask over cached-plus-new positions as in "Stateful Large Language Model Serving with
+ * Pensieve" (section "汎化PagedAttentionカーネル"); prefill turns (q_i > 1) and decode steps
+ * (q_i = 1) share one call.  GQA groups are contiguous ("KVキャッシュ管理の教科書" 第19章).
+ * The new tokens' K/V must already be in the cache (kv_append first).
+ *
+ * Layouts (all device memory):
+ *   q, out        [T, Hq, d], row-major, dtype `dims->dtype`.  `out` must not alias q or caches.
+ *   k_cache, v_cache  element (block b, kv head kh, slot s, dim x) at
+ *                 b * kv_block_stride + (kh * B + s) * d + x  (dtype `dims->dtype`).
+ *                 Physical blocks may be shared by several sequences (prefix sharing).
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq]; entries past ceil(n_i / B) are never read.
+ *   ctx_lens, q_lens  int32 [num_seqs].
+ *   scale         the softmax scale, normally 1/sqrt(d).
+ *   workspace     device scratch of at least pa_forward_workspace_size(dims) bytes, 256-byte
+ *                 aligned; contents need no initialisation and are clobbered.
+ * Supported: dtype f32 / bf16 / f16; d in {64, 128}; B in {8, 16, 32, 64, 128}; Hq % Hkv == 0;
+ * 16-byte aligned q, out and caches; kv_block_stride a multiple of 8 elements.
+ * Multi-token bf16/f16 sequences with d = 128 run on the tcgen05 tensor-core kernel; decode and
+ * everything else on the CUDA-core split-KV kernel.
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t dtype;              /* pa_dtype of q, out, k_cache and v_cache */
+    int32_t num_seqs;           /* >= 1 */
+    int64_t total_q;            /* T: rows of q and out; must equal sum(q_lens) */
+    int32_t num_q_heads;        /* Hq */
+    int32_t num_kv_heads;       /* Hkv, divides Hq */
+    int32_t head_dim;           /* d */
+    int32_t block_size;         /* B */
+    int64_t num_blocks;         /* physical blocks addressable through k_cache / v_cache */
+    int32_t max_blocks_per_seq; /* row length of block_tables */
+    int64_t kv_block_stride;    /* elements between physical blocks b and b+1; 0 = Hkv * B * d */
+} pa_dims;
+
+size_t pa_forward_workspace_size(const pa_dims *dims);
+
+pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
+                     float scale, void *out, void *workspace, size_t workspace_bytes,
+                     pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * kv_append: write the new tokens' K/V into the paged cache.
+ *
+ * For every new token t with slot_mapping[t] >= 0, every layer l and KV head h:
+ *   k_cache[l][slot / B][h][slot % B][:] = k_new[l][t][h][:]   (and the same for V)
+ * A slot is physical_block * B + offset; the caller's allocator picks it so that a sequence fills
+ * its partially filled last block before a fresh one ("SOSP 2023論文解説: PagedAttention",
+ * section "ブロックテーブルによるメモリ管理").  slot < 0 marks padding and is skipped; a slot
+ * >= num_blocks * B is skipped and flagged PA_DEV_BAD_SLOT.  Two tokens with the same slot in
+ * one call give an unspecified one of the two.  The copy is bit-exact.
+ *
+ * Layouts (device memory): k_new/v_new element (l, t, h, x) at l*new_layer_stride +
+ * (t*Hkv + h)*d + x; caches element (l, b, h, s, x) at l*cache_layer_stride +
+ * b*kv_block_stride + (h*B + s)*d + x; slot_mapping int64 [num_tokens].
+ * Rows must be 16-byte aligned (d * element size a multiple of 16).
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t dtype;              /* pa_dtype (only the element size matters) */
+    int64_t num_tokens;         /* T_new */
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int64_t num_blocks;
+    int64_t kv_block_stride;    /* 0 = Hkv * B * d */
+    int32_t num_layers;         /* >= 1 */
+    int64_t new_layer_stride;   /* 0 = num_tokens * Hkv * d */
+    int64_t cache_layer_stride; /* 0 = num_blocks * kv_block_stride */
+} kv_append_dims;
+
+pa_status kv_append(const kv_append_dims *dims, const void *k_new, const void *v_new,
+                    const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                    pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * block_copy: copy whole blocks, every plane, bit for bit.
+ *
+ * For every pair (s, t) = (pairs[2k], pairs[2k+1]) and every plane p < num_planes:
+ *   dst[p*dst_plane_stride + t*dst_block_stride .. + block_bytes) =
+ *   src[p*src_plane_stride + s*src_block_stride .. + block_bytes)
+ * Copy-on-write of a shared block before it is written ("SOSP 2023論文解説: PagedAttention",
+ * section "Copy-on-Writeによるメモリ共有") when src and dst are the same device pool; swap-in
+ * (src a page-locked host pool) and swap-out (dst a page-locked host pool) of blocks between the
+ * CPU and GPU tiers ("Stateful Large Language Model Serving with Pensieve", sections
+ * "GPU-CPU 2層キャッシュ構造" and "パイプライン化されたswap-in").  A plane is e.g. one
+ * (layer, K|V) slice of a pool.
+ *
+ * pairs is int64 [num_pairs, 2] in device memory.  All destination ids must be distinct and no
+ * destination may also be a source in the same call (pairs then act simultaneously); a violated
+ * precondition gives unspecified bytes in the affected blocks, nothing else.  Ids outside
+ * [0, src_num_blocks) / [0, dst_num_blocks) are skipped and flagged PA_DEV_BAD_PAIR.
+ * src and dst may be device memory or page-locked host memory.  block_bytes, strides and both
+ * base pointers must be multiples of 16 bytes.
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+    int64_t block_bytes;        /* bytes of one block in one plane */
+    int32_t num_planes;         /* >= 1 */
+    int64_t src_plane_stride;   /* bytes */
+    int64_t dst_plane_stride;   /* bytes */
+    int64_t src_block_stride;   /* bytes between blocks; 0 = block_bytes */
+    int64_t dst_block_stride;   /* bytes between blocks; 0 = block_bytes */
+    int64_t src_num_blocks;
+    int64_t dst_num_blocks;
+    int64_t num_pairs;          /* 0 is a no-op */
+} block_copy_dims;
+
+pa_status block_copy(const block_copy_dims *dims, const void *src, void *dst,
+                     const int64_t *pairs, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * pa_get_device_status: synchronise `stream`, return the current device's status bits
+ * (PA_DEV_*) accumulated since the last call in *flags, and clear them.  Returns PA_ERR_DEVICE
+ * when any bit was set, PA_ERR_CUDA when the synchronisation failed, else PA_OK.
+ * ---------------------------------------------------------------------------------------- */
+pa_status pa_get_device_status(uint32_t *flags, pa_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *pa_status_string(pa_status status);
+
+/* Library build identification: "pagedkv <version> sm_103a". */
+const char *pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,8 @@
+"""Generalized paged attention, cache append and block copy for one GB300 (sm_103a).
+
+The work runs in ``libpagedkv.so`` (hand-written CUDA behind a C ABI, ``include/pagedkv.h``);
+this package holds the in-tree build, a thin ctypes binding and the seeded workload generators.
+Calls raise if the library has not been built: there is no CPU fallback.
+"""
+from .pagedkv import (PagedKVError, block_copy, device_status, forward_workspace_size,  # noqa: F401
+                      kv_append, library_path, load_library, pa_forward, status_names, version)

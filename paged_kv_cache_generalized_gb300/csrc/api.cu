@@ -1,0 +1,250 @@
+// C-ABI entry points of libpagedkv.so: argument validation, workspace layout and the launch
+// sequence.  The declarations, with the meaning of every argument, are in include/pagedkv.h.
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+// Device status word (PA_DEV_* bits), one per device that loads the library.
+__device__ unsigned g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+// The status word's device address for the current device (looked up once per device; host
+// code must not use the symbol itself as an address).
+unsigned *status_ptr() {
+    static unsigned *ptrs[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<unsigned *>(p);
+    }
+    return ptrs[dev];
+}
+
+int sm_count() {
+    static int cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_dtype(int32_t t) { return t == PA_F32 || t == PA_BF16 || t == PA_F16; }
+
+bool overlap(const void *a, size_t an, const void *b, size_t bn) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bn && y < x + an;
+}
+
+pa_status check_dims(const pa_dims *d) {
+    if (!d) return PA_ERR_INVALID_ARG;
+    if (!valid_dtype(d->dtype)) return PA_ERR_INVALID_ARG;
+    if (d->num_seqs < 1 || d->num_seqs > (1 << 20)) return PA_ERR_INVALID_ARG;
+    if (d->total_q < d->num_seqs || d->total_q > (int64_t(1) << 30)) return PA_ERR_INVALID_ARG;
+    if (d->num_q_heads < 1 || d->num_kv_heads < 1 || d->num_q_heads > 1024) return PA_ERR_INVALID_ARG;
+    if (d->num_q_heads % d->num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (d->num_blocks < 1 || d->max_blocks_per_seq < 1) return PA_ERR_INVALID_ARG;
+    if (d->head_dim != 64 && d->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64 && d->block_size != 128)
+        return PA_ERR_UNSUPPORTED;
+    const int64_t dense = (int64_t)d->num_kv_heads * d->block_size * d->head_dim;
+    if (d->kv_block_stride != 0) {
+        if (d->kv_block_stride < dense) return PA_ERR_INVALID_ARG;
+        if ((d->kv_block_stride * elem_bytes(d->dtype)) % 16) return PA_ERR_INVALID_ARG;
+    }
+    if ((int64_t)d->max_blocks_per_seq * d->block_size > (int64_t(1) << 30)) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+}  // namespace
+
+int rows_per_item(const pa_dims &d) {
+    const int g = d.num_q_heads / d.num_kv_heads;
+    return g >= 4 ? 4 : (g >= 2 ? 2 : 1);
+}
+
+WsLayout ws_layout(const pa_dims &d) {
+    WsLayout L;
+    const size_t S = (size_t)d.num_seqs;
+    const int R = rows_per_item(d);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    L.counters = take(kNumCounters * sizeof(uint32_t));
+    L.cu_q = take((S + 1) * 4);
+    L.simt_cu = take((S + 1) * 4);
+    L.parts_cu = take((S + 1) * 4);
+    L.comb_cu = take((S + 1) * 4);
+    L.groups = take(S * 4);
+    L.nchunk = take(S * 4);
+    L.tc_cu = take((S + 1) * 4);
+    L.tc_seq = take(S * 4);
+    // Only sequences whose rows fit one row group are split, into at most kMaxSplits parts.
+    const int64_t splits = d.max_blocks_per_seq < kMaxSplits ? d.max_blocks_per_seq : kMaxSplits;
+    L.max_parts = splits > 1 ? (int64_t)d.num_kv_heads * (int64_t)S * splits : 0;
+    L.rows_per_item = R;
+    L.parts_ml = take((size_t)L.max_parts * R * sizeof(float) * 2);
+    L.parts_o = take((size_t)L.max_parts * R * d.head_dim * sizeof(float));
+    L.total = off;
+    return L;
+}
+
+bool tc_supported(const pa_dims &d) {
+    (void)d;
+    return false;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char *pa_version(void) { return "pagedkv 0.1 sm_103a"; }
+
+const char *pa_status_string(pa_status s) {
+    switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_DEVICE: return "PA_ERR_DEVICE";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+size_t pa_forward_workspace_size(const pa_dims *dims) {
+    if (check_dims(dims) != PA_OK) return 0;
+    return ws_layout(*dims).total;
+}
+
+pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
+                     float scale, void *out, void *workspace, size_t workspace_bytes,
+                     pa_stream_t stream) {
+    const pa_status st = check_dims(dims);
+    if (st != PA_OK) return st;
+    const pa_dims &d = *dims;
+    if (!q || !k_cache || !v_cache || !block_tables || !ctx_lens || !q_lens || !out)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(block_tables, 4) || !aligned(ctx_lens, 4) || !aligned(q_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;  // NaN scale
+    const size_t rows_bytes = (size_t)d.total_q * d.num_q_heads * d.head_dim * elem_bytes(d.dtype);
+    if (overlap(q, rows_bytes, out, rows_bytes)) return PA_ERR_INVALID_ARG;
+    const WsLayout lay = ws_layout(d);
+    if (!workspace || workspace_bytes < lay.total || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+    FwdArgs a;
+    a.dims = d;
+    a.q = q;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.out = out;
+    a.bt = block_tables;
+    a.ctx = ctx_lens;
+    a.qlen = q_lens;
+    a.scale = scale;
+    a.ws = static_cast<char *>(workspace);
+    a.lay = lay;
+    a.status = status_ptr();
+    a.num_sms = sm_count();
+    if (!a.status || a.num_sms <= 0) return PA_ERR_CUDA;
+    a.maybe_prefill = d.total_q > d.num_seqs;
+    a.tc = a.maybe_prefill && tc_supported(d);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_plan(a, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (a.tc && launch_tc(a, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_simt(a, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (lay.max_parts > 0 && launch_combine(a, s) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+pa_status kv_append(const kv_append_dims *dims, const void *k_new, const void *v_new,
+                    const int64_t *slot_mapping, void *k_cache, void *v_cache, pa_stream_t stream) {
+    if (!dims) return PA_ERR_INVALID_ARG;
+    const kv_append_dims &d = *dims;
+    if (!valid_dtype(d.dtype) || d.num_tokens < 0 || d.num_kv_heads < 1 || d.head_dim < 1 ||
+        d.block_size < 1 || d.num_blocks < 1 || d.num_layers < 1)
+        return PA_ERR_INVALID_ARG;
+    if (d.num_tokens == 0) return PA_OK;
+    const int eb = elem_bytes(d.dtype);
+    if ((d.head_dim * eb) % 16) return PA_ERR_UNSUPPORTED;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    const int64_t dense = (int64_t)d.num_kv_heads * d.block_size * d.head_dim;
+    if (d.kv_block_stride && (d.kv_block_stride < dense || (d.kv_block_stride * eb) % 16))
+        return PA_ERR_INVALID_ARG;
+    if ((d.new_layer_stride * eb) % 16 || (d.cache_layer_stride * eb) % 16) return PA_ERR_INVALID_ARG;
+    if (d.num_layers > 1) {
+        const int64_t bs = d.kv_block_stride ? d.kv_block_stride : dense;
+        if (d.new_layer_stride && d.new_layer_stride < d.num_tokens * d.num_kv_heads * d.head_dim)
+            return PA_ERR_INVALID_ARG;
+        if (d.cache_layer_stride && d.cache_layer_stride < d.num_blocks * bs) return PA_ERR_INVALID_ARG;
+    }
+    unsigned *status = status_ptr();
+    const int sms = sm_count();
+    if (!status || sms <= 0) return PA_ERR_CUDA;
+    if (launch_kv_append(d, k_new, v_new, slot_mapping, k_cache, v_cache, status, sms,
+                         reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+pa_status block_copy(const block_copy_dims *dims, const void *src, void *dst, const int64_t *pairs,
+                     pa_stream_t stream) {
+    if (!dims) return PA_ERR_INVALID_ARG;
+    const block_copy_dims &d = *dims;
+    if (d.num_pairs < 0 || d.num_planes < 1 || d.block_bytes <= 0 || d.src_num_blocks < 1 ||
+        d.dst_num_blocks < 1)
+        return PA_ERR_INVALID_ARG;
+    if (d.num_pairs == 0) return PA_OK;
+    if (!src || !dst || !pairs) return PA_ERR_INVALID_ARG;
+    if (d.block_bytes % 16 || d.src_plane_stride % 16 || d.dst_plane_stride % 16 ||
+        d.src_block_stride % 16 || d.dst_block_stride % 16)
+        return PA_ERR_INVALID_ARG;
+    if (d.src_block_stride && d.src_block_stride < d.block_bytes) return PA_ERR_INVALID_ARG;
+    if (d.dst_block_stride && d.dst_block_stride < d.block_bytes) return PA_ERR_INVALID_ARG;
+    if (!aligned(src, 16) || !aligned(dst, 16) || !aligned(pairs, 8)) return PA_ERR_INVALID_ARG;
+    unsigned *status = status_ptr();
+    const int sms = sm_count();
+    if (!status || sms <= 0) return PA_ERR_CUDA;
+    if (launch_block_copy(d, src, dst, pairs, status, sms, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+pa_status pa_get_device_status(uint32_t *flags, pa_stream_t stream) {
+    if (!flags) return PA_ERR_INVALID_ARG;
+    *flags = 0;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess) return PA_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess) return PA_ERR_CUDA;
+    *flags = v;
+    return v ? PA_ERR_DEVICE : PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,683 @@
+// Generalized paged attention on CUDA cores: the device-side planner, the split-KV work-item
+// kernel and the split combine.
+//
+// Method: softmax(QK^T / sqrt(d_k)) V evaluated block by block through the block table
+// ("SOSP 2023論文解説: PagedAttention", section "PagedAttentionアルゴリズム", blockwise A_j and
+// o = sum_j A_j V_j), for ragged multi-token queries with a causal mask over cached-plus-new
+// positions ("Stateful Large Language Model Serving with Pensieve", section
+// "汎化PagedAttentionカーネル").  The softmax is computed online with a running max and sum,
+// and a sequence's KV range may be split across work items whose partial (max, sum, weighted V)
+// triples are merged with the logsumexp rule L = m + log(l) ("KVキャッシュ管理の教科書", 第6章,
+// FlashAttention-2's statistics).
+//
+// GB300 design: one warp owns one work item (a KV head, up to R query rows of one sequence that
+// share it, and a range of KV blocks).  The warp streams its K/V through a private ring of
+// shared-memory stages filled by bulk asynchronous copies (cp.async.bulk, one 16-token run of a
+// (block, head) per copy, completion on an mbarrier), so each SM keeps ~100+ KB of HBM reads in
+// flight.  Half-warps take alternate keys; each lane holds d/16 dimensions, reductions are
+// warp shuffles.  Work items are taken from a global counter (persistent grid).
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kStageTokens = 16;       // keys per pipeline stage
+constexpr int kSimtMaxWarps = 8;
+
+// ----------------------------------------------------------------------------------------------
+// Planner (one CTA).  Reads q_lens/ctx_lens on the device, so no host round trip is needed.
+// ----------------------------------------------------------------------------------------------
+struct PlanParams {
+    const int32_t *ctx;
+    const int32_t *qlen;
+    uint32_t *counters;
+    int32_t *cu_q, *simt_cu, *parts_cu, *comb_cu, *groups, *nchunk, *tc_cu, *tc_seq;
+    unsigned *status;
+    int64_t total_q;
+    int64_t max_parts;
+    int num_seqs, kv_heads, group, block_size, max_blocks, rows, tc, total_warps;
+};
+
+constexpr int kPlanThreads = 1024;
+
+// In-place exclusive scan of a[0..n) (a[n] receives the total), one CTA.
+__device__ int64_t block_exclusive_scan(int32_t *a, int n) {
+    __shared__ int64_t warp_sums[32];
+    __shared__ int64_t carry_sh;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry_sh = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += kPlanThreads) {
+        const int i = base + tid;
+        int64_t v = i < n ? a[i] : 0;
+        int64_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int64_t w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_sums[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int64_t carry = carry_sh;
+        const int64_t before = (warp ? warp_sums[warp - 1] : 0) + x - v;
+        if (i < n) a[i] = (int32_t)(carry + before);
+        __syncthreads();
+        if (tid == 0) carry_sh = carry + warp_sums[31];
+        __syncthreads();
+    }
+    const int64_t total = carry_sh;
+    if (tid == 0) a[n] = (int32_t)total;
+    __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
+    __shared__ int64_t red[32];
+    const int tid = threadIdx.x;
+    const int S = p.num_seqs;
+    if (tid < kNumCounters) p.counters[tid] = 0;
+    // pass A: exclusive prefix of q_lens (the caller's packing of q and out)
+    for (int i = tid; i < S; i += kPlanThreads) p.cu_q[i] = max(p.qlen[i], 0);
+    __syncthreads();
+    const int64_t total = block_exclusive_scan(p.cu_q, S);
+    const bool packing_ok = (total == p.total_q);
+    if (!packing_ok && tid == 0) report(p.status, PA_DEV_BAD_LENGTHS);
+
+    // pass B: classify sequences, total CUDA-core work (block-heads) for the split size
+    int64_t work = 0;
+    for (int i = tid; i < S; i += kPlanThreads) {
+        const int c = p.ctx[i], q = p.qlen[i];
+        const int64_t n = (int64_t)c + q;
+        const int64_t nb = (n + p.block_size - 1) / p.block_size;
+        const bool valid = packing_ok && q >= 1 && c >= 0 && nb <= p.max_blocks;
+        if (packing_ok && !valid) report(p.status, PA_DEV_BAD_LENGTHS);
+        int path = 0;
+        if (valid) path = (p.tc && (int64_t)q * p.group >= kTcMinRows) ? 2 : 1;
+        const int64_t rows = (int64_t)q * p.group;
+        const int G = path == 1 ? (int)((rows + p.rows - 1) / p.rows) : 0;
+        p.groups[i] = path == 0 ? -1 : G;    // -1 marks an invalid sequence
+        p.nchunk[i] = path == 2 ? 0 : 1;
+        if (path == 1) work += (int64_t)p.kv_heads * G * nb;
+    }
+    // block reduce of work
+    {
+        int64_t w = work;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+        if ((tid & 31) == 0) red[tid >> 5] = w;
+        __syncthreads();
+        if (tid < 32) {
+            w = red[tid];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+            if (tid == 0) red[0] = w;
+        }
+        __syncthreads();
+        work = red[0];
+        __syncthreads();
+    }
+    // about 16 work items per warp slot of the persistent grid
+    const int64_t target = (int64_t)p.total_warps * 16;
+    int64_t chunk = (work + target - 1) / (target > 0 ? target : 1);
+    if (chunk < 1) chunk = 1;
+    if (tid == 0) p.counters[kChunkBlocks] = (uint32_t)chunk;
+
+    // pass C: per-sequence counts
+    for (int i = tid; i < S; i += kPlanThreads) {
+        const int G = p.groups[i];
+        int32_t items = 0, parts = 0, comb = 0;
+        if (G > 0) {
+            const int64_t n = (int64_t)p.ctx[i] + p.qlen[i];
+            const int64_t nb = (n + p.block_size - 1) / p.block_size;
+            // only sequences whose rows fit one row group are split (decode steps); longer
+            // turns already spread over their row groups
+            int K = 1;
+            if (G == 1) {
+                int64_t c_i = chunk;
+                const int64_t min_c = (nb + kMaxSplits - 1) / kMaxSplits;
+                if (c_i < min_c) c_i = min_c;
+                K = (int)((nb + c_i - 1) / c_i);
+            }
+            p.nchunk[i] = K;
+            items = p.kv_heads * G * K;
+            if (K > 1) {
+                parts = items;
+                comb = p.kv_heads * G * p.rows;
+            }
+        }
+        p.simt_cu[i] = items;
+        p.parts_cu[i] = parts;
+        p.comb_cu[i] = comb;
+    }
+    __syncthreads();
+    const int64_t n_items = block_exclusive_scan(p.simt_cu, S);
+    const int64_t n_parts = block_exclusive_scan(p.parts_cu, S);
+    const int64_t n_comb = block_exclusive_scan(p.comb_cu, S);
+    if (n_parts > p.max_parts) {
+        // cannot happen with the workspace bound; refuse rather than overflow
+        if (tid == 0) report(p.status, PA_DEV_BAD_LENGTHS);
+        if (tid == 0) {
+            p.counters[kSimtTotal] = 0;
+            p.counters[kCombTotal] = 0;
+        }
+    } else if (tid == 0) {
+        p.counters[kSimtTotal] = (uint32_t)n_items;
+        p.counters[kCombTotal] = (uint32_t)n_comb;
+    }
+
+    // tensor-core tiles: sequences ranked by descending length (longest first), ties by index
+    if (p.tc) {
+        for (int i = tid; i < S; i += kPlanThreads) p.tc_seq[i] = -1;
+        __syncthreads();
+        const bool rank_by_len = S <= 4096;
+        for (int i = tid; i < S; i += kPlanThreads) {
+            if (p.groups[i] < 0 || p.nchunk[i] != 0) continue;   // not a tensor-core sequence
+            const int64_t ni = (int64_t)p.ctx[i] + p.qlen[i];
+            int rank = 0;
+            for (int k = 0; k < S; ++k) {
+                if (p.groups[k] < 0 || p.nchunk[k] != 0) continue;
+                if (rank_by_len) {
+                    const int64_t nk = (int64_t)p.ctx[k] + p.qlen[k];
+                    if (nk > ni || (nk == ni && k < i)) ++rank;
+                } else if (k < i) {
+                    ++rank;
+                }
+            }
+            p.tc_seq[rank] = i;
+        }
+        __syncthreads();
+        for (int r = tid; r < S; r += kPlanThreads) {
+            const int i = p.tc_seq[r];
+            int32_t tiles = 0;
+            if (i >= 0) {
+                const int64_t rows = (int64_t)p.qlen[i] * p.group;
+                tiles = p.kv_heads * (int32_t)((rows + kTcTileRows - 1) / kTcTileRows);
+            }
+            p.tc_cu[r] = tiles;
+        }
+        __syncthreads();
+        const int64_t n_tiles = block_exclusive_scan(p.tc_cu, S);
+        if (tid == 0) p.counters[kTcTotal] = (uint32_t)n_tiles;
+    }
+}
+
+// Last index k in [0, n) with a[k] <= key (a is a non-decreasing prefix array of n+1 entries
+// and key < a[n]).
+__device__ __forceinline__ int find_owner(const int32_t *a, int n, int key) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a + mid) <= key) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ----------------------------------------------------------------------------------------------
+// Work-item kernel
+// ----------------------------------------------------------------------------------------------
+struct SimtParams {
+    const char *q;
+    const char *k;
+    const char *v;
+    char *out;
+    const int32_t *bt, *ctx, *qlen;
+    const int32_t *cu_q, *simt_cu, *parts_cu, *groups, *nchunk;
+    uint32_t *counters;
+    float2 *parts_ml;
+    float *parts_o;
+    unsigned *status;
+    int64_t num_blocks, block_stride;   // elements
+    float scale_log2;                   // scale * log2(e)
+    int num_seqs, q_heads, kv_heads, group, block_size, max_blocks, nst, bar_bytes;
+};
+
+template <typename T, int D, int R>
+__global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(SimtParams p) {
+    constexpr int E = D / 16;                       // dims per lane
+    constexpr uint32_t kRunBytes = kStageTokens * D * sizeof(T);
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = lane >> 4, sub = lane & 15;
+    const int NST = p.nst;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * NST;
+    unsigned char *ring = smem + p.bar_bytes + (size_t)warp * NST * 2 * kRunBytes;
+    if (lane == 0) {
+        for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+
+    const int B = p.block_size;
+    const int spb = B / kStageTokens;               // stages per block
+    uint32_t issued = 0, consumed = 0;               // ring positions (persist across items)
+    const uint32_t total_items = p.counters[kSimtTotal];
+
+    while (true) {
+        int item = 0;
+        if (lane == 0) item = (int)atomicAdd(&p.counters[kSimtNext], 1u);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if ((uint32_t)item >= total_items) break;
+
+        const int seq = find_owner(p.simt_cu, p.num_seqs, item);
+        const int local = item - __ldg(p.simt_cu + seq);
+        const int K = __ldg(p.nchunk + seq);
+        const int G = __ldg(p.groups + seq);
+        const int chunk = local % K;
+        const int rest = local / K;
+        const int grp = rest % G;
+        const int kvh = rest / G;
+        const int c = __ldg(p.ctx + seq), qn = __ldg(p.qlen + seq);
+        const int64_t tok0 = __ldg(p.cu_q + seq);
+        const int rows_total = qn * p.group;
+        const int r0 = grp * R;
+        const int nrows = min(R, rows_total - r0);
+        const int64_t n = (int64_t)c + qn;
+        const int64_t nb = (n + B - 1) / B;
+        const int64_t cblocks = (nb + K - 1) / K;     // blocks per split of this sequence
+
+        // query rows -> registers, pre-scaled into log2 units
+        float qf[R][E];
+        int64_t Pr[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (r < nrows) {
+                const int row = r0 + r;
+                const int j = row / p.group, hh = row - (row / p.group) * p.group;
+                Pr[r] = (int64_t)c + j;
+                const T *qp = reinterpret_cast<const T *>(p.q) +
+                              ((tok0 + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D + sub * E;
+                load_f<T, E>(qp, qf[r]);
+#pragma unroll
+                for (int e = 0; e < E; ++e) qf[r][e] *= p.scale_log2;
+            } else {
+                Pr[r] = -1;
+#pragma unroll
+                for (int e = 0; e < E; ++e) qf[r][e] = 0.f;
+            }
+        }
+        const int64_t Pmax = (int64_t)c + (r0 + nrows - 1) / p.group;
+        const int64_t nb_lim = (Pmax + B) / B;                  // blocks holding keys 0..Pmax
+        const int64_t st_lo = (int64_t)chunk * cblocks * spb;
+        int64_t st_hi = (int64_t)(chunk + 1) * cblocks * spb;
+        const int64_t st_need = (Pmax + kStageTokens) / kStageTokens;
+        if (st_hi > st_need) st_hi = st_need;
+
+        float m[R], l[R], acc[R][E];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            m[r] = -INFINITY;
+            l[r] = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
+        }
+
+        const int32_t *bt_row = p.bt + (int64_t)seq * p.max_blocks;
+        int64_t wbase = -1000000;
+        int32_t win = 0;
+        bool timed_out = false;
+        int64_t st_issue = st_lo;
+
+        auto issue = [&](int64_t st) {
+            const int64_t b = st / spb;
+            if (b >= wbase + 32 || b < wbase) {
+                wbase = b;
+                win = (wbase + lane < nb_lim) ? __ldg(bt_row + wbase + lane) : 0;
+            }
+            int32_t phys = __shfl_sync(0xffffffffu, win, (int)(b - wbase));
+            if (phys < 0 || (int64_t)phys >= p.num_blocks) {
+                if (lane == 0) report(p.status, PA_DEV_BAD_BLOCK_ID);
+                phys = 0;
+            }
+            if (lane == 0) {
+                const uint32_t slot = issued % NST;
+                const int64_t off =
+                    (int64_t)phys * p.block_stride +
+                    ((int64_t)kvh * B + (int64_t)(st - b * spb) * kStageTokens) * D;
+                unsigned char *dst = ring + (size_t)slot * 2 * kRunBytes;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&bars[slot], 2 * kRunBytes);
+                bulk_g2s(dst, p.k + off * sizeof(T), kRunBytes, &bars[slot]);
+                bulk_g2s(dst + kRunBytes, p.v + off * sizeof(T), kRunBytes, &bars[slot]);
+            }
+            ++issued;
+        };
+
+        while (st_issue < st_hi && issued - consumed < (uint32_t)NST) issue(st_issue++);
+
+        for (int64_t st = st_lo; st < st_hi; ++st) {
+            const uint32_t slot = consumed % NST;
+            if (!mbar_wait(&bars[slot], (consumed / NST) & 1u)) {
+                timed_out = true;
+                break;
+            }
+            const T *sk = reinterpret_cast<const T *>(ring + (size_t)slot * 2 * kRunBytes);
+            const T *sv = reinterpret_cast<const T *>(ring + (size_t)slot * 2 * kRunBytes + kRunBytes);
+            const int64_t p0 = st * kStageTokens;
+
+            float s[R][kStageTokens / 2];
+#pragma unroll
+            for (int i = 0; i < kStageTokens / 2; ++i) {
+                const int key = 2 * i + half;
+                float kf[E];
+                load_f<T, E>(sk + key * D + sub * E, kf);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float dot = 0.f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) dot = fmaf(qf[r][e], kf[e], dot);
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 8);
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                    s[r][i] = (p0 + key <= Pr[r]) ? dot : -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < kStageTokens / 2; ++i) mx = fmaxf(mx, s[r][i]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mnew = fmaxf(m[r], mx);
+                const float mref = (mnew == -INFINITY) ? 0.f : mnew;
+                const float alpha = exp2f(m[r] - mref);
+                float ps = 0.f;
+#pragma unroll
+                for (int i = 0; i < kStageTokens / 2; ++i) {
+                    s[r][i] = exp2f(s[r][i] - mref);
+                    ps += s[r][i];
+                }
+                l[r] = l[r] * alpha + ps;
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[r][e] *= alpha;
+                m[r] = mnew;
+            }
+#pragma unroll
+            for (int i = 0; i < kStageTokens / 2; ++i) {
+                const int key = 2 * i + half;
+                if (p0 + key > Pmax) continue;        // never read slots past the last query
+                float vf[E];
+                load_f<T, E>(sv + key * D + sub * E, vf);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[r][e] = fmaf(s[r][i], vf[e], acc[r][e]);
+            }
+            __syncwarp();
+            ++consumed;
+            if (st_issue < st_hi) issue(st_issue++);
+        }
+
+        if (timed_out) {
+            if (lane == 0) report(p.status, PA_DEV_TIMEOUT);
+            // let the copies already in flight land before the warp leaves
+            while (consumed < issued) {
+                mbar_wait(&bars[consumed % NST], (consumed / NST) & 1u);
+                ++consumed;
+            }
+            return;
+        }
+
+        // merge the two half-warps (alternate keys)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            l[r] += __shfl_xor_sync(0xffffffffu, l[r], 16);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], 16);
+        }
+        if (K == 1) {
+            if (half == 0) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r >= nrows) continue;
+                    const int row = r0 + r;
+                    const int j = row / p.group, hh = row - (row / p.group) * p.group;
+                    const float inv = 1.f / l[r];
+                    float o[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) o[e] = acc[r][e] * inv;
+                    T *op = reinterpret_cast<T *>(p.out) +
+                            ((tok0 + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D + sub * E;
+                    store_f<T, E>(op, o);
+                }
+            }
+        } else {
+            const int64_t part = (int64_t)__ldg(p.parts_cu + seq) + local;
+            if (half == 0) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r >= nrows) continue;
+                    float *po = p.parts_o + ((part * R + r) * D + sub * E);
+#pragma unroll
+                    for (int e = 0; e < E; e += 4)
+                        *reinterpret_cast<float4 *>(po + e) =
+                            make_float4(acc[r][e], acc[r][e + 1], acc[r][e + 2], acc[r][e + 3]);
+                    if (sub == 0) p.parts_ml[part * R + r] = make_float2(m[r], l[r]);
+                }
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------------------------
+// Split combine: one warp per (sequence, KV head, row group, row) whose KV range was split.
+// out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k, M = max_k m_k.
+// ----------------------------------------------------------------------------------------------
+struct CombineParams {
+    char *out;
+    const int32_t *qlen, *cu_q, *parts_cu, *comb_cu, *groups, *nchunk;
+    const uint32_t *counters;
+    const float2 *parts_ml;
+    const float *parts_o;
+    int num_seqs, q_heads, group, rows;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
+    constexpr int E = D / 32;
+    const int lane = threadIdx.x & 31;
+    const uint32_t total = p.counters[kCombTotal];
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < total;
+         u += warps) {
+        const int seq = find_owner(p.comb_cu, p.num_seqs, (int)u);
+        const int local = (int)u - __ldg(p.comb_cu + seq);
+        const int r = local % p.rows;
+        const int rest = local / p.rows;
+        const int G = __ldg(p.groups + seq);
+        const int grp = rest % G;
+        const int kvh = rest / G;
+        const int row = grp * p.rows + r;
+        if (row >= __ldg(p.qlen + seq) * p.group) continue;
+        const int K = __ldg(p.nchunk + seq);
+        const int64_t base = (int64_t)__ldg(p.parts_cu + seq) + (int64_t)(kvh * G + grp) * K;
+        float M = -INFINITY;
+        for (int k = 0; k < K; ++k) M = fmaxf(M, p.parts_ml[(base + k) * p.rows + r].x);
+        float L = 0.f, o[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = 0.f;
+        for (int k = 0; k < K; ++k) {
+            const float2 ml = p.parts_ml[(base + k) * p.rows + r];
+            const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+            L += w * ml.y;
+            const float *po = p.parts_o + ((base + k) * p.rows + r) * D + lane * E;
+            float x[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) x[e] = po[e];
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] = fmaf(w, x[e], o[e]);
+        }
+        const float inv = 1.f / L;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] *= inv;
+        const int j = row / p.group, hh = row - (row / p.group) * p.group;
+        T *op = reinterpret_cast<T *>(p.out) +
+                (((int64_t)__ldg(p.cu_q + seq) + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D +
+                lane * E;
+        if constexpr (E * sizeof(T) >= 8) {
+            store_f<T, E>(op, o);
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) op[e] = Elem<T>::from_f(o[e]);
+        }
+    }
+}
+
+template <typename T, int D, int R>
+cudaError_t launch_simt_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s) {
+    SimtParams p = p0;
+    const size_t run = (size_t)kStageTokens * D * sizeof(T);
+    const size_t stage = 2 * run;
+    const size_t budget = 200 * 1024;
+    int nst = stage <= 8192 ? 3 : 2;
+    int warps = (int)(budget / (nst * stage));
+    if (warps > 8) warps = 8;
+    if (warps < 1) {
+        nst = 2;
+        warps = 1;
+    }
+    p.nst = nst;
+    p.bar_bytes = (int)align_up((size_t)warps * nst * sizeof(uint64_t), 128);
+    const size_t smem = p.bar_bytes + (size_t)warps * nst * stage;
+    auto kern = simt_attention_kernel<T, D, R>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, warps * 32, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    kern<<<a.num_sms * per_sm, warps * 32, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_simt_rows(const FwdArgs &a, const SimtParams &p, cudaStream_t s) {
+    switch (a.lay.rows_per_item) {
+    case 1: return launch_simt_t<T, D, 1>(a, p, s);
+    case 2: return launch_simt_t<T, D, 2>(a, p, s);
+    default: return launch_simt_t<T, D, 4>(a, p, s);
+    }
+}
+
+template <typename T>
+cudaError_t launch_simt_dim(const FwdArgs &a, const SimtParams &p, cudaStream_t s) {
+    return a.dims.head_dim == 64 ? launch_simt_rows<T, 64>(a, p, s) : launch_simt_rows<T, 128>(a, p, s);
+}
+
+template <typename T, int D>
+cudaError_t launch_combine_t(const FwdArgs &a, const CombineParams &p, cudaStream_t s) {
+    combine_kernel<T, D><<<a.num_sms * 4, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_combine_dim(const FwdArgs &a, const CombineParams &p, cudaStream_t s) {
+    return a.dims.head_dim == 64 ? launch_combine_t<T, 64>(a, p, s) : launch_combine_t<T, 128>(a, p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const FwdArgs &a, cudaStream_t s) {
+    PlanParams p;
+    const WsLayout &L = a.lay;
+    p.ctx = a.ctx;
+    p.qlen = a.qlen;
+    p.counters = reinterpret_cast<uint32_t *>(a.ws + L.counters);
+    p.cu_q = reinterpret_cast<int32_t *>(a.ws + L.cu_q);
+    p.simt_cu = reinterpret_cast<int32_t *>(a.ws + L.simt_cu);
+    p.parts_cu = reinterpret_cast<int32_t *>(a.ws + L.parts_cu);
+    p.comb_cu = reinterpret_cast<int32_t *>(a.ws + L.comb_cu);
+    p.groups = reinterpret_cast<int32_t *>(a.ws + L.groups);
+    p.nchunk = reinterpret_cast<int32_t *>(a.ws + L.nchunk);
+    p.tc_cu = reinterpret_cast<int32_t *>(a.ws + L.tc_cu);
+    p.tc_seq = reinterpret_cast<int32_t *>(a.ws + L.tc_seq);
+    p.status = a.status;
+    p.total_q = a.dims.total_q;
+    p.max_parts = L.max_parts;
+    p.num_seqs = a.dims.num_seqs;
+    p.kv_heads = a.dims.num_kv_heads;
+    p.group = a.dims.num_q_heads / a.dims.num_kv_heads;
+    p.block_size = a.dims.block_size;
+    p.max_blocks = a.dims.max_blocks_per_seq;
+    p.rows = L.rows_per_item;
+    p.tc = a.tc ? 1 : 0;
+    p.total_warps = a.num_sms * 8;
+    plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_simt(const FwdArgs &a, cudaStream_t s) {
+    const WsLayout &L = a.lay;
+    SimtParams p;
+    p.q = static_cast<const char *>(a.q);
+    p.k = static_cast<const char *>(a.k);
+    p.v = static_cast<const char *>(a.v);
+    p.out = static_cast<char *>(a.out);
+    p.bt = a.bt;
+    p.ctx = a.ctx;
+    p.qlen = a.qlen;
+    p.cu_q = reinterpret_cast<const int32_t *>(a.ws + L.cu_q);
+    p.simt_cu = reinterpret_cast<const int32_t *>(a.ws + L.simt_cu);
+    p.parts_cu = reinterpret_cast<const int32_t *>(a.ws + L.parts_cu);
+    p.groups = reinterpret_cast<const int32_t *>(a.ws + L.groups);
+    p.nchunk = reinterpret_cast<const int32_t *>(a.ws + L.nchunk);
+    p.counters = reinterpret_cast<uint32_t *>(a.ws + L.counters);
+    p.parts_ml = reinterpret_cast<float2 *>(a.ws + L.parts_ml);
+    p.parts_o = reinterpret_cast<float *>(a.ws + L.parts_o);
+    p.status = a.status;
+    p.num_blocks = a.dims.num_blocks;
+    const int64_t dflt = (int64_t)a.dims.num_kv_heads * a.dims.block_size * a.dims.head_dim;
+    p.block_stride = a.dims.kv_block_stride ? a.dims.kv_block_stride : dflt;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.num_seqs = a.dims.num_seqs;
+    p.q_heads = a.dims.num_q_heads;
+    p.kv_heads = a.dims.num_kv_heads;
+    p.group = a.dims.num_q_heads / a.dims.num_kv_heads;
+    p.block_size = a.dims.block_size;
+    p.max_blocks = a.dims.max_blocks_per_seq;
+    switch (a.dims.dtype) {
+    case PA_F32: return launch_simt_dim<float>(a, p, s);
+    case PA_BF16: return launch_simt_dim<__nv_bfloat16>(a, p, s);
+    default: return launch_simt_dim<__half>(a, p, s);
+    }
+}
+
+cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s) {
+    const WsLayout &L = a.lay;
+    CombineParams p;
+    p.out = static_cast<char *>(a.out);
+    p.qlen = a.qlen;
+    p.cu_q = reinterpret_cast<const int32_t *>(a.ws + L.cu_q);
+    p.parts_cu = reinterpret_cast<const int32_t *>(a.ws + L.parts_cu);
+    p.comb_cu = reinterpret_cast<const int32_t *>(a.ws + L.comb_cu);
+    p.groups = reinterpret_cast<const int32_t *>(a.ws + L.groups);
+    p.nchunk = reinterpret_cast<const int32_t *>(a.ws + L.nchunk);
+    p.counters = reinterpret_cast<const uint32_t *>(a.ws + L.counters);
+    p.parts_ml = reinterpret_cast<const float2 *>(a.ws + L.parts_ml);
+    p.parts_o = reinterpret_cast<const float *>(a.ws + L.parts_o);
+    p.num_seqs = a.dims.num_seqs;
+    p.q_heads = a.dims.num_q_heads;
+    p.group = a.dims.num_q_heads / a.dims.num_kv_heads;
+    p.rows = L.rows_per_item;
+    switch (a.dims.dtype) {
+    case PA_F32: return launch_combine_dim<float>(a, p, s);
+    case PA_BF16: return launch_combine_dim<__nv_bfloat16>(a, p, s);
+    default: return launch_combine_dim<__half>(a, p, s);
+    }
+}
+
+}  // namespace pkv

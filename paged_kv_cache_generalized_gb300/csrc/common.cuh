@@ -1,0 +1,159 @@
+// Device helpers shared by the libpagedkv kernels (sm_103a): element conversion, mbarrier and
+// bulk-copy PTX wrappers, bounded waits, the device status word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+// A bounded wait gives up after this many nanoseconds of %globaltimer and reports
+// PA_DEV_TIMEOUT instead of spinning forever.
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
+
+__device__ __forceinline__ void report(unsigned *status, unsigned bits) {
+    if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- element conversion -------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float to_f(float x) { return x; }
+    static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+template <> struct Elem<__half> {
+    static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+    static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+
+// Loads N consecutive elements (N * sizeof(T) a multiple of 8 bytes, naturally aligned to the
+// vector width) from shared or global memory and widens them to float.  16-byte multiples use
+// 128-bit accesses.
+template <typename T, int N>
+__device__ __forceinline__ void load_f(const T *p, float (&out)[N]) {
+    constexpr int kBytes = N * sizeof(T);
+    static_assert(kBytes % 8 == 0, "vector width");
+    if constexpr (kBytes % 16 == 0) {
+        uint4 raw[kBytes / 16];
+#pragma unroll
+        for (int w = 0; w < kBytes / 16; ++w) raw[w] = reinterpret_cast<const uint4 *>(p)[w];
+        const T *e = reinterpret_cast<const T *>(raw);
+#pragma unroll
+        for (int i = 0; i < N; ++i) out[i] = Elem<T>::to_f(e[i]);
+    } else {
+        uint2 raw[kBytes / 8];
+#pragma unroll
+        for (int w = 0; w < kBytes / 8; ++w) raw[w] = reinterpret_cast<const uint2 *>(p)[w];
+        const T *e = reinterpret_cast<const T *>(raw);
+#pragma unroll
+        for (int i = 0; i < N; ++i) out[i] = Elem<T>::to_f(e[i]);
+    }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void store_f(T *p, const float (&in)[N]) {
+    constexpr int kBytes = N * sizeof(T);
+    static_assert(kBytes % 8 == 0, "vector width");
+    if constexpr (kBytes % 16 == 0) {
+        uint4 raw[kBytes / 16];
+        T *e = reinterpret_cast<T *>(raw);
+#pragma unroll
+        for (int i = 0; i < N; ++i) e[i] = Elem<T>::from_f(in[i]);
+#pragma unroll
+        for (int w = 0; w < kBytes / 16; ++w) reinterpret_cast<uint4 *>(p)[w] = raw[w];
+    } else {
+        uint2 raw[kBytes / 8];
+        T *e = reinterpret_cast<T *>(raw);
+#pragma unroll
+        for (int i = 0; i < N; ++i) e[i] = Elem<T>::from_f(in[i]);
+#pragma unroll
+        for (int w = 0; w < kBytes / 8; ++w) reinterpret_cast<uint2 *>(p)[w] = raw[w];
+    }
+}
+
+// ---- mbarrier ---------------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete; false after kWaitTimeoutNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+    }
+}
+
+// ---- bulk (non-tensor) async copy global -> shared, completion on an mbarrier -------------------
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before later async-proxy
+// (bulk copy / tensor core) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+}  // namespace pkv

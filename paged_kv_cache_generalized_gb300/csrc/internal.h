@@ -1,0 +1,89 @@
+// Internal interface between the C-ABI entry points (api.cu) and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+// Query rows handled by one CUDA-core work item: (token, head-in-group) pairs of one KV head.
+// Chosen per call from the GQA group size.
+constexpr int kMaxRowsPerItem = 4;
+// Multi-token sequences with at least this many query rows per KV head (q_len * g) go to the
+// tensor-core kernel when it supports the dtype and head_dim.
+constexpr int kTcMinRows = 16;
+// Rows of one tensor-core tile (UMMA M).
+constexpr int kTcTileRows = 128;
+// Upper bound on the KV splits of one CUDA-core work item's rows.
+constexpr int kMaxSplits = 64;
+
+// Counters at the start of the workspace.
+enum Counter : int {
+    kSimtNext = 0,    // next CUDA-core item to take
+    kSimtTotal = 1,   // number of CUDA-core items
+    kTcNext = 2,      // next tensor-core tile to take
+    kTcTotal = 3,     // number of tensor-core tiles
+    kCombTotal = 4,   // number of split-KV rows to combine
+    kChunkBlocks = 5, // KV blocks per CUDA-core split
+    kNumCounters = 16
+};
+
+// Byte offsets of the workspace regions (all 256-byte aligned).
+struct WsLayout {
+    size_t counters;   // uint32 [kNumCounters]
+    size_t cu_q;       // int32 [S+1]  exclusive prefix of q_lens
+    size_t simt_cu;    // int32 [S+1]  prefix of CUDA-core items
+    size_t parts_cu;   // int32 [S+1]  prefix of split partial records
+    size_t comb_cu;    // int32 [S+1]  prefix of rows to combine
+    size_t groups;     // int32 [S]    row groups per KV head (CUDA-core sequences)
+    size_t nchunk;     // int32 [S]    KV splits per row group (CUDA-core sequences)
+    size_t tc_cu;      // int32 [S+1]  prefix of tensor-core tiles over sequences in rank order
+    size_t tc_seq;     // int32 [S]    sequence at each rank
+    size_t parts_ml;   // float2 [max_parts * R]  (running max in log2 units, sum)
+    size_t parts_o;    // float  [max_parts * R * d]
+    size_t total;
+    int64_t max_parts;
+    int rows_per_item; // R
+};
+
+WsLayout ws_layout(const pa_dims &d);
+int rows_per_item(const pa_dims &d);
+bool tc_supported(const pa_dims &d);
+
+struct FwdArgs {
+    pa_dims dims;
+    const void *q;
+    const void *k;
+    const void *v;
+    void *out;
+    const int32_t *bt;
+    const int32_t *ctx;
+    const int32_t *qlen;
+    float scale;
+    char *ws;
+    WsLayout lay;
+    unsigned *status;
+    int num_sms;
+    bool tc;            // tensor-core kernel available for this call
+    bool maybe_prefill; // some sequence may have q_len > 1
+};
+
+cudaError_t launch_plan(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_simt(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s);
+
+cudaError_t launch_kv_append(const kv_append_dims &d, const void *k_new, const void *v_new,
+                             const int64_t *slots, void *k_cache, void *v_cache, unsigned *status,
+                             int num_sms, cudaStream_t s);
+cudaError_t launch_block_copy(const block_copy_dims &d, const void *src, void *dst,
+                              const int64_t *pairs, unsigned *status, int num_sms,
+                              cudaStream_t s);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
+
+}  // namespace pkv

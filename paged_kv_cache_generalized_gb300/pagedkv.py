@@ -1,0 +1,236 @@
+"""Thin Python binding of libpagedkv.so (ctypes): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; PyTorch supplies device memory, the
+workspace allocation and the current stream.  There is no CPU fallback: if the library has not
+been built (``paged_kv_cache_generalized_gb300.build.build()``) every call raises.
+
+The functions mirror the C ABI in ``include/pagedkv.h`` (same names and semantics).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+PA_OK = 0
+STATUS_BITS = {
+    0x1: "PA_DEV_BAD_BLOCK_ID",
+    0x2: "PA_DEV_BAD_LENGTHS",
+    0x4: "PA_DEV_BAD_SLOT",
+    0x8: "PA_DEV_BAD_PAIR",
+    0x10: "PA_DEV_TIMEOUT",
+}
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+_ELEM = {torch.float32: 4, torch.bfloat16: 2, torch.float16: 2}
+
+EXPORTED = ("pa_forward_workspace_size", "pa_forward", "kv_append", "block_copy",
+            "pa_get_device_status", "pa_status_string", "pa_version")
+
+
+class PaDims(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("num_seqs", ctypes.c_int32), ("total_q", ctypes.c_int64),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int64), ("max_blocks_per_seq", ctypes.c_int32),
+                ("kv_block_stride", ctypes.c_int64)]
+
+
+class KvAppendDims(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("num_tokens", ctypes.c_int64),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64),
+                ("kv_block_stride", ctypes.c_int64), ("num_layers", ctypes.c_int32),
+                ("new_layer_stride", ctypes.c_int64), ("cache_layer_stride", ctypes.c_int64)]
+
+
+class BlockCopyDims(ctypes.Structure):
+    _fields_ = [("block_bytes", ctypes.c_int64), ("num_planes", ctypes.c_int32),
+                ("src_plane_stride", ctypes.c_int64), ("dst_plane_stride", ctypes.c_int64),
+                ("src_block_stride", ctypes.c_int64), ("dst_block_stride", ctypes.c_int64),
+                ("src_num_blocks", ctypes.c_int64), ("dst_num_blocks", ctypes.c_int64),
+                ("num_pairs", ctypes.c_int64)]
+
+
+class PagedKVError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Loads libpagedkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB_PATH
+    if not os.path.exists(path):
+        raise PagedKVError(f"libpagedkv.so not found at {path}: build it first "
+                           "(paged_kv_cache_generalized_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    P, sz = ctypes.c_void_p, ctypes.c_size_t
+    lib.pa_forward_workspace_size.restype = sz
+    lib.pa_forward_workspace_size.argtypes = [ctypes.POINTER(PaDims)]
+    lib.pa_forward.restype = ctypes.c_int
+    lib.pa_forward.argtypes = [ctypes.POINTER(PaDims), P, P, P, P, P, P, ctypes.c_float, P, P, sz, P]
+    lib.kv_append.restype = ctypes.c_int
+    lib.kv_append.argtypes = [ctypes.POINTER(KvAppendDims), P, P, P, P, P, P]
+    lib.block_copy.restype = ctypes.c_int
+    lib.block_copy.argtypes = [ctypes.POINTER(BlockCopyDims), P, P, P, P]
+    lib.pa_get_device_status.restype = ctypes.c_int
+    lib.pa_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_status_string.argtypes = [ctypes.c_int]
+    lib.pa_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, what: str):
+    if rc != PA_OK:
+        name = load_library().pa_status_string(rc).decode()
+        raise PagedKVError(f"{what} failed: {name}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _cache_geometry(cache: torch.Tensor):
+    """[num_blocks, Hkv, B, d] view (the block dim may be strided, e.g. a block-first pool)."""
+    if cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    nb, hkv, bs, d = cache.shape
+    if cache.stride(3) != 1 or cache.stride(2) != d or cache.stride(1) != bs * d:
+        raise ValueError("cache: the (head, slot, dim) dims of a block must be contiguous")
+    return nb, hkv, bs, d, cache.stride(0)
+
+
+def forward_dims(q, k_cache, block_tables, ctx_lens) -> PaDims:
+    nb, hkv, bs, d, bstride = _cache_geometry(k_cache)
+    T, hq, dq = q.shape
+    if dq != d:
+        raise ValueError("q and cache head_dim differ")
+    return PaDims(_DTYPES[q.dtype], ctx_lens.shape[0], T, hq, hkv, d, bs, nb,
+                  block_tables.shape[1], bstride)
+
+
+def forward_workspace_size(q, k_cache, block_tables, ctx_lens) -> int:
+    dims = forward_dims(q, k_cache, block_tables, ctx_lens)
+    return int(load_library().pa_forward_workspace_size(ctypes.byref(dims)))
+
+
+def pa_forward(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale=None, out=None,
+               workspace=None, stream=None):
+    """Generalized paged attention (see ``pa_forward`` in include/pagedkv.h).
+
+    q: [T, Hq, d]; k_cache/v_cache: [num_blocks, Hkv, B, d] (same dtype as q); block_tables:
+    int32 [S, max_blocks]; ctx_lens/q_lens: int32 [S].  Returns ``out`` ([T, Hq, d])."""
+    lib = load_library()
+    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
+        raise ValueError("k_cache and v_cache must have the same shape and strides")
+    for t in (k_cache, v_cache):
+        if t.dtype != q.dtype:
+            raise ValueError("q and caches must share a dtype")
+    for t in (block_tables, ctx_lens, q_lens):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError("block_tables, ctx_lens and q_lens must be contiguous int32")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous [T, Hq, d]")
+    dims = forward_dims(q, k_cache, block_tables, ctx_lens)
+    if scale is None:
+        scale = 1.0 / float(dims.head_dim) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    need = int(lib.pa_forward_workspace_size(ctypes.byref(dims)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.pa_forward(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                        _ptr(block_tables), _ptr(ctx_lens), _ptr(q_lens), ctypes.c_float(scale),
+                        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                        _stream(stream))
+    _check(rc, "pa_forward")
+    return out
+
+
+def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
+    """Writes new tokens' K/V into their slots (see ``kv_append`` in include/pagedkv.h).
+
+    Single layer: k_new [T, Hkv, d], caches [num_blocks, Hkv, B, d].  Several layers: k_new
+    [L, T, Hkv, d], caches [L, num_blocks, Hkv, B, d] (layer and block dims may be strided)."""
+    lib = load_library()
+    if k_new.dim() == 3:
+        k_new, v_new, k_cache, v_cache = (x.unsqueeze(0) for x in (k_new, v_new, k_cache, v_cache))
+    L, T, hkv, d = k_new.shape
+    if k_cache.shape[0] != L or v_cache.shape != k_cache.shape or v_new.shape != k_new.shape:
+        raise ValueError("kv_append: inconsistent shapes")
+    if k_cache.stride() != v_cache.stride() or k_new.stride() != v_new.stride():
+        raise ValueError("kv_append: K and V must share strides")
+    nb, hkv_c, bs, dc, bstride = _cache_geometry(k_cache[0])
+    if (hkv_c, dc) != (hkv, d):
+        raise ValueError("kv_append: cache and new tokens disagree on heads or head_dim")
+    if k_new.stride(3) != 1 or k_new.stride(2) != d or k_new.stride(1) != hkv * d:
+        raise ValueError("kv_append: each layer of k_new must be contiguous [T, Hkv, d]")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous int64")
+    dims = KvAppendDims(_DTYPES[k_new.dtype], T, hkv, d, bs, nb, bstride, L,
+                        k_new.stride(0) if L > 1 else 0, k_cache.stride(0) if L > 1 else 0)
+    rc = lib.kv_append(ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                       _ptr(k_cache), _ptr(v_cache), _stream(stream))
+    _check(rc, "kv_append")
+
+
+def block_copy(src, dst, pairs, stream=None):
+    """Copies whole blocks of every plane (see ``block_copy`` in include/pagedkv.h).
+
+    src/dst: [planes, num_blocks, ...] (each block's trailing dims contiguous; src or dst may be
+    pinned host memory); pairs: int64 [P, 2] (source block, destination block) on the device."""
+    lib = load_library()
+    if src.dim() < 2 or dst.dim() < 2 or src.shape[0] != dst.shape[0]:
+        raise ValueError("block_copy: src and dst must be [planes, num_blocks, ...] with equal planes")
+    if src.shape[2:] != dst.shape[2:] or src.dtype != dst.dtype:
+        raise ValueError("block_copy: block shapes differ")
+    es = src.element_size()
+    block_elems = 1
+    for x in src.shape[2:]:
+        block_elems *= x
+    for t in (src, dst):
+        if not t[0, 0].is_contiguous():
+            raise ValueError("block_copy: each block must be contiguous")
+    if pairs.dtype != torch.int64 or not pairs.is_contiguous():
+        raise ValueError("pairs must be contiguous int64 [P, 2]")
+    dims = BlockCopyDims(block_elems * es, src.shape[0], src.stride(0) * es, dst.stride(0) * es,
+                         src.stride(1) * es, dst.stride(1) * es, src.shape[1], dst.shape[1],
+                         pairs.numel() // 2)
+    rc = lib.block_copy(ctypes.byref(dims), _ptr(src), _ptr(dst), _ptr(pairs), _stream(stream))
+    _check(rc, "block_copy")
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream, returns and clears the device status bits (0 = no fault seen)."""
+    lib = load_library()
+    flags = ctypes.c_uint32(0)
+    rc = lib.pa_get_device_status(ctypes.byref(flags), _stream(stream))
+    if rc not in (0, 5):
+        _check(rc, "pa_get_device_status")
+    return int(flags.value)
+
+
+def status_names(flags: int):
+    return [n for b, n in STATUS_BITS.items() if flags & b]
+
+
+def version() -> str:
+    return load_library().pa_version().decode()

@@ -1,0 +1,132 @@
+"""The C ABI without a GPU: the library loads, exports every function include/pagedkv.h declares,
+and rejects bad arguments on the host (before any CUDA call) with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_generalized_gb300 import build, pagedkv
+
+    build.build()
+    return pagedkv.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("pa_forward", "pa_forward_workspace_size", "kv_append", "block_copy",
+              "pa_get_device_status", "pa_status_string", "pa_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), f"libpagedkv.so does not export {n}"
+
+
+def test_binding_names_match_the_header():
+    from paged_kv_cache_generalized_gb300 import pagedkv
+
+    assert set(pagedkv.EXPORTED) <= set(_declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    for code, name in enumerate(["PA_OK", "PA_ERR_INVALID_ARG", "PA_ERR_UNSUPPORTED",
+                                 "PA_ERR_WORKSPACE", "PA_ERR_CUDA", "PA_ERR_DEVICE"]):
+        assert lib.pa_status_string(code).decode() == name
+    assert "sm_103a" in lib.pa_version().decode()
+
+
+def _dims(**kw):
+    from paged_kv_cache_generalized_gb300.pagedkv import PaDims
+
+    base = dict(dtype=1, num_seqs=2, total_q=3, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                block_size=16, num_blocks=10, max_blocks_per_seq=4, kv_block_stride=0)
+    base.update(kw)
+    return PaDims(**base)
+
+
+def test_workspace_size_is_host_only(lib):
+    assert lib.pa_forward_workspace_size(ctypes.byref(_dims())) > 0
+    assert lib.pa_forward_workspace_size(ctypes.byref(_dims(num_q_heads=7))) == 0
+    big = lib.pa_forward_workspace_size(ctypes.byref(_dims(num_seqs=64, total_q=64, max_blocks_per_seq=257)))
+    assert big >= 64 * 2 * 64 * 4 * 128 * 4          # split partials: heads x seqs x splits x rows x d
+
+
+FAKE = ctypes.c_void_p(0x10000)   # 256-byte aligned, never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_q_heads=6, num_kv_heads=4), 1),   # Hq % Hkv != 0
+    (dict(head_dim=96), 2),                     # unsupported head_dim
+    (dict(block_size=8), 2),                    # unsupported block size
+    (dict(dtype=7), 1),                         # unknown dtype
+    (dict(total_q=1), 1),                       # fewer rows than sequences
+    (dict(kv_block_stride=100), 1),             # block stride smaller than a block
+])
+def test_forward_rejects_bad_dims(lib, kw, code):
+    d = _dims(**kw)
+    rc = lib.pa_forward(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.1),
+                        ctypes.c_void_p(0x20000), FAKE, 1 << 30, None)
+    assert rc == code
+
+
+def test_forward_rejects_small_or_missing_workspace(lib):
+    d = _dims()
+    need = lib.pa_forward_workspace_size(ctypes.byref(d))
+    args = [ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.1),
+            ctypes.c_void_p(0x20000)]
+    assert lib.pa_forward(*args, FAKE, need - 1, None) == 3
+    assert lib.pa_forward(*args, None, need, None) == 3
+    assert lib.pa_forward(*args, ctypes.c_void_p(0x10010), need, None) == 3   # not 256-aligned
+
+
+def test_forward_rejects_null_and_misaligned_pointers(lib):
+    d = _dims()
+    rc = lib.pa_forward(ctypes.byref(d), None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.1),
+                        ctypes.c_void_p(0x20000), FAKE, 1 << 30, None)
+    assert rc == 1
+    rc = lib.pa_forward(ctypes.byref(d), ctypes.c_void_p(0x10008), FAKE, FAKE, FAKE, FAKE, FAKE,
+                        ctypes.c_float(0.1), ctypes.c_void_p(0x20000), FAKE, 1 << 30, None)
+    assert rc == 1
+    # out aliasing q
+    rc = lib.pa_forward(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.1),
+                        FAKE, ctypes.c_void_p(0x40000), 1 << 30, None)
+    assert rc == 1
+
+
+def test_append_and_copy_reject_bad_arguments(lib):
+    from paged_kv_cache_generalized_gb300.pagedkv import BlockCopyDims, KvAppendDims
+
+    a = KvAppendDims(dtype=1, num_tokens=4, num_kv_heads=2, head_dim=4, block_size=16,
+                     num_blocks=8, kv_block_stride=0, num_layers=1, new_layer_stride=0,
+                     cache_layer_stride=0)
+    # a row of 4 bf16 (8 bytes) is not a whole number of 16-byte vectors
+    assert lib.kv_append(ctypes.byref(a), FAKE, FAKE, FAKE, FAKE, FAKE, None) == 2
+    a.head_dim = 64
+    assert lib.kv_append(ctypes.byref(a), None, FAKE, FAKE, FAKE, FAKE, None) == 1
+    a.num_tokens = 0                                   # empty append is a no-op
+    assert lib.kv_append(ctypes.byref(a), None, None, None, None, None, None) == 0
+    c = BlockCopyDims(block_bytes=100, num_planes=1, src_plane_stride=0, dst_plane_stride=0,
+                      src_block_stride=0, dst_block_stride=0, src_num_blocks=4, dst_num_blocks=4,
+                      num_pairs=1)
+    assert lib.block_copy(ctypes.byref(c), FAKE, FAKE, FAKE, None) == 1    # not a multiple of 16
+    c.block_bytes = 4096
+    c.num_pairs = 0
+    assert lib.block_copy(ctypes.byref(c), None, None, None, None) == 0   # no pairs: no-op
+    c.num_pairs = 2
+    assert lib.block_copy(ctypes.byref(c), ctypes.c_void_p(0x10004), FAKE, FAKE, None) == 1

@@ -1,0 +1,172 @@
+"""GPU parity of pa_forward against the float64 oracle (through the C ABI).
+
+Small cases are compared row by row in full (several KV tiles, ragged tails, every dtype, head
+dim, block size and GQA group the library supports).  The benchmark-sized configurations are
+compared on sampled rows, including every sequence's last token (the longest causal range).
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_generalized_gb300 as pkg
+from paged_kv_cache_generalized_gb300 import workloads as W
+
+from gpu_util import (as_f64, assert_close, batch_to_dev, gather_rows, run_forward, sample_rows,
+                      to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    pkg.device_status()
+    yield
+
+
+def _full_parity(b, threads=8):
+    out = run_forward(b)
+    ref = oracle.paged_attention_batch(b, threads=threads)
+    err = assert_close(as_f64(out), ref, b.dtype, b.name)
+    assert pkg.device_status() == 0
+    return err
+
+
+def test_tiny_config():
+    _full_parity(W.tiny())
+
+
+CASES = [
+    # name, ctx_lens, q_lens, Hq, Hkv, d, B, dtype, layout
+    ("decode_mha_bf16", [512, 1000, 37, 4096, 15, 16], [1] * 6, 8, 8, 128, 16, "bf16", "shuffle"),
+    ("decode_gqa4_bf16", [700, 33, 2000, 0], [1] * 4, 16, 4, 128, 32, "bf16", "shuffle"),
+    ("decode_gqa8_f16", [300, 129, 64], [1] * 3, 16, 2, 128, 16, "f16", "shuffle"),
+    ("decode_d64_f32", [250, 17, 1], [1] * 3, 4, 2, 64, 16, "f32", "shuffle"),
+    ("prefill_mha_bf16", [300, 0, 129], [200, 150, 33], 4, 4, 128, 16, "bf16", "segments"),
+    ("prefill_gqa4_bf16", [1024, 77, 5], [96, 300, 16], 8, 2, 128, 32, "bf16", "shuffle"),
+    ("prefill_short_turns_bf16", [64, 200, 31], [2, 3, 15], 8, 8, 128, 16, "bf16", "shuffle"),
+    ("prefill_d64_bf16", [100, 40], [70, 9], 4, 2, 64, 16, "bf16", "shuffle"),
+    ("prefill_f32", [60, 0], [40, 33], 4, 4, 128, 16, "f32", "shuffle"),
+    ("mixed_gqa_bf16", [500, 100, 2000, 33, 0, 700], [1, 130, 1, 17, 64, 1], 32, 8, 128, 32,
+     "bf16", "shuffle"),
+    ("block64_f16", [200, 70], [1, 90], 8, 4, 128, 64, "f16", "shuffle"),
+    ("block128_bf16", [300, 5], [130, 1], 4, 1, 128, 128, "bf16", "shuffle"),
+    ("exact_block_multiples_bf16", [16, 31, 32, 48], [16, 1, 32, 16], 4, 4, 128, 16, "bf16", "shuffle"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_small_cases_full_parity(case):
+    name, ctx, ql, hq, hkv, d, B, dtype, layout = case
+    b = W.make_attn_batch(name, ctx, ql, hq, hkv, d, B, dtype, seed=zlib.crc32(name.encode()) % 1000,
+                          layout=layout, seg=(32, 160))
+    _full_parity(b)
+
+
+def test_many_sequences_exercise_the_planner():
+    """More sequences than one planner pass (1024 threads) covers; mixed decode and turns."""
+    rng = np.random.default_rng(7)
+    S = 2500
+    ctx = rng.integers(0, 120, S)
+    ql = np.where(rng.random(S) < 0.8, 1, rng.integers(2, 40, S))
+    b = W.make_attn_batch("many", ctx, ql, 8, 2, 64, 16, "bf16", seed=7)
+    out = run_forward(b)
+    rows = sample_rows(b, 3000, seed=1)
+    ref = oracle.paged_attention_batch(b, rows=rows, threads=8)
+    assert_close(gather_rows(out, b, rows), ref, "bf16", "many")
+    assert pkg.device_status() == 0
+
+
+def test_prefix_sharing_aliasing():
+    b = W.make_attn_batch("prefix", [200, 150, 96], [1, 40, 1], 8, 8, 128, 16, "bf16", seed=3,
+                          shared_prefix_blocks=5, slack=0.5)
+    _full_parity(b)
+
+
+def test_nan_poisoned_unread_slots_do_not_leak():
+    """Free blocks and the tails of last blocks hold NaN; block-table padding holds garbage ids."""
+    b = W.make_attn_batch("poison", [45, 0, 300, 17], [1, 37, 100, 1], 8, 2, 128, 16, "bf16",
+                          seed=5, poison=True)
+    bt = b.block_tables.copy()
+    bt[bt < 0] = 2 ** 30
+    b.block_tables = bt
+    _full_parity(b)
+
+
+def test_chunked_turn_matches_one_prefill():
+    """ConvKV turn-level prefix extension: a turn attended in two chunks (append chunk, attend;
+    append next chunk, attend) gives the rows of attending the whole turn at once."""
+    b = W.make_attn_batch("chunked", [500], [200], 8, 2, 128, 16, "bf16", seed=11)
+    d = batch_to_dev(b)
+    full = as_f64(pkg.pa_forward(d["q"], d["k"], d["v"], d["bt"], d["ctx"], d["ql"], b.scale))
+    parts = []
+    for c0, n in ((500, 120), (620, 80)):
+        qq = d["q"][c0 - 500:c0 - 500 + n].contiguous()
+        o = pkg.pa_forward(qq, d["k"], d["v"], d["bt"], torch.tensor([c0], dtype=torch.int32, device="cuda"),
+                           torch.tensor([n], dtype=torch.int32, device="cuda"), b.scale)
+        parts.append(as_f64(o))
+    torch.cuda.synchronize()
+    ref = oracle.paged_attention_batch(b)
+    assert_close(full, ref, "bf16", "whole turn")
+    assert_close(np.concatenate(parts), ref, "bf16", "chunked turn")
+
+
+def test_deterministic():
+    b = W.make_attn_batch("det", [900, 30, 2000], [1, 64, 1], 16, 4, 128, 16, "bf16", seed=13)
+    d = batch_to_dev(b)
+    o1 = run_forward(b, d).clone()
+    o2 = run_forward(b, d)
+    assert torch.equal(o1, o2)
+
+
+def test_bad_block_id_is_flagged_not_trapped():
+    b = W.make_attn_batch("badblk", [100, 100], [1, 1], 4, 4, 128, 16, "bf16", seed=17)
+    bt = b.block_tables.copy()
+    bt[1, 2] = b.num_blocks + 1000
+    b.block_tables = bt
+    out = run_forward(b)
+    flags = pkg.device_status()
+    assert flags & 0x1, pkg.status_names(flags)
+    # the other sequence is unaffected
+    ref = oracle.paged_attention(b.q[:1], b.k_cache, b.v_cache, "bf16", b.block_tables[:1],
+                                 b.ctx_lens[:1], b.q_lens[:1], 4, 4, 128, 16, b.scale)
+    assert_close(as_f64(out[:1]), ref, "bf16", "unaffected sequence")
+
+
+def test_inconsistent_lengths_are_flagged():
+    b = W.make_attn_batch("badlen", [10, 20], [3, 2], 4, 4, 64, 16, "f32", seed=19)
+    d = batch_to_dev(b)
+    d["ql"] = torch.tensor([3, 9], dtype=torch.int32, device="cuda")     # sum != total_q
+    out = torch.full_like(d["q"], 7.0)
+    pkg.pa_forward(d["q"], d["k"], d["v"], d["bt"], d["ctx"], d["ql"], b.scale, out=out)
+    flags = pkg.device_status()
+    assert flags & 0x2
+    assert torch.all(out == 7.0)               # nothing was written
+
+
+# ------------------------------------------------------------------------------------------------
+# Benchmark-sized configurations: sampled rows
+# ------------------------------------------------------------------------------------------------
+
+def _sampled(b, n_rows, seed=0, **kw):
+    d = batch_to_dev(b)
+    out = run_forward(b, d, **kw)
+    rows = sample_rows(b, n_rows, seed=seed)
+    ref = oracle.paged_attention_batch(b, rows=rows, threads=16)
+    err = assert_close(gather_rows(out, b, rows), ref, b.dtype, b.name)
+    assert pkg.device_status() == 0
+    return out, err
+
+
+def test_config_decode13b_full_size():
+    _sampled(W.decode13b(), 512)
+
+
+def test_config_mixed_gqa_full_size():
+    _sampled(W.mixed_gqa(), 384)
+
+
+def test_config_longprefill_full_size():
+    _sampled(W.longprefill(), 128)
