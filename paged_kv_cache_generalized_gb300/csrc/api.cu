@@ -95,9 +95,13 @@ WsLayout ws_layout(const pa_dims &d) {
     L.nchunk = take(S * 4);
     L.tc_cu = take((S + 1) * 4);
     L.tc_seq = take(S * 4);
-    // Only sequences whose rows fit one row group are split, into at most kMaxSplits parts.
+    // Only sequences whose rows fit one row group are split, into at most kMaxSplits parts of at
+    // least C = ceil(work / target) blocks each, so the partial records number at most
+    // sum_i Hkv * ceil(nb_i / C) <= target + Hkv * S.
     const int64_t splits = d.max_blocks_per_seq < kMaxSplits ? d.max_blocks_per_seq : kMaxSplits;
-    L.max_parts = splits > 1 ? (int64_t)d.num_kv_heads * (int64_t)S * splits : 0;
+    int64_t parts = splits > 1 ? (int64_t)d.num_kv_heads * (int64_t)S * splits : 0;
+    const int64_t by_target = kMaxTargetItems + (int64_t)d.num_kv_heads * (int64_t)S;
+    L.max_parts = parts < by_target ? parts : by_target;
     L.rows_per_item = R;
     L.parts_ml = take((size_t)L.max_parts * R * sizeof(float) * 2);
     L.parts_o = take((size_t)L.max_parts * R * d.head_dim * sizeof(float));

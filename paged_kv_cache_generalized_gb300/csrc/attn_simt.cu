@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         __syncthreads();
     }
     // about 16 work items per warp slot of the persistent grid
-    const int64_t target = (int64_t)p.total_warps * 16;
+    int64_t target = (int64_t)p.total_warps * 16;
+    if (target > kMaxTargetItems) target = kMaxTargetItems;
     int64_t chunk = (work + target - 1) / (target > 0 ? target : 1);
     if (chunk < 1) chunk = 1;
     if (tid == 0) p.counters[kChunkBlocks] = (uint32_t)chunk;

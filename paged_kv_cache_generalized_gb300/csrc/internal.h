@@ -19,6 +19,9 @@ constexpr int kTcMinRows = 16;
 constexpr int kTcTileRows = 128;
 // Upper bound on the KV splits of one CUDA-core work item's rows.
 constexpr int kMaxSplits = 64;
+// The planner sizes splits for about 16 work items per warp of the persistent grid, capped here
+// (enough for 256 SMs x 8 warps); the workspace bound on split partials follows from it.
+constexpr int64_t kMaxTargetItems = 32768;
 
 // Counters at the start of the workspace.
 enum Counter : int {
