@@ -105,6 +105,33 @@ pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, co
                      pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * pa_forward_no_alloc: pa_forward without a caller-provided workspace.
+ *
+ * The pages have no counterpart for this call; it exists for callers that cannot allocate
+ * device memory where they run attention -- for example a plug-in inside an engine whose own
+ * allocator owns every byte of device memory, or a latency-critical loop that must not call
+ * cudaMalloc / cudaFree (which can synchronise the whole device).  Same arguments, semantics and
+ * results as pa_forward, minus `workspace` / `workspace_bytes`.
+ *
+ *  - Scratch: a library-owned device array of PA_NO_ALLOC_WORKSPACE_BYTES (32 MiB), held by every
+ *    GPU that loads the library until the process exits.  The call allocates nothing (no
+ *    cudaMalloc, cudaFree or allocating library routine).
+ *  - Dims whose pa_forward_workspace_size exceeds PA_NO_ALLOC_WORKSPACE_BYTES are rejected with
+ *    PA_ERR_WORKSPACE before any device work (use pa_forward with your own workspace instead).
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last call's contents (nothing
+ *    in it needs to start at zero).  Calls whose work overlaps on the GPU -- on different streams,
+ *    or from different host threads -- race on it and give undefined results: serialise them.
+ * ---------------------------------------------------------------------------------------- */
+#define PA_NO_ALLOC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+
+pa_status pa_forward_no_alloc(const pa_dims *dims, const void *q, const void *k_cache,
+                              const void *v_cache, const int32_t *block_tables,
+                              const int32_t *ctx_lens, const int32_t *q_lens, float scale,
+                              void *out, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * kv_append: write the new tokens' K/V into the paged cache.
  *
  * For every new token t with slot_mapping[t] >= 0, every layer l and KV head h:

@@ -28,8 +28,9 @@ STATUS_BITS = {
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 _ELEM = {torch.float32: 4, torch.bfloat16: 2, torch.float16: 2}
 
-EXPORTED = ("pa_forward_workspace_size", "pa_forward", "kv_append", "block_copy",
-            "pa_get_device_status", "pa_status_string", "pa_version")
+EXPORTED = ("pa_forward_workspace_size", "pa_forward", "pa_forward_no_alloc", "kv_append",
+            "block_copy", "pa_get_device_status", "pa_status_string", "pa_version")
+NO_ALLOC_WORKSPACE_BYTES = 32 * 1024 * 1024
 
 
 class PaDims(ctypes.Structure):
@@ -79,6 +80,9 @@ def load_library(path: str | None = None):
     lib.pa_forward_workspace_size.argtypes = [ctypes.POINTER(PaDims)]
     lib.pa_forward.restype = ctypes.c_int
     lib.pa_forward.argtypes = [ctypes.POINTER(PaDims), P, P, P, P, P, P, ctypes.c_float, P, P, sz, P]
+    lib.pa_forward_no_alloc.restype = ctypes.c_int
+    lib.pa_forward_no_alloc.argtypes = [ctypes.POINTER(PaDims), P, P, P, P, P, P, ctypes.c_float,
+                                        P, P]
     lib.kv_append.restype = ctypes.c_int
     lib.kv_append.argtypes = [ctypes.POINTER(KvAppendDims), P, P, P, P, P, P]
     lib.block_copy.restype = ctypes.c_int
@@ -162,6 +166,26 @@ def pa_forward(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale=None, 
                         _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                         _stream(stream))
     _check(rc, "pa_forward")
+    return out
+
+
+def pa_forward_no_alloc(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale=None, out=None,
+                        stream=None):
+    """pa_forward with the library's own fixed-size scratch (see ``pa_forward_no_alloc`` in
+    include/pagedkv.h): for callers that cannot allocate device memory.  Raises if the batch
+    needs more scratch than the library holds."""
+    lib = load_library()
+    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
+        raise ValueError("k_cache and v_cache must have the same shape and strides")
+    dims = forward_dims(q, k_cache, block_tables, ctx_lens)
+    if scale is None:
+        scale = 1.0 / float(dims.head_dim) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib.pa_forward_no_alloc(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(block_tables), _ptr(ctx_lens), _ptr(q_lens),
+                                 ctypes.c_float(scale), _ptr(out), _stream(stream))
+    _check(rc, "pa_forward_no_alloc")
     return out
 
 
