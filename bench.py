@@ -127,9 +127,12 @@ def attn_flops(ctx, ql, hq, d):
     return 4.0 * d * hq * pairs
 
 
-def _tc_enabled():
-    """Whether libpagedkv routes multi-token bf16/f16 turns to its tensor-core kernel."""
-    return False
+def _tc_enabled(batch):
+    """Whether libpagedkv routes this batch's multi-token turns to its tensor-core kernel (bf16 or
+    f16, head_dim 128, a GQA group dividing 128, blocks of 16..128 tokens)."""
+    g = batch.num_q_heads // batch.num_kv_heads
+    return (batch.dtype in ("bf16", "f16") and batch.head_dim == 128 and 128 % g == 0
+            and 16 <= batch.block_size <= 128)
 
 
 class AttnStep:
@@ -194,7 +197,7 @@ class AttnStep:
         self.d2h_bytes = self.out.numel() * self.out.element_size()
         # block_copy (if any fork) + kv_append + pa_forward's plan, CUDA-core and combine kernels
         # (+ the tensor-core kernel when the batch has multi-token turns it supports)
-        tc = T > batch.num_seqs and batch.dtype in ("bf16", "f16") and d == 128 and _tc_enabled()
+        tc = T > batch.num_seqs and _tc_enabled(batch)
         self.launches_per_step = (1 if len(pairs) else 0) + 1 + 3 + (1 if tc else 0)
 
     def _copy(self, inp):
@@ -422,7 +425,8 @@ def run_native(args):
         achieved = step_obj.flops / (attn_ms * 1e-3) / 1e12
         pk = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
-                "frac": achieved / pk, "traffic": None, "kernel": "pa_forward",
+                "frac": achieved / pk, "traffic": None,
+                "kernel": "pa_forward (plan + tcgen05 tensor-core prefill + CUDA-core decode + combine)",
                 "peak_source": f"bf16_tflops (burst) of {peak_src}"}
 
     cpu = None

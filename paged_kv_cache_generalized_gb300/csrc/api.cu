@@ -109,10 +109,7 @@ WsLayout ws_layout(const pa_dims &d) {
     return L;
 }
 
-bool tc_supported(const pa_dims &d) {
-    (void)d;
-    return false;
-}
+bool tc_supported(const pa_dims &d) { return tc_shape_supported(d); }
 
 }  // namespace pkv
 

@@ -55,6 +55,7 @@ struct WsLayout {
 WsLayout ws_layout(const pa_dims &d);
 int rows_per_item(const pa_dims &d);
 bool tc_supported(const pa_dims &d);
+bool tc_shape_supported(const pa_dims &d);  // attn_tc.cu
 
 struct FwdArgs {
     pa_dims dims;

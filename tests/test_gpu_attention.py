@@ -170,3 +170,41 @@ def test_config_mixed_gqa_full_size():
 
 def test_config_longprefill_full_size():
     _sampled(W.longprefill(), 128)
+
+
+# ------------------------------------------------------------------------------------------------
+# Tensor-core path (multi-token bf16/f16 turns, head_dim 128)
+# ------------------------------------------------------------------------------------------------
+
+def _forward_with_workspace(b):
+    d = batch_to_dev(b)
+    need = pkg.forward_workspace_size(d["q"], d["k"], d["bt"], d["ctx"])
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+    out = pkg.pa_forward(d["q"], d["k"], d["v"], d["bt"], d["ctx"], d["ql"], b.scale, workspace=ws)
+    torch.cuda.synchronize()
+    counters = ws[:64].view(torch.int32).cpu().numpy()
+    return out, counters
+
+
+TC_CASES = [
+    # name, ctx, q, Hq, Hkv, B, dtype, scale
+    ("tc_one_tile", [0], [128], 1, 1, 16, "bf16", None),
+    ("tc_one_tile_scale0", [0], [128], 1, 1, 16, "bf16", 0.0),
+    ("tc_ctx_not_multiple", [77], [100], 2, 2, 16, "bf16", None),
+    ("tc_gqa4_b32", [1000, 31], [64, 200], 16, 4, 32, "bf16", None),
+    ("tc_gqa8_f16", [260], [40], 16, 2, 64, "f16", None),
+    ("tc_b128", [300], [129], 2, 1, 128, "bf16", None),
+    ("tc_long", [3000], [300], 1, 1, 16, "bf16", None),
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=[c[0] for c in TC_CASES])
+def test_tensor_core_path(case):
+    name, ctx, ql, hq, hkv, B, dtype, scale = case
+    b = W.make_attn_batch(name, ctx, ql, hq, hkv, 128, B, dtype, seed=zlib.crc32(name.encode()) % 1000,
+                          scale=scale)
+    out, counters = _forward_with_workspace(b)
+    assert counters[3] > 0, "no tile went to the tensor-core kernel"
+    assert pkg.device_status() == 0
+    ref = oracle.paged_attention_batch(b, threads=8)
+    assert_close(as_f64(out), ref, b.dtype, name)
