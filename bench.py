@@ -45,7 +45,31 @@ if ROOT not in sys.path:
 from paged_kv_cache_generalized_gb300 import workloads as W  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+CSRC = os.path.join(ROOT, "paged_kv_cache_generalized_gb300", "csrc")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def measured_traffic(workload, algorithmic_bytes):
+    """DRAM bytes of one launch of the dominant kernel: the ratio (traffic / algorithmic bytes)
+    from the last ncu capture of this workload's kernel, scaled to this launch; None when the
+    kernel sources changed since that capture (or there is none)."""
+    import hashlib
+
+    try:
+        with open(TRAFFIC_FILE) as f:
+            entry = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None, None
+    if not entry:
+        return None, None
+    h = hashlib.sha256()
+    for name in entry["sources"]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != entry["source_sha"]:
+        return None, "kernel changed since the ncu capture"
+    return entry["ratio"] * algorithmic_bytes, entry["captured_case"]
 
 
 def load_peaks():
@@ -227,10 +251,11 @@ def build_attn_step(name, dev, seqs=None):
         b = W.decode13b(seed=2, num_seqs=seqs or 64, poison=False)
         return AttnStep(b, dev, cow_frac=0.1, seed=2), b
     if name == "mixed_gqa":
-        b = W.mixed_gqa(seed=3, poison=False)
+        half = (seqs or 64) // 2
+        b = W.mixed_gqa(seed=3, n_resume=half, n_decode=half, poison=False)
         return AttnStep(b, dev, cow_frac=0.0, seed=3), b
     if name == "longprefill":
-        b = W.longprefill(seed=4, poison=False)
+        b = W.longprefill(seed=4, num_seqs=seqs or 8, poison=False)
         return AttnStep(b, dev, cow_frac=0.0, seed=4), b
     raise ValueError(name)
 
@@ -417,15 +442,19 @@ def run_native(args):
         return
     if unit == "GB/s":
         achieved = step_obj.bytes_attn / (attn_ms * 1e-3) / 1e9
+        traffic, tsrc = measured_traffic(name, step_obj.bytes_attn)
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "traffic_source": tsrc,
+                "algorithmic_bytes": step_obj.bytes_attn,
                 "kernel": "pa_forward (plan + split-KV CUDA-core attention + combine)",
                 "peak_source": f"hbm_gbs of {peak_src}"}
     else:
         achieved = step_obj.flops / (attn_ms * 1e-3) / 1e12
         pk = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        traffic, tsrc = measured_traffic(name, step_obj.bytes_attn)
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
-                "frac": achieved / pk, "traffic": None,
+                "frac": achieved / pk, "traffic": traffic, "traffic_source": tsrc,
+                "algorithmic_flops": step_obj.flops,
                 "kernel": "pa_forward (plan + tcgen05 tensor-core prefill + CUDA-core decode + combine)",
                 "peak_source": f"bf16_tflops (burst) of {peak_src}"}
 
@@ -462,7 +491,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--seqs", type=int, default=None,
-                    help="decode13b only: number of sequences (default 64; smaller for profiling)")
+                    help="number of sequences (defaults 64 / 64 / 8; smaller for profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -79,10 +79,11 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
  *   scale         the softmax scale, normally 1/sqrt(d).
  *   workspace     device scratch of at least pa_forward_workspace_size(dims) bytes, 256-byte
  *                 aligned; contents need no initialisation and are clobbered.
- * Supported: dtype f32 / bf16 / f16; d in {64, 128}; B in {8, 16, 32, 64, 128}; Hq % Hkv == 0;
- * 16-byte aligned q, out and caches; kv_block_stride a multiple of 8 elements.
- * Multi-token bf16/f16 sequences with d = 128 run on the tcgen05 tensor-core kernel; decode and
- * everything else on the CUDA-core split-KV kernel.
+ * Supported: dtype f32 / bf16 / f16; d in {64, 128}; B in {16, 32, 64, 128}; Hq % Hkv == 0;
+ * 16-byte aligned q, out and caches; kv_block_stride * element size a multiple of 16 bytes.
+ * Sequences with q_len * g >= 16 query rows per KV head run on the tcgen05 tensor-core kernel when
+ * the dtype is bf16/f16, d = 128, g divides 128 and scale >= 0; decode steps, short turns and
+ * everything else run on the CUDA-core split-KV kernel.
  * ---------------------------------------------------------------------------------------- */
 typedef struct {
     int32_t dtype;              /* pa_dtype of q, out, k_cache and v_cache */
