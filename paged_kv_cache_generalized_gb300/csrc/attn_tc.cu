@@ -10,20 +10,24 @@
 // One work item is a tile of 128 query rows of one sequence and one KV head.  Rows are
 // (token, head-in-GQA-group) pairs, so the g query heads sharing a KV head are packed into the
 // same tile (M = 128 even for short turns with GQA).  Per 128-key tile:
-//   S = Q K^T   (tcgen05.mma, M=N=128, K=d=128, bf16/f16 -> fp32 in tensor memory)
-//   P = exp2(S * scale * log2 e - m), rows masked causally on diagonal tiles only
-//   O += P V    (tcgen05.mma, P from shared memory, V MN-major, O accumulates in tensor memory)
-// The running max is only moved (and O rescaled in tensor memory) when it grows by more than
-// 2^8, so most tiles skip the rescale; the final O / l is exact either way.
+//   S = Q K^T   (tcgen05.mma, M=N=128, K=d=128: Q from tensor memory, K from shared memory)
+//   P = exp2(S * scale * log2 e - m), causal mask on diagonal tiles only, P -> 16 bits
+//   O += P V    (tcgen05.mma: P from tensor memory, V from shared memory (MN-major))
+// Q and P live in tensor memory, so the tensor cores read only K and V from shared memory and P
+// never goes through shared memory.  P overwrites the S buffer it was computed from (the MMAs of
+// one CTA execute in issue order, so the next S into that buffer comes after the PV that reads
+// P).  The running max is only moved (and O rescaled in tensor memory) when it grows by more than
+// 2^8; only then does the softmax wait for the previous PV.  The final O / l is exact either way.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over the tile list):
-//   warp 0      TMA producer: Q tile once per item; K and V tiles gathered block by block through
-//               the block table, one 3-D box (64 columns x B rows of one (block, head)) per copy,
-//               128-byte swizzled, two stages each for K and V.
+// Warp roles (224 threads, one CTA per SM, persistent over the tile list):
+//   warps 0, 6  TMA producers for K and for V: per 128-key tile one 3-D box (64 columns x B rows
+//               of one (block, head)) per block and panel, 128-byte swizzled, 3 stages each; the
+//               block-table entries of the next tile are fetched while the current one is issued.
 //   warp 1      MMA issuer (one lane) and tensor-memory owner; zeroes V rows past the last key of
 //               a sequence's final tile (those slots may hold anything, NaN included).
-//   warps 2-5   softmax: one thread per tile row (tensor-memory lane), P to shared memory in the
-//               UMMA K-major 128-byte-swizzled layout, lazy O rescale, epilogue O / l -> out.
+//   warps 2-5   softmax: one thread per tile row (tensor-memory lane): loads its Q row into tensor
+//               memory once per item, then per tile S -> P, and the epilogue O / l -> out.
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256,384), Q [384,448).
 // Every wait is bounded; on a timeout the role reports PA_DEV_TIMEOUT and stops, the kernel
 // drains what it issued, frees its tensor memory and returns.
 #include <cuda.h>
@@ -42,23 +46,28 @@ constexpr int kKeys = 128;          // keys per KV tile (UMMA N of QK^T, K of PV
 constexpr int kDim = 128;           // head_dim
 constexpr int kPanel = 128 * 128;   // bytes of one 64-column panel of a 128-row tile (16 KiB)
 constexpr int kTile = 2 * kPanel;   // one 128 x 128 16-bit tile (32 KiB)
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+constexpr int kKWarp = 0, kMmaWarp = 1, kVWarp = 6;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemQ = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 2^8
 
+// K and V are each triple-buffered: a stage is refilled once the MMA that read it is done.
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
+
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int kSmQ = 0;
-constexpr int kSmK = kSmQ + kTile;          // 2 stages
-constexpr int kSmV = kSmK + 2 * kTile;      // 2 stages
-constexpr int kSmP = kSmV + 2 * kTile;
-constexpr int kSmBar = kSmP + kTile;
+constexpr int kSmK = 0;
+constexpr int kSmV = kSmK + kKStages * kTile;
+constexpr int kSmBar = kSmV + kVStages * kTile;
 constexpr int kSmBytes = kSmBar + 256 + 1024;   // barriers, tensor-memory slot, alignment slack
 
 enum Bar {
-    kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
-    kSFull0, kSFull1, kPFull, kOReady, kDrain, kNumBars
+    kKFull0 = 0, kKEmpty0 = kKFull0 + kKStages, kVFull0 = kKEmpty0 + kKStages,
+    kVEmpty0 = kVFull0 + kVStages, kSFull0 = kVEmpty0 + kVStages, kSFull1, kPFull, kOReady, kQFull,
+    kDrain, kNumBars
 };
+static_assert(kNumBars * 8 + 4 <= 256, "barrier area");
 
 // ---- tcgen05 / TMA wrappers -----------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
@@ -88,13 +97,14 @@ __host__ __device__ constexpr uint32_t instr_desc(bool b_mn_major, bool f16) {
            ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                     uint32_t accumulate) {
+// D (tensor memory) (+)= A (tensor memory) * B (shared-memory descriptor).
+__device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -149,6 +159,27 @@ __device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint32_t (&r)
         : "memory");
 }
 
+// All 128 fp32 columns of this thread's tensor-memory lane in one load (+ wait).
+__device__ __forceinline__ void tmem_load128(uint32_t taddr, uint32_t (&r)[128]) {
+    asm volatile(
+        "{\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t}"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+        : "r"(taddr)
+        : "memory");
+}
+
+// 64 32-bit columns (128 packed 16-bit values) into this thread's tensor-memory lane (+ wait).
+__device__ __forceinline__ void tmem_store64(uint32_t taddr, const uint32_t (&r)[64]) {
+    asm volatile(
+        "{\n\t"
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};\n\t"
+        "tcgen05.wait::st.sync.aligned;\n\t}"
+        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
+        : "memory");
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -183,6 +214,7 @@ __device__ __forceinline__ int find_rank(const int32_t *a, int n, int key) {
 }
 
 struct TcParams {
+    const char *q;
     char *out;
     const int32_t *bt, *ctx, *qlen;
     const int32_t *cu_q, *tc_cu, *tc_seq;
@@ -217,10 +249,27 @@ __device__ __forceinline__ Item decode_item(const TcParams &p, int it) {
     return t;
 }
 
+// Physical block of each lane's block in KV tile kt (lanes < blocks of the tile), clamped.
+__device__ __forceinline__ int tile_block(const TcParams &p, const int32_t *bt_row, const Item &t,
+                                          int kt, int bpt, int lane, int &nblk) {
+    const int64_t key0 = (int64_t)kt * kKeys;
+    const int64_t keys = min((int64_t)kKeys, t.pmax + 1 - key0);
+    nblk = (int)((keys + p.block_size - 1) / p.block_size);
+    int phys = 0;
+    if (lane < nblk) {
+        phys = __ldg(bt_row + (int64_t)kt * bpt + lane);
+        if (phys < 0 || (int64_t)phys >= p.num_blocks) {
+            report(p.status, PA_DEV_BAD_BLOCK_ID);
+            phys = (int)p.num_blocks;   // outside the tensor map: the copy fills zeros
+        }
+    }
+    return phys;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                        const __grid_constant__ CUtensorMap vmap, TcParams p) {
+    tc_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        TcParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -232,10 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idesc_pv = instr_desc(true, kF16);
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], b == kPFull ? 4 : 1);
+        for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], (b == kPFull || b == kQFull) ? 4 : 1);
         mbar_fence_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(tmem_slot)),
                      "r"(kTmemCols)
@@ -250,109 +299,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int B = p.block_size;
     const int bpt = kKeys / B;   // blocks per KV tile
 
-    if (warp == 0) {
-        // ------------------------------------------------------------------ TMA producer
-        uint32_t kv_iter = 0, items = 0;
-        uint32_t armed_k[2] = {0, 0}, armed_v[2] = {0, 0}, armed_q = 0;
+    if (warp == kKWarp || warp == kVWarp) {
+        // ------------------------------------------------------------ TMA producers (K or V)
+        const bool is_k = warp == kKWarp;
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        const int full0 = is_k ? kKFull0 : kVFull0, empty0 = is_k ? kKEmpty0 : kVEmpty0;
+        const int nst = is_k ? kKStages : kVStages;
+        unsigned char *stage0 = smem + (is_k ? kSmK : kSmV);
+        uint32_t iter = 0;
+        uint32_t armed[3] = {0, 0, 0};
         bool ok = true;
-        for (int it = blockIdx.x; it < total && ok; it += gridDim.x, ++items) {
+        for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
             const Item t = decode_item(p, it);
-            if (items > 0 && !warp_wait(&bars[kQEmpty], (items - 1) & 1)) { ok = false; break; }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars[kQFull], kTile);
-                const int y = t.kvh * p.group;
-                const int z = (int)(t.tok0 + t.j0);
-                tma_load_3d(smem + kSmQ, &qmap, 0, y, z, &bars[kQFull]);
-                tma_load_3d(smem + kSmQ + kPanel, &qmap, 64, y, z, &bars[kQFull]);
-            }
-            ++armed_q;
             const int32_t *bt_row = p.bt + (int64_t)t.seq * p.max_blocks;
-            for (int kt = 0; kt < t.ntiles; ++kt, ++kv_iter) {
-                const int s = kv_iter & 1;
-                const int64_t key0 = (int64_t)kt * kKeys;
-                const int64_t keys = min((int64_t)kKeys, t.pmax + 1 - key0);
-                const int nblk = (int)((keys + B - 1) / B);
-                int phys = 0;
-                if (lane < nblk) {
-                    phys = __ldg(bt_row + (int64_t)kt * bpt + lane);
-                    if (phys < 0 || (int64_t)phys >= p.num_blocks) {
-                        report(p.status, PA_DEV_BAD_BLOCK_ID);
-                        phys = (int)p.num_blocks;   // out of the tensor map: the copy fills zeros
-                    }
-                }
-                const uint32_t bytes = (uint32_t)nblk * B * 128 * 2;
-                if (kv_iter >= 2 && !warp_wait(&bars[kKEmpty0 + s], ((kv_iter >> 1) - 1) & 1)) { ok = false; break; }
-                if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull0 + s], bytes);
+            int nblk_next = 0;
+            int phys_next = tile_block(p, bt_row, t, 0, bpt, lane, nblk_next);
+            for (int kt = 0; kt < t.ntiles; ++kt, ++iter) {
+                const int phys = phys_next, nblk = nblk_next;
+                if (kt + 1 < t.ntiles) phys_next = tile_block(p, bt_row, t, kt + 1, bpt, lane, nblk_next);
+                const int s = iter % nst;
+                const uint32_t use = iter / nst;
+                if (use > 0 && !warp_wait(&bars[empty0 + s], (use - 1) & 1)) { ok = false; break; }
+                if (lane == 0) mbar_arrive_expect_tx(&bars[full0 + s], (uint32_t)nblk * B * 128 * 2);
                 __syncwarp();
                 if (lane < nblk) {
-                    unsigned char *dst = smem + kSmK + s * kTile + lane * B * 128;
-                    tma_load_3d(dst, &kmap, 0, t.kvh * B, phys, &bars[kKFull0 + s]);
-                    tma_load_3d(dst + kPanel, &kmap, 64, t.kvh * B, phys, &bars[kKFull0 + s]);
+                    unsigned char *dst = stage0 + s * kTile + lane * B * 128;
+                    tma_load_3d(dst, map, 0, t.kvh * B, phys, &bars[full0 + s]);
+                    tma_load_3d(dst + kPanel, map, 64, t.kvh * B, phys, &bars[full0 + s]);
                 }
-                ++armed_k[s];
-                if (kv_iter >= 2 && !warp_wait(&bars[kVEmpty0 + s], ((kv_iter >> 1) - 1) & 1)) { ok = false; break; }
-                if (lane == 0) mbar_arrive_expect_tx(&bars[kVFull0 + s], bytes);
-                __syncwarp();
-                if (lane < nblk) {
-                    unsigned char *dst = smem + kSmV + s * kTile + lane * B * 128;
-                    tma_load_3d(dst, &vmap, 0, t.kvh * B, phys, &bars[kVFull0 + s]);
-                    tma_load_3d(dst + kPanel, &vmap, 64, t.kvh * B, phys, &bars[kVFull0 + s]);
-                }
-                ++armed_v[s];
+                if (s == 0) ++armed[0];
+                else if (s == 1) ++armed[1];
+                else ++armed[2];
             }
         }
         if (!ok && lane == 0) report(p.status, PA_DEV_TIMEOUT);
         // every copy this warp issued lands before the CTA can exit
-        for (int s = 0; s < 2; ++s) {
-            if (armed_k[s]) mbar_wait(&bars[kKFull0 + s], (armed_k[s] - 1) & 1);
-            if (armed_v[s]) mbar_wait(&bars[kVFull0 + s], (armed_v[s] - 1) & 1);
-        }
-        if (armed_q) mbar_wait(&bars[kQFull], (armed_q - 1) & 1);
-    } else if (warp == 1) {
+        for (int s = 0; s < nst; ++s)
+            if (armed[s]) mbar_wait(&bars[full0 + s], (armed[s] - 1) & 1);
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
-        uint32_t kv_iter = 0, items = 0;
+        uint32_t iter = 0, items = 0;
         bool ok = true;
-        const uint32_t q_addr = smem_addr(smem + kSmQ);
-        const uint32_t p_addr = smem_addr(smem + kSmP);
+        const uint32_t k_base = smem_addr(smem + kSmK), v_base = smem_addr(smem + kSmV);
         auto issue_s = [&](uint32_t g) -> bool {
-            const int s = g & 1;
-            if (!warp_wait(&bars[kKFull0 + s], (g >> 1) & 1)) return false;
+            const uint32_t s_tmem = tmem + ((g & 1) ? kTmemS1 : kTmemS0);
+            const int ks = g % kKStages;
+            if (!warp_wait(&bars[kKFull0 + ks], (g / kKStages) & 1)) return false;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t k_addr = smem_addr(smem + kSmK + s * kTile);
-                const uint32_t d_tmem = tmem + (s ? kTmemS1 : kTmemS0);
+                const uint32_t k_addr = k_base + ks * kTile;
 #pragma unroll
                 for (int k = 0; k < kDim / 16; ++k) {
                     const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
-                    umma(d_tmem, smem_desc(q_addr + off, 16, 1024), smem_desc(k_addr + off, 16, 1024),
-                         idesc_qk, k > 0);
+                    umma_ts(s_tmem, tmem + kTmemQ + k * 8, smem_desc(k_addr + off, 16, 1024), idesc_qk,
+                            k > 0);
                 }
-                umma_commit(&bars[kSFull0 + s]);
-                umma_commit(&bars[kKEmpty0 + s]);
+                umma_commit(&bars[kSFull0 + (g & 1)]);
+                umma_commit(&bars[kKEmpty0 + ks]);
             }
             __syncwarp();
             return true;
         };
         for (int it = blockIdx.x; it < total && ok; it += gridDim.x, ++items) {
             const Item t = decode_item(p, it);
-            if (!warp_wait(&bars[kQFull], items & 1)) { ok = false; break; }
+            if (!warp_wait(&bars[kQFull], items & 1)) { ok = false; break; }   // Q rows in tensor memory
             tc_fence_after();
-            if (!issue_s(kv_iter)) { ok = false; break; }
+            if (!issue_s(iter)) { ok = false; break; }
             for (int kt = 0; kt < t.ntiles; ++kt) {
-                const uint32_t g = kv_iter + kt;
-                if (kt + 1 < t.ntiles) {
-                    if (!issue_s(g + 1)) { ok = false; break; }
-                } else if (lane == 0) {
-                    umma_commit(&bars[kQEmpty]);      // Q is free once every S of the item is done
-                }
-                __syncwarp();
+                const uint32_t g = iter + kt;
+                if (kt + 1 < t.ntiles && !issue_s(g + 1)) { ok = false; break; }
                 if (!warp_wait(&bars[kPFull], g & 1)) { ok = false; break; }
-                const int s = g & 1;
-                if (!warp_wait(&bars[kVFull0 + s], (g >> 1) & 1)) { ok = false; break; }
+                const int vs = g % kVStages;
+                if (!warp_wait(&bars[kVFull0 + vs], (g / kVStages) & 1)) { ok = false; break; }
                 // zero V rows past the last key any row of this tile sees (free or stale slots)
                 const int64_t valid = t.pmax + 1 - (int64_t)kt * kKeys;
                 if (valid < kKeys) {
-                    unsigned char *vb = smem + kSmV + s * kTile;
+                    unsigned char *vb = smem + kSmV + vs * kTile;
                     const int first = (int)valid;
                     const int n16 = (kKeys - first) * 8;            // 16-byte chunks per panel
                     for (int i = lane; i < 2 * n16; i += 32) {
@@ -365,20 +387,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t v_addr = smem_addr(smem + kSmV + s * kTile);
+                    const uint32_t p_tmem = tmem + ((g & 1) ? kTmemS1 : kTmemS0);
+                    const uint32_t v_addr = v_base + vs * kTile;
 #pragma unroll
-                    for (int k = 0; k < kKeys / 16; ++k) {
-                        const uint32_t a_off = (k >> 2) * kPanel + (k & 3) * 32;
-                        umma(tmem + kTmemO, smem_desc(p_addr + a_off, 16, 1024),
-                             smem_desc(v_addr + k * 16 * 128, kPanel, 1024), idesc_pv,
-                             (kt > 0 || k > 0) ? 1u : 0u);
-                    }
+                    for (int k = 0; k < kKeys / 16; ++k)
+                        umma_ts(tmem + kTmemO, p_tmem + k * 8, smem_desc(v_addr + k * 16 * 128, kPanel, 1024),
+                                idesc_pv, (kt > 0 || k > 0) ? 1u : 0u);
                     umma_commit(&bars[kOReady]);
-                    umma_commit(&bars[kVEmpty0 + s]);
+                    umma_commit(&bars[kVEmpty0 + vs]);
                 }
                 __syncwarp();
             }
-            kv_iter += t.ntiles;
+            iter += t.ntiles;
         }
         if (!ok && lane == 0) report(p.status, PA_DEV_TIMEOUT);
         // no tensor-core work of this CTA may be in flight when its tensor memory is freed
@@ -390,92 +410,118 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        unsigned char *pbase = smem + kSmP;
-        uint32_t kv_iter = 0, pv_seen = 0;
+        const float c_log2 = p.scale_log2;            // >= 0 (negative scales use CUDA cores)
+        uint32_t iter = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
             const Item t = decode_item(p, it);
+            const int j = t.j0 + row / p.group, hh = row % p.group;
+            // this row of Q -> tensor memory (the previous item's MMAs are all complete: its
+            // epilogue waited for its last PV, which follows every S of that item)
+            {
+                uint32_t qr[64];
+                if (row < t.rows_valid) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        p.q + (((t.tok0 + j) * p.q_heads + (int64_t)t.kvh * p.group + hh) * kDim) * sizeof(T));
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const uint4 v = __ldg(src + c);
+                        qr[4 * c] = v.x;
+                        qr[4 * c + 1] = v.y;
+                        qr[4 * c + 2] = v.z;
+                        qr[4 * c + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) qr[c] = 0u;
+                }
+                tmem_store64(lane_base + kTmemQ, qr);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kQFull]);
+            }
             int64_t prow = t.pmin + row / p.group;
             if (prow > t.pmax) prow = t.pmax;             // padding rows: finite, never stored
             float m = -INFINITY, l = 0.f;
             for (int kt = 0; kt < t.ntiles; ++kt) {
-                const uint32_t g = kv_iter + kt;
-                const int s = g & 1;
-                if (!warp_wait(&bars[kSFull0 + s], (g >> 1) & 1)) { ok = false; break; }
+                const uint32_t g = iter + kt;
+                const uint32_t s_tmem = lane_base + ((g & 1) ? kTmemS1 : kTmemS0);
+                if (!warp_wait(&bars[kSFull0 + (g & 1)], (g >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                float x[kKeys];
-#pragma unroll
-                for (int c = 0; c < kKeys / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_load32(lane_base + (s ? kTmemS1 : kTmemS0) + c * 32, r);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]) * p.scale_log2;
-                }
+                uint32_t raw[kKeys];
+                tmem_load128(s_tmem, raw);
+                float *x = reinterpret_cast<float *>(raw);   // raw scores q.k (unscaled)
                 const int64_t key0 = (int64_t)kt * kKeys;
-                if (key0 + kKeys - 1 > t.pmin) {           // diagonal tile: causal mask
-                    const int64_t lim = prow - key0;       // visible columns: 0 .. lim
+                const bool diag = key0 + kKeys - 1 > t.pmin;  // tile crosses some row's diagonal
+                const int64_t lim = prow - key0;               // visible columns: 0 .. lim
+                if (diag) {
 #pragma unroll
                     for (int i = 0; i < kKeys; ++i)
                         if (i > lim) x[i] = -INFINITY;
                 }
-                float mt = x[0];
+                // row max of the raw scores (scale >= 0 keeps the order), 8 independent chains
+                float mx[8];
 #pragma unroll
-                for (int i = 1; i < kKeys; ++i) mt = fmaxf(mt, x[i]);
+                for (int k = 0; k < 8; ++k) mx[k] = x[k];
+#pragma unroll
+                for (int i = 8; i < kKeys; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
+                const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                const float mt = (mraw == -INFINITY) ? -INFINITY : mraw * c_log2;
                 const float mnew = fmaxf(m, mt);
                 const bool rescale = mnew > m + kRescaleThreshold;
                 const float muse = rescale ? mnew : m;
-                if (kt > 0) {
-                    // PV of the previous tile must be done: it reads P, and O may be rescaled
-                    if (!warp_wait(&bars[kOReady], pv_seen & 1)) { ok = false; break; }
-                    ++pv_seen;
-                    tc_fence_after();
-                    // tensor-memory loads/stores are warp-collective: the whole warp rescales
-                    // when any of its rows must (alpha = 1 for the others)
-                    if (__any_sync(0xffffffffu, rescale)) {
-                        const float alpha = rescale ? fast_exp2(m - muse) : 1.f;
-                        l *= alpha;
-#pragma unroll 1
-                        for (int c = 0; c < kDim / 32; ++c) {
-                            uint32_t r[32];
-                            tmem_load32(lane_base + kTmemO + c * 32, r);
+                // P = exp2(scale*log2e*s - m), packed to 16 bits; partial row sums in 8 chains
+                uint32_t pk[kKeys / 2];
+                float ls[8];
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                            tmem_store32(lane_base + kTmemO + c * 32, r);
-                        }
+                for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll
+                for (int i = 0; i < kKeys / 2; ++i) {
+                    float e0 = fast_exp2(fmaf(x[2 * i], c_log2, -muse));
+                    float e1 = fast_exp2(fmaf(x[2 * i + 1], c_log2, -muse));
+                    if (diag) {
+                        if (2 * i > lim) e0 = 0.f;
+                        if (2 * i + 1 > lim) e1 = 0.f;
+                    }
+                    ls[i & 7] += e0 + e1;
+                    pk[i] = pack2<T>(e0, e1);
+                }
+                float lsum = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) lsum += ls[k];
+                // tensor-memory loads/stores are warp-collective: the whole warp rescales when any
+                // of its rows must (alpha = 1 for the others), after the previous PV is complete
+                if (kt > 0 && __any_sync(0xffffffffu, rescale)) {
+                    if (!warp_wait(&bars[kOReady], (g - 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const float alpha = rescale ? fast_exp2(m - muse) : 1.f;
+                    l *= alpha;
+#pragma unroll 1
+                    for (int c = 0; c < kDim / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_load32(lane_base + kTmemO + c * 32, r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_store32(lane_base + kTmemO + c * 32, r);
                     }
                 }
                 m = muse;
-                // P = exp2(x - m) -> 16-bit, into the K-major swizzled A tile of the PV product
-#pragma unroll
-                for (int c16 = 0; c16 < kKeys / 8; ++c16) {
-                    float e[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        e[i] = fast_exp2(x[c16 * 8 + i] - m);
-                        l += e[i];
-                    }
-                    uint4 v;
-                    v.x = pack2<T>(e[0], e[1]);
-                    v.y = pack2<T>(e[2], e[3]);
-                    v.z = pack2<T>(e[4], e[5]);
-                    v.w = pack2<T>(e[6], e[7]);
-                    const int panel = c16 >> 3, chunk = (c16 & 7) ^ (row & 7);
-                    *reinterpret_cast<uint4 *>(pbase + panel * kPanel + row * 128 + chunk * 16) = v;
-                }
-                fence_proxy_async_smem();
+                l += lsum;
+                // P over the first 64 columns of the S buffer it came from
+                tmem_store64(s_tmem, pk);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[kPFull]);
             }
             if (!ok) break;
-            // epilogue: O / l -> out
-            if (!warp_wait(&bars[kOReady], pv_seen & 1)) { ok = false; break; }
-            ++pv_seen;
+            // epilogue: O / l -> out, after the item's last PV
+            const uint32_t glast = iter + t.ntiles - 1;
+            if (!warp_wait(&bars[kOReady], glast & 1)) { ok = false; break; }
             tc_fence_after();
             const float inv = 1.f / l;
             const bool store = row < t.rows_valid;
-            const int j = t.j0 + row / p.group, hh = row % p.group;
             T *orow = reinterpret_cast<T *>(p.out) +
                       ((t.tok0 + j) * p.q_heads + (int64_t)t.kvh * p.group + hh) * kDim;
 #pragma unroll 1
@@ -495,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            kv_iter += t.ntiles;
+            iter += t.ntiles;
         }
         if (!ok && lane == 0) report(p.status, PA_DEV_TIMEOUT);
     }
@@ -503,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
     }
@@ -561,16 +607,15 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s) {
     const uint64_t es = 2;
     const int64_t bstride = d.kv_block_stride ? d.kv_block_stride
                                               : (int64_t)d.num_kv_heads * d.block_size * d.head_dim;
-    CUtensorMap qmap, kmap, vmap;
-    if (!make_map(&qmap, d.dtype, a.q, kDim, d.num_q_heads, d.total_q, kDim * es,
-                  (uint64_t)d.num_q_heads * kDim * es, g, kRows / g) ||
-        !make_map(&kmap, d.dtype, a.k, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
+    CUtensorMap kmap, vmap;
+    if (!make_map(&kmap, d.dtype, a.k, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
                   kDim * es, bstride * es, d.block_size, 1) ||
         !make_map(&vmap, d.dtype, a.v, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
                   kDim * es, bstride * es, d.block_size, 1))
         return cudaErrorInvalidValue;
     TcParams p;
     const WsLayout &L = a.lay;
+    p.q = static_cast<const char *>(a.q);
     p.out = static_cast<char *>(a.out);
     p.bt = a.bt;
     p.ctx = a.ctx;
@@ -592,11 +637,11 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s) {
     if (d.dtype == PA_F16) {
         e = cudaFuncSetAttribute(tc_attention_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmBytes);
         if (e != cudaSuccess) return e;
-        tc_attention_kernel<__half><<<a.num_sms, kThreads, kSmBytes, s>>>(qmap, kmap, vmap, p);
+        tc_attention_kernel<__half><<<a.num_sms, kThreads, kSmBytes, s>>>(kmap, vmap, p);
     } else {
         e = cudaFuncSetAttribute(tc_attention_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmBytes);
         if (e != cudaSuccess) return e;
-        tc_attention_kernel<__nv_bfloat16><<<a.num_sms, kThreads, kSmBytes, s>>>(qmap, kmap, vmap, p);
+        tc_attention_kernel<__nv_bfloat16><<<a.num_sms, kThreads, kSmBytes, s>>>(kmap, vmap, p);
     }
     return cudaGetLastError();
 }
