@@ -246,6 +246,81 @@ class AttnStep:
         self.out_host.copy_(self.out, non_blocking=True)
 
 
+class KVMoveStep:
+    """KV movement over a multi-layer fp16 pool [L, 2, num_blocks, Hkv, B, d] resident on the GPU:
+    block_copy of the copy-on-write pairs (every resident layer, K and V), kv_append of every
+    session's new tokens into all layers, then the swap-in of host-staged sessions layer by layer
+    (one block_copy per layer from a page-locked host pool)."""
+
+    def __init__(self, plan: W.KVMovePlan, dev):
+        import torch
+        import paged_kv_cache_generalized_gb300 as pkg
+
+        self.pkg, self.torch, self.plan, self.dev = pkg, torch, plan, dev
+        L, nb, hkv, B, d = plan.num_layers, plan.num_blocks, plan.num_kv_heads, plan.block_size, plan.head_dim
+        g = torch.Generator(device=dev)
+        g.manual_seed(plan.seed)
+        # values do not matter for timing (bit-exactness is tested on the same kernels elsewhere)
+        self.pool = torch.empty((L, 2, nb, hkv, B, d), dtype=torch.float16, device=dev)
+        self.pool.view(torch.int16).random_(generator=g)
+        T = len(plan.slot_mapping)
+        self.new = torch.empty((L, 2, T, hkv, d), dtype=torch.float16, device=dev)
+        self.new.view(torch.int16).random_(generator=g)
+        host_dev = torch.empty((L, 2, plan.num_host_blocks, hkv, B, d), dtype=torch.float16, device=dev)
+        host_dev.view(torch.int16).random_(generator=g)
+        self.host_pool = host_dev.cpu().pin_memory()
+        del host_dev
+        self.cow = torch.from_numpy(plan.cow_pairs).to(dev)
+        self.swap = torch.from_numpy(plan.swap_pairs).to(dev)
+        self.slots = torch.from_numpy(plan.slot_mapping).to(dev)
+        self.cow_planes = self.pool.view(L * 2, nb, hkv, B, d)
+        bb = plan.block_bytes
+        self.bytes_cow = float(len(plan.cow_pairs) * 2 * L * bb * 2)
+        self.bytes_append = float(2 * L * T * hkv * d * 2 * 2 + 8 * T)
+        self.bytes_swap = float(len(plan.swap_pairs) * 2 * L * bb * 2)
+        self.flops = 0.0
+        self.launches_per_step = 1 + 1 + L
+        self.h2d_bytes = self.bytes_swap / 2 + self.new.numel() * 2 + 8 * T + plan.cow_pairs.nbytes + plan.swap_pairs.nbytes
+        self.d2h_bytes = 0
+        self.out = None
+
+    def step(self, ev=None):
+        pkg, L = self.pkg, self.plan.num_layers
+        if ev is not None:
+            ev[0].record()
+        pkg.block_copy(self.cow_planes, self.cow_planes, self.cow)
+        if ev is not None:
+            ev[1].record()
+        pkg.kv_append(self.new[:, 0], self.new[:, 1], self.slots, self.pool[:, 0], self.pool[:, 1])
+        if ev is not None:
+            ev[2].record()
+        for layer in range(L):
+            pkg.block_copy(self.host_pool[layer], self.pool[layer], self.swap)
+        if ev is not None:
+            ev[3].record()
+
+    def e2e_step(self):
+        # the step's host inputs: new tokens, slot map, pair lists (the swap source is already host)
+        self.step()
+
+
+def h2d_peak_gbs(dev, nbytes=1 << 30, reps=5):
+    """Page-locked host -> device copy bandwidth measured here (the swap-in roofline)."""
+    import torch
+
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        dst.copy_(src, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    return nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+
 def build_attn_step(name, dev, seqs=None):
     if name == "decode13b":
         b = W.decode13b(seed=2, num_seqs=seqs or 64, poison=False)
@@ -267,6 +342,10 @@ WORKLOAD_TEXT = {
                  "(ctx U{256..8192}), GQA 32/8, head_dim 128, bf16, block 32",
     "longprefill": "longprefill: 8 seqs x (16384 cached + 2048 new), 40 MHA heads, head_dim 128, "
                    "bf16, block 16, ConvKV turn segments 64..1024 tokens",
+    "kvmove": "kvmove: 40-layer x 5120-hidden fp16 pool (0.78 MB/token), 8 layers resident, block 32, "
+              "64 sessions U{512..8192} tokens, append U{1..256} tokens each, copy-on-write of 10% of "
+              "blocks shared by U{2..4} sequences, swap-in of 8 sessions from pinned host memory, "
+              "layer by layer",
 }
 
 
@@ -337,7 +416,9 @@ def oracle_sample(b: W.AttnBatch, budget_s: float, max_rows=None):
 
 
 def metric_for(name):
-    if name in ("decode13b", "kvmove"):
+    if name == "kvmove":
+        return ("KV movement GB/s (bytes read + written by copy-on-write, append and swap-in per step / step time)", "GB/s", True)
+    if name == "decode13b":
         return ("paged-attn decode KV GB/s (algorithmic HBM bytes per step / step time)", "GB/s", True)
     return ("paged-attn mixed-prefill TFLOP/s (causal-exact attention FLOPs / step time)", "TFLOP/s", True)
 
@@ -348,6 +429,26 @@ def run_reference(args):
         return
     name = args.workload
     metric, unit, hib = metric_for(name)
+    if name == "kvmove":
+        plan = W.kvmove_plan(seed=5, num_layers=args.layers)
+        total = args.steps + args.warmup
+        per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
+        secs, moved, reps_all = 0.0, 0.0, 0
+        for s_ in range(total):
+            t, mv, reps = kvmove_oracle_sample(plan, per_step)
+            if s_ >= args.warmup:
+                secs += t
+                moved += mv
+        value = moved / secs / 1e9
+        line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(1, args.steps) * 1e3,
+                "higher_is_better": hib, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+                "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[name]},
+                "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                                 "sample": "numpy block copy of 64 copy-on-write pairs and append of 256 tokens per repetition"},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     b = {"decode13b": lambda: W.decode13b(seed=2, poison=False),
          "mixed_gqa": lambda: W.mixed_gqa(seed=3, poison=False),
          "longprefill": lambda: W.longprefill(seed=4, poison=False)}[name]()
@@ -482,6 +583,112 @@ def run_native(args):
     print(json.dumps(line), flush=True)
 
 
+def kvmove_oracle_sample(plan: W.KVMovePlan, budget_s: float):
+    """Times the oracle's block copy and append (numpy) on a bounded sample of the KV-movement
+    step: one layer's K and V planes holding only the blocks the sampled pairs and slots touch."""
+    import oracle
+
+    rng = np.random.default_rng(0)
+    hkv, B, d = plan.num_kv_heads, plan.block_size, plan.head_dim
+    moved, secs, reps = 0.0, 0.0, 0
+    while secs < budget_s:
+        cow = plan.cow_pairs[rng.choice(len(plan.cow_pairs), min(64, len(plan.cow_pairs)), replace=False)]
+        ids = np.unique(cow.ravel())
+        remap = {int(b): i for i, b in enumerate(ids)}
+        pool = W.random_bits16((2, len(ids), hkv, B, d), reps)
+        pairs = np.array([[remap[int(a)], remap[int(b)]] for a, b in cow], dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.block_copy(pool, pool, pairs)
+        secs += time.perf_counter() - t0
+        moved += len(pairs) * 2 * plan.block_bytes * 2
+        sl = plan.slot_mapping[:256]
+        blocks = np.unique(sl // B)
+        bmap = {int(b): i for i, b in enumerate(blocks)}
+        small_slots = np.array([bmap[int(x) // B] * B + int(x) % B for x in sl], dtype=np.int64)
+        kc = W.random_bits16((len(blocks), hkv, B, d), reps + 1)
+        new = W.random_bits16((len(sl), hkv, d), reps + 2)
+        t0 = time.perf_counter()
+        oracle.kv_append(new, new, small_slots, kc, kc, B)
+        secs += time.perf_counter() - t0
+        moved += 2 * len(sl) * hkv * d * 2 * 2
+        reps += 1
+    return secs, moved, reps
+
+
+def run_native_kvmove(args):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    peaks, peak_src = load_peaks()
+    metric, unit, hib = metric_for("kvmove")
+    sessions = args.seqs or 64
+    plan = W.kvmove_plan(seed=5, num_layers=args.layers, num_sessions=sessions,
+                         swap_sessions=max(1, sessions // 8))
+    step_obj = KVMoveStep(plan, dev)
+    h2d = h2d_peak_gbs(dev)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step_obj.step()
+    torch.cuda.synchronize()
+    flags = step_obj.pkg.device_status()
+    if flags:
+        raise RuntimeError(f"device status after warm-up: {step_obj.pkg.status_names(flags)}")
+    K = args.steps
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record()
+        for i in range(K):
+            step_obj.step(evs[i])
+        stop.record()
+        torch.cuda.synchronize()
+    barrier(dist)
+    ms_step = max_over_ranks(dist, start.elapsed_time(stop), dev) / K
+    cow_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    app_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    swap_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+    step_bytes = step_obj.bytes_cow + step_obj.bytes_append + step_obj.bytes_swap
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    flags = step_obj.pkg.device_status()
+    if rank != 0:
+        return
+    cow_gbs = step_obj.bytes_cow / (cow_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": cow_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": cow_gbs / peaks["hbm_gbs"], "traffic": None,
+            "algorithmic_bytes": step_obj.bytes_cow,
+            "kernel": "block_copy (copy-on-write, device pool, all resident layers, K and V)",
+            "peak_source": f"hbm_gbs of {peak_src}"}
+    swap_gbs = step_obj.bytes_swap / 2 / (swap_ms * 1e-3) / 1e9
+    t, moved, reps = kvmove_oracle_sample(plan, args.cpu_seconds)
+    cpu = {"value": moved / t / 1e9, "unit": unit, "cores": 1, "kind": "oracle",
+           "sample": f"numpy block copy of 64 copy-on-write pairs (one layer, K and V) and append of "
+                     f"256 tokens, {reps} repetitions, {t:.1f}s"}
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": hib,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT["kvmove"], "layers_resident": plan.num_layers,
+                       "l2": "inputs larger than L2 (pool %.1f GB)" % (step_obj.pool.numel() * 2 / 1e9),
+                       "bytes_per_step": step_bytes, "cow_pairs": len(plan.cow_pairs),
+                       "swap_blocks": len(plan.swap_pairs), "append_tokens": len(plan.slot_mapping),
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "swap_in": {"achieved": swap_gbs, "unit": "GB/s (host bytes read)", "peak": h2d,
+                        "frac": swap_gbs / h2d, "peak_source": "pinned host->device copy measured in this run",
+                        "ms": swap_ms},
+            "append": {"ms": app_ms, "achieved": step_obj.bytes_append / (app_ms * 1e-3) / 1e9},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": step_obj.bytes_swap / 2,
+                    "d2h_bytes_per_step": 0, "note": "the swap-in reads its blocks from pinned host memory inside the step"},
+            "gpu_launches": step_obj.launches_per_step * K, "device_status": flags,
+            "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -490,13 +697,17 @@ def main():
     ap.add_argument("--workload", default="decode13b", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=8,
+                    help="kvmove only: layers resident on the GPU (of 40)")
     ap.add_argument("--seqs", type=int, default=None,
-                    help="number of sequences (defaults 64 / 64 / 8; smaller for profiling runs)")
+                    help="number of sequences or sessions (defaults 64 / 64 / 8 / 64; smaller for profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "kvmove":
+        run_native_kvmove(args)
     else:
         run_native(args)
 
