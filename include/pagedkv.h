@@ -82,7 +82,7 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
  * Supported: dtype f32 / bf16 / f16; d in {64, 128}; B in {16, 32, 64, 128}; Hq % Hkv == 0;
  * 16-byte aligned q, out and caches; kv_block_stride * element size a multiple of 16 bytes.
  * Sequences with q_len * g >= 16 query rows per KV head run on the tcgen05 tensor-core kernel when
- * the dtype is bf16/f16, d = 128, g divides 128 and scale >= 0; decode steps, short turns and
+ * the dtype is bf16/f16, d = 128, g divides 128 and scale > 0; decode steps, short turns and
  * everything else run on the CUDA-core split-KV kernel.
  * ---------------------------------------------------------------------------------------- */
 typedef struct {

@@ -170,7 +170,7 @@ pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, co
     a.num_sms = sm_count();
     if (!a.status || a.num_sms <= 0) return PA_ERR_CUDA;
     a.maybe_prefill = d.total_q > d.num_seqs;
-    a.tc = a.maybe_prefill && scale >= 0.f && tc_supported(d);
+    a.tc = a.maybe_prefill && scale > 0.f && tc_supported(d);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (launch_plan(a, s) != cudaSuccess) return PA_ERR_CUDA;
     if (a.tc && launch_tc(a, s) != cudaSuccess) return PA_ERR_CUDA;

@@ -133,7 +133,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     int64_t target = (int64_t)p.total_warps * 16;
     if (target > kMaxTargetItems) target = kMaxTargetItems;
     int64_t chunk = (work + target - 1) / (target > 0 ? target : 1);
-    if (chunk < 1) chunk = 1;
+    // at least kMinSplitTokens keys per split, so a warp's pipeline fill and its partial record
+    // stay small next to the keys it streams
+    const int64_t min_chunk = (kMinSplitTokens + p.block_size - 1) / p.block_size;
+    if (chunk < min_chunk) chunk = min_chunk;
     if (tid == 0) p.counters[kChunkBlocks] = (uint32_t)chunk;
 
     // pass C: per-sequence counts

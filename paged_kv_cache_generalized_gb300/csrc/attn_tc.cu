@@ -65,9 +65,12 @@ constexpr int kSmBytes = kSmBar + 256 + 1024;   // barriers, tensor-memory slot,
 enum Bar {
     kKFull0 = 0, kKEmpty0 = kKFull0 + kKStages, kVFull0 = kKEmpty0 + kKStages,
     kVEmpty0 = kVFull0 + kVStages, kSFull0 = kVEmpty0 + kVStages, kSFull1, kPFull, kOReady, kQFull,
-    kDrain, kNumBars
+    kDrain, kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1, kNumBars
 };
-static_assert(kNumBars * 8 + 4 <= 256, "barrier area");
+// Tiles are claimed dynamically from a global counter by the K producer and handed to the other
+// six warps through a two-slot ring in shared memory.
+constexpr int kItemConsumers = 6;   // V producer, MMA issuer, four softmax warps
+static_assert(kNumBars * 8 + 4 + 8 <= 256, "barrier area");
 
 // ---- tcgen05 / TMA wrappers -----------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
@@ -180,6 +183,13 @@ __device__ __forceinline__ void tmem_store64(uint32_t taddr, const uint32_t (&r)
         : "memory");
 }
 
+// Maximum of three floats in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -275,13 +285,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kSmBar + kNumBars * 8);
+    volatile int *item_ring = reinterpret_cast<volatile int *>(smem + kSmBar + kNumBars * 8 + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr bool kF16 = std::is_same<T, __half>::value;
     const uint32_t idesc_qk = instr_desc(false, kF16);
     const uint32_t idesc_pv = instr_desc(true, kF16);
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], (b == kPFull || b == kQFull) ? 4 : 1);
+        for (int b = 0; b < kNumBars; ++b) {
+            uint32_t count = 1;
+            if (b == kPFull || b == kQFull) count = 4;
+            if (b == kItemEmpty0 || b == kItemEmpty1) count = kItemConsumers;
+            mbar_init(&bars[b], count);
+        }
         mbar_fence_init();
     }
     if (warp == kMmaWarp) {
@@ -296,6 +312,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int total = (int)p.counters[kTcTotal];
+    uint32_t *next_item = const_cast<uint32_t *>(p.counters) + kTcNext;
+    // next tile for every warp but the K producer: -1 = no more work, -2 = the wait timed out
+    auto receive_item = [&](uint32_t n) -> int {
+        const int slot = n & 1;
+        if (!warp_wait(&bars[kItemFull0 + slot], (n >> 1) & 1)) return -2;
+        const int it = item_ring[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
+        return it;
+    };
     const int B = p.block_size;
     const int bpt = kKeys / B;   // blocks per KV tile
 
@@ -309,7 +335,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t iter = 0;
         uint32_t armed[3] = {0, 0, 0};
         bool ok = true;
-        for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        for (uint32_t n = 0; ok; ++n) {
+            int it;
+            if (is_k) {
+                const int slot = n & 1;
+                if (n >= 2 && !warp_wait(&bars[kItemEmpty0 + slot], ((n >> 1) - 1) & 1)) { ok = false; break; }
+                if (lane == 0) {
+                    const uint32_t claimed = atomicAdd(next_item, 1u);
+                    item_ring[slot] = claimed < (uint32_t)total ? (int)claimed : -1;
+                    mbar_arrive(&bars[kItemFull0 + slot]);
+                }
+                __syncwarp();
+                it = item_ring[slot];
+            } else {
+                it = receive_item(n);
+                if (it == -2) { ok = false; break; }
+            }
+            if (it < 0) break;
             const Item t = decode_item(p, it);
             const int32_t *bt_row = p.bt + (int64_t)t.seq * p.max_blocks;
             int nblk_next = 0;
@@ -360,7 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             return true;
         };
-        for (int it = blockIdx.x; it < total && ok; it += gridDim.x, ++items) {
+        for (uint32_t n = 0; ok; ++n, ++items) {
+            const int it = receive_item(n);
+            if (it == -2) { ok = false; break; }
+            if (it < 0) break;
             const Item t = decode_item(p, it);
             if (!warp_wait(&bars[kQFull], items & 1)) { ok = false; break; }   // Q rows in tensor memory
             tc_fence_after();
@@ -410,10 +455,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        const float c_log2 = p.scale_log2;            // >= 0 (negative scales use CUDA cores)
+        const float c_log2 = p.scale_log2;            // > 0 (other scales use CUDA cores)
         uint32_t iter = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+        for (uint32_t n = 0; ok; ++n) {
+            const int it = receive_item(n);
+            if (it == -2) { ok = false; break; }
+            if (it < 0) break;
             const Item t = decode_item(p, it);
             const int j = t.j0 + row / p.group, hh = row % p.group;
             // this row of Q -> tensor memory (the previous item's MMAs are all complete: its
@@ -454,20 +502,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t key0 = (int64_t)kt * kKeys;
                 const bool diag = key0 + kKeys - 1 > t.pmin;  // tile crosses some row's diagonal
                 const int64_t lim = prow - key0;               // visible columns: 0 .. lim
+                // masked scores become -inf, so their exp2 below is exactly 0 (scale > 0 here)
                 if (diag) {
 #pragma unroll
                     for (int i = 0; i < kKeys; ++i)
                         if (i > lim) x[i] = -INFINITY;
                 }
-                // row max of the raw scores (scale >= 0 keeps the order), 8 independent chains
+                // row max of the raw scores (scale > 0 keeps the order): 8 chains of 3-input max
                 float mx[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) mx[k] = x[k];
 #pragma unroll
-                for (int i = 8; i < kKeys; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+                for (int i = 8; i + 16 <= kKeys; i += 16)       // columns 8 .. 119
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
-                const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                    for (int k = 0; k < 8; ++k) mx[k] = max3(mx[k], x[i + k], x[i + 8 + k]);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], x[kKeys - 8 + k]);   // 120 .. 127
+                const float mraw = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                 const float mt = (mraw == -INFINITY) ? -INFINITY : mraw * c_log2;
                 const float mnew = fmaxf(m, mt);
                 const bool rescale = mnew > m + kRescaleThreshold;
@@ -479,12 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 8; ++k) ls[k] = 0.f;
 #pragma unroll
                 for (int i = 0; i < kKeys / 2; ++i) {
-                    float e0 = fast_exp2(fmaf(x[2 * i], c_log2, -muse));
-                    float e1 = fast_exp2(fmaf(x[2 * i + 1], c_log2, -muse));
-                    if (diag) {
-                        if (2 * i > lim) e0 = 0.f;
-                        if (2 * i + 1 > lim) e1 = 0.f;
-                    }
+                    const float e0 = fast_exp2(fmaf(x[2 * i], c_log2, -muse));
+                    const float e1 = fast_exp2(fmaf(x[2 * i + 1], c_log2, -muse));
                     ls[i & 7] += e0 + e1;
                     pk[i] = pack2<T>(e0, e1);
                 }

@@ -22,6 +22,8 @@ constexpr int kMaxSplits = 64;
 // The planner sizes splits for about 16 work items per warp of the persistent grid, capped here
 // (enough for 256 SMs x 8 warps); the workspace bound on split partials follows from it.
 constexpr int64_t kMaxTargetItems = 32768;
+// Smallest KV split of a CUDA-core work item, in keys.
+constexpr int kMinSplitTokens = 256;
 
 // Counters at the start of the workspace.
 enum Counter : int {

@@ -189,7 +189,7 @@ def _forward_with_workspace(b):
 TC_CASES = [
     # name, ctx, q, Hq, Hkv, B, dtype, scale
     ("tc_one_tile", [0], [128], 1, 1, 16, "bf16", None),
-    ("tc_one_tile_scale0", [0], [128], 1, 1, 16, "bf16", 0.0),
+    ("tc_one_tile_tiny_scale", [0], [128], 1, 1, 16, "bf16", 1e-30),   # weights ~uniform
     ("tc_ctx_not_multiple", [77], [100], 2, 2, 16, "bf16", None),
     ("tc_gqa4_b32", [1000, 31], [64, 200], 16, 4, 32, "bf16", None),
     ("tc_gqa8_f16", [260], [40], 16, 2, 64, "f16", None),
