@@ -208,7 +208,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
             int32_t tiles = 0;
             if (i >= 0) {
                 const int64_t rows = (int64_t)p.qlen[i] * p.group;
-                tiles = p.kv_heads * (int32_t)((rows + kTcTileRows - 1) / kTcTileRows);
+                const int64_t tph = (rows + kTcTileRows - 1) / kTcTileRows;
+                tiles = p.kv_heads * (int32_t)((tph + kTcTilesPerItem - 1) / kTcTilesPerItem);
             }
             p.tc_cu[r] = tiles;
         }

@@ -7,27 +7,26 @@
 // is written out).  Scores are computed tile by tile with an online softmax
 // ("KVキャッシュ管理の教科書" 第6章, FlashAttention's tiling in on-chip memory).
 //
-// One work item is a tile of 128 query rows of one sequence and one KV head.  Rows are
-// (token, head-in-GQA-group) pairs, so the g query heads sharing a KV head are packed into the
-// same tile (M = 128 even for short turns with GQA).  Per 128-key tile:
-//   S = Q K^T   (tcgen05.mma, M=N=128, K=d=128: Q from tensor memory, K from shared memory)
-//   P = exp2(S * scale * log2 e - m), causal mask on diagonal tiles only, P -> 16 bits
-//   O += P V    (tcgen05.mma: P from tensor memory, V from shared memory (MN-major))
-// Q and P live in tensor memory, so the tensor cores read only K and V from shared memory and P
-// never goes through shared memory.  P overwrites the S buffer it was computed from (the MMAs of
-// one CTA execute in issue order, so the next S into that buffer comes after the PV that reads
-// P).  The running max is only moved (and O rescaled in tensor memory) when it grows by more than
-// 2^8; only then does the softmax wait for the previous PV.  The final O / l is exact either way.
+// A work item is a pair of 128-row query tiles of one sequence and one KV head (rows are
+// (token, head-in-GQA-group) pairs, so the g query heads sharing a KV head fill the tiles even for
+// short turns).  Both tiles walk the same 128-key K/V tiles, which are loaded once per pair:
+//   S_t = Q_t K^T   (tcgen05.mma, M=N=128, K=d=128, Q_t and K from shared memory)
+//   P_t = exp2(S_t * scale * log2 e - m_t), causal mask on diagonal tiles only, 16-bit
+//   O_t += P_t V    (tcgen05.mma, P_t from tensor memory (over S_t), V from shared memory)
+// The MMA warp interleaves the two tiles -- PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) -- so the tensor
+// cores work on one tile while the other tile's softmax runs.  The running max is only moved (and
+// O_t rescaled in tensor memory) when it grows by more than 2^8; the final O / l is exact anyway.
 //
-// Warp roles (224 threads, one CTA per SM, persistent over the tile list):
-//   warps 0, 6  TMA producers for K and for V: per 128-key tile one 3-D box (64 columns x B rows
-//               of one (block, head)) per block and panel, 128-byte swizzled, 3 stages each; the
-//               block-table entries of the next tile are fetched while the current one is issued.
+// Warp roles (352 threads, one CTA per SM, persistent; items claimed from a global counter):
+//   warp 0      TMA producer for Q (both tiles, once per item) and K: per 128-key tile one 3-D
+//               box (64 columns x B rows of one (block, head)) per block and panel, 128-byte
+//               swizzled, 3 stages; block-table entries of the next tile fetched ahead.
 //   warp 1      MMA issuer (one lane) and tensor-memory owner; zeroes V rows past the last key of
-//               a sequence's final tile (those slots may hold anything, NaN included).
-//   warps 2-5   softmax: one thread per tile row (tensor-memory lane): loads its Q row into tensor
-//               memory once per item, then per tile S -> P, and the epilogue O / l -> out.
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256,384), Q [384,448).
+//               a pair's final tile (those slots may hold anything, NaN included).
+//   warp 2      TMA producer for V (2 stages).
+//   warps 3-6   softmax of tile 0, warps 7-10 softmax of tile 1: one thread per row
+//               (tensor-memory lane), S -> P per KV tile, epilogue O / l -> out.
+// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
 // Every wait is bounded; on a timeout the role reports PA_DEV_TIMEOUT and stops, the kernel
 // drains what it issued, frees its tensor memory and returns.
 #include <cuda.h>
@@ -46,30 +45,32 @@ constexpr int kKeys = 128;          // keys per KV tile (UMMA N of QK^T, K of PV
 constexpr int kDim = 128;           // head_dim
 constexpr int kPanel = 128 * 128;   // bytes of one 64-column panel of a 128-row tile (16 KiB)
 constexpr int kTile = 2 * kPanel;   // one 128 x 128 16-bit tile (32 KiB)
-constexpr int kThreads = 224;
-constexpr int kKWarp = 0, kMmaWarp = 1, kVWarp = 6;
+constexpr int kThreads = 352;
+constexpr int kKWarp = 0, kMmaWarp = 1, kVWarp = 2, kSoftmax0 = 3;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemQ = 384;
+// tensor-memory columns of S_u and O_u for query tile u of the pair
+__host__ __device__ constexpr uint32_t tmem_s(int u) { return u ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t tmem_o(int u) { return u ? 384u : 256u; }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 2^8
 
-// K and V are each triple-buffered: a stage is refilled once the MMA that read it is done.
-constexpr int kKStages = 3;
-constexpr int kVStages = 3;
+constexpr int kKStages = 3;   // K(j) is freed once both S(j) are done and needed one step later
+constexpr int kVStages = 2;   // V(j) is freed once both PV(j) are done and needed two steps later
 
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int kSmK = 0;
+constexpr int kSmQ = 0;                          // two Q tiles
+constexpr int kSmK = kSmQ + 2 * kTile;
 constexpr int kSmV = kSmK + kKStages * kTile;
 constexpr int kSmBar = kSmV + kVStages * kTile;
-constexpr int kSmBytes = kSmBar + 256 + 1024;   // barriers, tensor-memory slot, alignment slack
+constexpr int kSmBytes = kSmBar + 256 + 1024;    // barriers, tensor-memory slot, alignment slack
 
 enum Bar {
     kKFull0 = 0, kKEmpty0 = kKFull0 + kKStages, kVFull0 = kKEmpty0 + kKStages,
-    kVEmpty0 = kVFull0 + kVStages, kSFull0 = kVEmpty0 + kVStages, kSFull1, kPFull, kOReady, kQFull,
-    kDrain, kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1, kNumBars
+    kVEmpty0 = kVFull0 + kVStages, kSFull0 = kVEmpty0 + kVStages, kPFull0 = kSFull0 + 2,
+    kOReady0 = kPFull0 + 2, kQFull = kOReady0 + 2, kQEmpty, kDrain, kItemFull0, kItemEmpty0 = kItemFull0 + 2,
+    kNumBars = kItemEmpty0 + 2
 };
-// Tiles are claimed dynamically from a global counter by the K producer and handed to the other
-// six warps through a two-slot ring in shared memory.
-constexpr int kItemConsumers = 6;   // V producer, MMA issuer, four softmax warps
+// Items are claimed by the K producer and handed to the other ten warps through a two-slot ring.
+constexpr int kItemConsumers = 2 + 8;
 static_assert(kNumBars * 8 + 4 + 8 <= 256, "barrier area");
 
 // ---- tcgen05 / TMA wrappers -----------------------------------------------------------------
@@ -98,6 +99,17 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 __host__ __device__ constexpr uint32_t instr_desc(bool b_mn_major, bool f16) {
     return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
            ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// D (tensor memory) (+)= A (shared-memory descriptor) * B (shared-memory descriptor).
+__device__ __forceinline__ void umma_ss(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // D (tensor memory) (+)= A (tensor memory) * B (shared-memory descriptor).
@@ -224,7 +236,6 @@ __device__ __forceinline__ int find_rank(const int32_t *a, int n, int key) {
 }
 
 struct TcParams {
-    const char *q;
     char *out;
     const int32_t *bt, *ctx, *qlen;
     const int32_t *cu_q, *tc_cu, *tc_seq;
@@ -235,9 +246,14 @@ struct TcParams {
     int num_seqs, q_heads, kv_heads, group, block_size, max_blocks;
 };
 
+// One work item: query tiles qt0 = 2*pi and qt1 = 2*pi + 1 (if it exists) of one (sequence,
+// KV head).  Tile 1 holds later rows, so its causal range (and KV tile count) covers tile 0's.
 struct Item {
-    int seq, kvh, j0, rows_valid, ntiles;
-    int64_t tok0, pmin, pmax;
+    int seq, kvh, ntiles;         // ntiles: KV tiles of the pair (those of its last tile)
+    int64_t tok0;
+    bool two;                     // tile 1 exists
+    int j0[2], rows_valid[2], nt[2];
+    int64_t pmin[2], pmax[2];
 };
 
 __device__ __forceinline__ Item decode_item(const TcParams &p, int it) {
@@ -246,24 +262,31 @@ __device__ __forceinline__ Item decode_item(const TcParams &p, int it) {
     t.seq = __ldg(p.tc_seq + rank);
     const int local = it - __ldg(p.tc_cu + rank);
     const int rows = __ldg(p.qlen + t.seq) * p.group;
-    const int tph = (rows + kRows - 1) / kRows;
-    const int qt = tph - 1 - (local % tph);  // a sequence's last (longest) query tile first
-    t.kvh = local / tph;
-    t.j0 = qt * (kRows / p.group);
-    t.rows_valid = min(kRows, rows - qt * kRows);
+    const int tph = (rows + kRows - 1) / kRows;   // query tiles per KV head
+    const int pph = (tph + 1) / 2;                // tile pairs per KV head
+    const int pi = pph - 1 - (local % pph);       // a sequence's last (longest) pair first
+    t.kvh = local / pph;
     t.tok0 = __ldg(p.cu_q + t.seq);
     const int64_t c = __ldg(p.ctx + t.seq);
-    t.pmin = c + t.j0;
-    t.pmax = c + t.j0 + (t.rows_valid - 1) / p.group;
-    t.ntiles = (int)((t.pmax + kKeys) / kKeys);
+    t.two = 2 * pi + 1 < tph;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int qt = 2 * pi + (u == 1 && t.two ? 1 : 0);
+        t.j0[u] = qt * (kRows / p.group);
+        t.rows_valid[u] = min(kRows, rows - qt * kRows);
+        t.pmin[u] = c + t.j0[u];
+        t.pmax[u] = c + t.j0[u] + (t.rows_valid[u] - 1) / p.group;
+        t.nt[u] = (int)((t.pmax[u] + kKeys) / kKeys);
+    }
+    t.ntiles = t.two ? t.nt[1] : t.nt[0];
     return t;
 }
 
 // Physical block of each lane's block in KV tile kt (lanes < blocks of the tile), clamped.
-__device__ __forceinline__ int tile_block(const TcParams &p, const int32_t *bt_row, const Item &t,
+__device__ __forceinline__ int tile_block(const TcParams &p, const int32_t *bt_row, int64_t pmax,
                                           int kt, int bpt, int lane, int &nblk) {
     const int64_t key0 = (int64_t)kt * kKeys;
-    const int64_t keys = min((int64_t)kKeys, t.pmax + 1 - key0);
+    const int64_t keys = min((int64_t)kKeys, pmax + 1 - key0);
     nblk = (int)((keys + p.block_size - 1) / p.block_size);
     int phys = 0;
     if (lane < nblk) {
@@ -278,8 +301,8 @@ __device__ __forceinline__ int tile_block(const TcParams &p, const int32_t *bt_r
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                        TcParams p) {
+    tc_attention_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, TcParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -294,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b) {
             uint32_t count = 1;
-            if (b == kPFull || b == kQFull) count = 4;
-            if (b == kItemEmpty0 || b == kItemEmpty1) count = kItemConsumers;
+            if (b == kPFull0 || b == kPFull0 + 1) count = 4;
+            if (b == kItemEmpty0 || b == kItemEmpty0 + 1) count = kItemConsumers;
             mbar_init(&bars[b], count);
         }
         mbar_fence_init();
@@ -313,7 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const int total = (int)p.counters[kTcTotal];
     uint32_t *next_item = const_cast<uint32_t *>(p.counters) + kTcNext;
-    // next tile for every warp but the K producer: -1 = no more work, -2 = the wait timed out
+    const int B = p.block_size;
+    const int bpt = kKeys / B;   // blocks per KV tile
+    // next item for every warp but the K producer: -1 = no more work, -2 = the wait timed out
     auto receive_item = [&](uint32_t n) -> int {
         const int slot = n & 1;
         if (!warp_wait(&bars[kItemFull0 + slot], (n >> 1) & 1)) return -2;
@@ -322,18 +347,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
         return it;
     };
-    const int B = p.block_size;
-    const int bpt = kKeys / B;   // blocks per KV tile
 
     if (warp == kKWarp || warp == kVWarp) {
-        // ------------------------------------------------------------ TMA producers (K or V)
+        // ------------------------------------------------------------ TMA producers (Q+K or V)
         const bool is_k = warp == kKWarp;
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         const int full0 = is_k ? kKFull0 : kVFull0, empty0 = is_k ? kKEmpty0 : kVEmpty0;
         const int nst = is_k ? kKStages : kVStages;
         unsigned char *stage0 = smem + (is_k ? kSmK : kSmV);
-        uint32_t iter = 0;
-        uint32_t armed[3] = {0, 0, 0};
+        uint32_t iter = 0, items = 0;
+        uint32_t armed[3] = {0, 0, 0}, armed_q = 0;
         bool ok = true;
         for (uint32_t n = 0; ok; ++n) {
             int it;
@@ -353,12 +376,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (it < 0) break;
             const Item t = decode_item(p, it);
+            if (is_k) {
+                // both query tiles of the pair (the previous pair's S MMAs are done with Q)
+                if (items > 0 && !warp_wait(&bars[kQEmpty], (items - 1) & 1)) { ok = false; break; }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[kQFull], (t.two ? 2 : 1) * kTile);
+                    const int y = t.kvh * p.group;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        if (u == 1 && !t.two) break;
+                        const int z = (int)(t.tok0 + t.j0[u]);
+                        tma_load_3d(smem + kSmQ + u * kTile, &qmap, 0, y, z, &bars[kQFull]);
+                        tma_load_3d(smem + kSmQ + u * kTile + kPanel, &qmap, 64, y, z, &bars[kQFull]);
+                    }
+                }
+                ++armed_q;
+            }
+            ++items;
+            const int64_t pmax = t.two ? t.pmax[1] : t.pmax[0];
             const int32_t *bt_row = p.bt + (int64_t)t.seq * p.max_blocks;
             int nblk_next = 0;
-            int phys_next = tile_block(p, bt_row, t, 0, bpt, lane, nblk_next);
+            int phys_next = tile_block(p, bt_row, pmax, 0, bpt, lane, nblk_next);
             for (int kt = 0; kt < t.ntiles; ++kt, ++iter) {
                 const int phys = phys_next, nblk = nblk_next;
-                if (kt + 1 < t.ntiles) phys_next = tile_block(p, bt_row, t, kt + 1, bpt, lane, nblk_next);
+                if (kt + 1 < t.ntiles) phys_next = tile_block(p, bt_row, pmax, kt + 1, bpt, lane, nblk_next);
                 const int s = iter % nst;
                 const uint32_t use = iter / nst;
                 if (use > 0 && !warp_wait(&bars[empty0 + s], (use - 1) & 1)) { ok = false; break; }
@@ -378,26 +419,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every copy this warp issued lands before the CTA can exit
         for (int s = 0; s < nst; ++s)
             if (armed[s]) mbar_wait(&bars[full0 + s], (armed[s] - 1) & 1);
+        if (armed_q) mbar_wait(&bars[kQFull], (armed_q - 1) & 1);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
-        uint32_t iter = 0, items = 0;
+        uint32_t iter = 0, items = 0, pcount[2] = {0, 0};
         bool ok = true;
-        const uint32_t k_base = smem_addr(smem + kSmK), v_base = smem_addr(smem + kSmV);
-        auto issue_s = [&](uint32_t g) -> bool {
-            const uint32_t s_tmem = tmem + ((g & 1) ? kTmemS1 : kTmemS0);
-            const int ks = g % kKStages;
-            if (!warp_wait(&bars[kKFull0 + ks], (g / kKStages) & 1)) return false;
+        const uint32_t q_base = smem_addr(smem + kSmQ), k_base = smem_addr(smem + kSmK),
+                       v_base = smem_addr(smem + kSmV);
+        auto wait_k = [&](uint32_t g) -> bool {
+            if (!warp_wait(&bars[kKFull0 + g % kKStages], (g / kKStages) & 1)) return false;
             tc_fence_after();
+            return true;
+        };
+        auto issue_s = [&](int u, uint32_t g) {   // S_u = Q_u K(g)^T
             if (lane == 0) {
-                const uint32_t k_addr = k_base + ks * kTile;
+                const uint32_t q_addr = q_base + u * kTile, k_addr = k_base + (g % kKStages) * kTile;
 #pragma unroll
                 for (int k = 0; k < kDim / 16; ++k) {
                     const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
-                    umma_ts(s_tmem, tmem + kTmemQ + k * 8, smem_desc(k_addr + off, 16, 1024), idesc_qk,
-                            k > 0);
+                    umma_ss(tmem + tmem_s(u), smem_desc(q_addr + off, 16, 1024),
+                            smem_desc(k_addr + off, 16, 1024), idesc_qk, k > 0);
                 }
-                umma_commit(&bars[kSFull0 + (g & 1)]);
-                umma_commit(&bars[kKEmpty0 + ks]);
+                umma_commit(&bars[kSFull0 + u]);
+            }
+            __syncwarp();
+        };
+        auto issue_pv = [&](int u, uint32_t g, bool first) -> bool {   // O_u += P_u V(g)
+            if (!warp_wait(&bars[kPFull0 + u], pcount[u] & 1)) return false;
+            ++pcount[u];
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t v_addr = v_base + (g % kVStages) * kTile;
+#pragma unroll
+                for (int k = 0; k < kKeys / 16; ++k)
+                    umma_ts(tmem + tmem_o(u), tmem + tmem_s(u) + k * 8,
+                            smem_desc(v_addr + k * 16 * 128, kPanel, 1024), idesc_pv, (!first || k > 0) ? 1u : 0u);
+                umma_commit(&bars[kOReady0 + u]);
             }
             __syncwarp();
             return true;
@@ -407,17 +464,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it == -2) { ok = false; break; }
             if (it < 0) break;
             const Item t = decode_item(p, it);
-            if (!warp_wait(&bars[kQFull], items & 1)) { ok = false; break; }   // Q rows in tensor memory
+            if (!warp_wait(&bars[kQFull], items & 1)) { ok = false; break; }
             tc_fence_after();
-            if (!issue_s(iter)) { ok = false; break; }
+            if (!wait_k(iter)) { ok = false; break; }
+            issue_s(0, iter);
+            if (t.two) issue_s(1, iter);
+            if (lane == 0) umma_commit(&bars[kKEmpty0 + iter % kKStages]);
+            __syncwarp();
             for (int kt = 0; kt < t.ntiles; ++kt) {
                 const uint32_t g = iter + kt;
-                if (kt + 1 < t.ntiles && !issue_s(g + 1)) { ok = false; break; }
-                if (!warp_wait(&bars[kPFull], g & 1)) { ok = false; break; }
+                const bool last = kt + 1 == t.ntiles;
+                const bool act0 = kt < t.nt[0];
                 const int vs = g % kVStages;
                 if (!warp_wait(&bars[kVFull0 + vs], (g / kVStages) & 1)) { ok = false; break; }
-                // zero V rows past the last key any row of this tile sees (free or stale slots)
-                const int64_t valid = t.pmax + 1 - (int64_t)kt * kKeys;
+                // zero V rows past the last key any row of the pair sees (free or stale slots)
+                const int64_t valid = (t.two ? t.pmax[1] : t.pmax[0]) + 1 - (int64_t)kt * kKeys;
                 if (valid < kKeys) {
                     unsigned char *vb = smem + kSmV + vs * kTile;
                     const int first = (int)valid;
@@ -430,19 +491,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t p_tmem = tmem + ((g & 1) ? kTmemS1 : kTmemS0);
-                    const uint32_t v_addr = v_base + vs * kTile;
-#pragma unroll
-                    for (int k = 0; k < kKeys / 16; ++k)
-                        umma_ts(tmem + kTmemO, p_tmem + k * 8, smem_desc(v_addr + k * 16 * 128, kPanel, 1024),
-                                idesc_pv, (kt > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(&bars[kOReady]);
-                    umma_commit(&bars[kVEmpty0 + vs]);
+                if (act0 && !issue_pv(0, g, kt == 0)) { ok = false; break; }
+                if (!last) {
+                    if (!wait_k(g + 1)) { ok = false; break; }
+                    if (kt + 1 < t.nt[0]) issue_s(0, g + 1);
                 }
+                if (t.two && !issue_pv(1, g, kt == 0)) { ok = false; break; }
+                if (lane == 0) umma_commit(&bars[kVEmpty0 + vs]);
                 __syncwarp();
+                if (!last) {
+                    if (t.two) issue_s(1, g + 1);
+                    if (lane == 0) umma_commit(&bars[kKEmpty0 + (g + 1) % kKStages]);
+                    __syncwarp();
+                }
             }
+            // Q is free once every S of the pair is done
+            if (lane == 0) umma_commit(&bars[kQEmpty]);
+            __syncwarp();
             iter += t.ntiles;
         }
         if (!ok && lane == 0) report(p.status, PA_DEV_TIMEOUT);
@@ -452,56 +517,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bars[kDrain], 0);
     } else {
         // ------------------------------------------------------------------ softmax warps
-        const int quad = warp & 3;
+        const int u = (warp - kSoftmax0) >> 2;          // query tile of the pair this warp serves
+        const int quad = warp & 3;                      // tensor-memory lanes this warp may access
         const int row = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const uint32_t s_tmem = lane_base + tmem_s(u), o_tmem = lane_base + tmem_o(u);
         const float c_log2 = p.scale_log2;            // > 0 (other scales use CUDA cores)
-        uint32_t iter = 0;
+        uint32_t scount = 0;                           // S / PV tiles of this query tile so far
         bool ok = true;
         for (uint32_t n = 0; ok; ++n) {
             const int it = receive_item(n);
             if (it == -2) { ok = false; break; }
             if (it < 0) break;
             const Item t = decode_item(p, it);
-            const int j = t.j0 + row / p.group, hh = row % p.group;
-            // this row of Q -> tensor memory (the previous item's MMAs are all complete: its
-            // epilogue waited for its last PV, which follows every S of that item)
-            {
-                uint32_t qr[64];
-                if (row < t.rows_valid) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        p.q + (((t.tok0 + j) * p.q_heads + (int64_t)t.kvh * p.group + hh) * kDim) * sizeof(T));
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const uint4 v = __ldg(src + c);
-                        qr[4 * c] = v.x;
-                        qr[4 * c + 1] = v.y;
-                        qr[4 * c + 2] = v.z;
-                        qr[4 * c + 3] = v.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) qr[c] = 0u;
-                }
-                tmem_store64(lane_base + kTmemQ, qr);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kQFull]);
-            }
-            int64_t prow = t.pmin + row / p.group;
-            if (prow > t.pmax) prow = t.pmax;             // padding rows: finite, never stored
+            if (u == 1 && !t.two) continue;
+            const int64_t pmin = t.pmin[u], pmax = t.pmax[u];
+            const int nt = t.nt[u];
+            const int j = t.j0[u] + row / p.group, hh = row % p.group;
+            int64_t prow = pmin + row / p.group;
+            if (prow > pmax) prow = pmax;               // padding rows: finite, never stored
             float m = -INFINITY, l = 0.f;
-            for (int kt = 0; kt < t.ntiles; ++kt) {
-                const uint32_t g = iter + kt;
-                const uint32_t s_tmem = lane_base + ((g & 1) ? kTmemS1 : kTmemS0);
-                if (!warp_wait(&bars[kSFull0 + (g & 1)], (g >> 1) & 1)) { ok = false; break; }
+            for (int kt = 0; kt < nt; ++kt, ++scount) {
+                if (!warp_wait(&bars[kSFull0 + u], scount & 1)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t raw[kKeys];
                 tmem_load128(s_tmem, raw);
                 float *x = reinterpret_cast<float *>(raw);   // raw scores q.k (unscaled)
                 const int64_t key0 = (int64_t)kt * kKeys;
-                const bool diag = key0 + kKeys - 1 > t.pmin;  // tile crosses some row's diagonal
-                const int64_t lim = prow - key0;               // visible columns: 0 .. lim
+                const bool diag = key0 + kKeys - 1 > pmin;   // tile crosses some row's diagonal
+                const int64_t lim = prow - key0;             // visible columns: 0 .. lim
                 // masked scores become -inf, so their exp2 below is exactly 0 (scale > 0 here)
                 if (diag) {
 #pragma unroll
@@ -541,17 +585,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tensor-memory loads/stores are warp-collective: the whole warp rescales when any
                 // of its rows must (alpha = 1 for the others), after the previous PV is complete
                 if (kt > 0 && __any_sync(0xffffffffu, rescale)) {
-                    if (!warp_wait(&bars[kOReady], (g - 1) & 1)) { ok = false; break; }
+                    if (!warp_wait(&bars[kOReady0 + u], (scount - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
                     const float alpha = rescale ? fast_exp2(m - muse) : 1.f;
                     l *= alpha;
 #pragma unroll 1
                     for (int c = 0; c < kDim / 32; ++c) {
                         uint32_t r[32];
-                        tmem_load32(lane_base + kTmemO + c * 32, r);
+                        tmem_load32(o_tmem + c * 32, r);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_store32(lane_base + kTmemO + c * 32, r);
+                        tmem_store32(o_tmem + c * 32, r);
                     }
                 }
                 m = muse;
@@ -560,21 +604,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_store64(s_tmem, pk);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kPFull]);
+                if (lane == 0) mbar_arrive(&bars[kPFull0 + u]);
             }
             if (!ok) break;
-            // epilogue: O / l -> out, after the item's last PV
-            const uint32_t glast = iter + t.ntiles - 1;
-            if (!warp_wait(&bars[kOReady], glast & 1)) { ok = false; break; }
+            // epilogue: O / l -> out, after this tile's last PV
+            if (!warp_wait(&bars[kOReady0 + u], (scount - 1) & 1)) { ok = false; break; }
             tc_fence_after();
             const float inv = 1.f / l;
-            const bool store = row < t.rows_valid;
+            const bool store = row < t.rows_valid[u];
             T *orow = reinterpret_cast<T *>(p.out) +
                       ((t.tok0 + j) * p.q_heads + (int64_t)t.kvh * p.group + hh) * kDim;
 #pragma unroll 1
             for (int c = 0; c < kDim / 32; ++c) {
                 uint32_t r[32];
-                tmem_load32(lane_base + kTmemO + c * 32, r);
+                tmem_load32(o_tmem + c * 32, r);
                 if (store) {
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
@@ -588,7 +631,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            iter += t.ntiles;
         }
         if (!ok && lane == 0) report(p.status, PA_DEV_TIMEOUT);
     }
@@ -654,15 +696,16 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s) {
     const uint64_t es = 2;
     const int64_t bstride = d.kv_block_stride ? d.kv_block_stride
                                               : (int64_t)d.num_kv_heads * d.block_size * d.head_dim;
-    CUtensorMap kmap, vmap;
-    if (!make_map(&kmap, d.dtype, a.k, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
+    CUtensorMap qmap, kmap, vmap;
+    if (!make_map(&qmap, d.dtype, a.q, kDim, d.num_q_heads, d.total_q, kDim * es,
+                  (uint64_t)d.num_q_heads * kDim * es, g, kRows / g) ||
+        !make_map(&kmap, d.dtype, a.k, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
                   kDim * es, bstride * es, d.block_size, 1) ||
         !make_map(&vmap, d.dtype, a.v, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
                   kDim * es, bstride * es, d.block_size, 1))
         return cudaErrorInvalidValue;
     TcParams p;
     const WsLayout &L = a.lay;
-    p.q = static_cast<const char *>(a.q);
     p.out = static_cast<char *>(a.out);
     p.bt = a.bt;
     p.ctx = a.ctx;
@@ -684,11 +727,11 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s) {
     if (d.dtype == PA_F16) {
         e = cudaFuncSetAttribute(tc_attention_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmBytes);
         if (e != cudaSuccess) return e;
-        tc_attention_kernel<__half><<<a.num_sms, kThreads, kSmBytes, s>>>(kmap, vmap, p);
+        tc_attention_kernel<__half><<<a.num_sms, kThreads, kSmBytes, s>>>(qmap, kmap, vmap, p);
     } else {
         e = cudaFuncSetAttribute(tc_attention_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmBytes);
         if (e != cudaSuccess) return e;
-        tc_attention_kernel<__nv_bfloat16><<<a.num_sms, kThreads, kSmBytes, s>>>(kmap, vmap, p);
+        tc_attention_kernel<__nv_bfloat16><<<a.num_sms, kThreads, kSmBytes, s>>>(qmap, kmap, vmap, p);
     }
     return cudaGetLastError();
 }

@@ -17,6 +17,9 @@ constexpr int kMaxRowsPerItem = 4;
 constexpr int kTcMinRows = 16;
 // Rows of one tensor-core tile (UMMA M).
 constexpr int kTcTileRows = 128;
+// Query tiles of one (sequence, KV head) processed together by one tensor-core work item (they
+// share every K/V tile load).
+constexpr int kTcTilesPerItem = 2;
 // Upper bound on the KV splits of one CUDA-core work item's rows.
 constexpr int kMaxSplits = 64;
 // The planner sizes splits for about 16 work items per warp of the persistent grid, capped here
