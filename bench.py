@@ -349,6 +349,19 @@ WORKLOAD_TEXT = {
 }
 
 
+
+def workload_text(name, args):
+    """The workload's description; a run with --seqs / --layers says it is a reduced case."""
+    t = WORKLOAD_TEXT[name]
+    extra = []
+    if getattr(args, "seqs", None):
+        extra.append(f"--seqs {args.seqs}")
+    if name == "kvmove" and getattr(args, "layers", None):
+        extra.append(f"--layers {args.layers}")
+    if extra:
+        t += "; REDUCED case (" + ", ".join(extra) + "), not the headline workload"
+    return t
+
 # ------------------------------------------------------------------------------------------------
 # Distributed helpers (independent replicas; timing barrier and max over ranks only)
 # ------------------------------------------------------------------------------------------------
@@ -443,7 +456,7 @@ def run_reference(args):
         line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(1, args.steps) * 1e3,
                 "higher_is_better": hib, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-                "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[name]},
+                "data": "synthetic", "config": {"workload": workload_text(name, args)},
                 "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                                  "sample": "numpy block copy of 64 copy-on-write pairs and append of 256 tokens per repetition"},
                 "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -470,7 +483,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": secs / max(1, len(vals)) * 1e3, "higher_is_better": hib,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[name]},
+            "config": {"workload": workload_text(name, args)},
             "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
                              "sample": sample_desc},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -569,7 +582,7 @@ def run_native(args):
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": hib,
             "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype, "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[name],
+            "config": {"workload": workload_text(name, args),
                        "l2": "inputs larger than L2 (KV pool %.2f GB resident)" % (
                            (step_obj.pool.numel() * step_obj.pool.element_size()) / 1e9),
                        "bytes_per_step": step_bytes, "attn_flops_per_step": step_obj.flops,
@@ -671,7 +684,7 @@ def run_native_kvmove(args):
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": hib,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT["kvmove"], "layers_resident": plan.num_layers,
+            "config": {"workload": workload_text("kvmove", args), "layers_resident": plan.num_layers,
                        "l2": "inputs larger than L2 (pool %.1f GB)" % (step_obj.pool.numel() * 2 / 1e9),
                        "bytes_per_step": step_bytes, "cow_pairs": len(plan.cow_pairs),
                        "swap_blocks": len(plan.swap_pairs), "append_tokens": len(plan.slot_mapping),

@@ -208,6 +208,26 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Two fp32 values in one 64-bit register pair, for the packed fp32 instructions.
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
 template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -567,21 +587,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mnew = fmaxf(m, mt);
                 const bool rescale = mnew > m + kRescaleThreshold;
                 const float muse = rescale ? mnew : m;
-                // P = exp2(scale*log2e*s - m), packed to 16 bits; partial row sums in 8 chains
+                // P = exp2(scale*log2e*s - m), packed to 16 bits; the argument and the partial row
+                // sums (4 chains) use the packed two-lane fp32 instructions
                 uint32_t pk[kKeys / 2];
-                float ls[8];
+                const uint64_t c2 = f2pack(c_log2, c_log2), nm2 = f2pack(-muse, -muse);
+                uint64_t ls[4];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+                for (int k = 0; k < 4; ++k) ls[k] = 0ull;
 #pragma unroll
                 for (int i = 0; i < kKeys / 2; ++i) {
-                    const float e0 = fast_exp2(fmaf(x[2 * i], c_log2, -muse));
-                    const float e1 = fast_exp2(fmaf(x[2 * i + 1], c_log2, -muse));
-                    ls[i & 7] += e0 + e1;
+                    float y0, y1;
+                    f2unpack(fma2(f2pack(x[2 * i], x[2 * i + 1]), c2, nm2), y0, y1);
+                    const float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
+                    ls[i & 3] = add2(ls[i & 3], f2pack(e0, e1));
                     pk[i] = pack2<T>(e0, e1);
                 }
                 float lsum = 0.f;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) lsum += ls[k];
+                for (int k = 0; k < 4; ++k) {
+                    float a0, a1;
+                    f2unpack(ls[k], a0, a1);
+                    lsum += a0 + a1;
+                }
                 // tensor-memory loads/stores are warp-collective: the whole warp rescales when any
                 // of its rows must (alpha = 1 for the others), after the previous PV is complete
                 if (kt > 0 && __any_sync(0xffffffffu, rescale)) {
