@@ -442,99 +442,109 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (armed_q) mbar_wait(&bars[kQFull], (armed_q - 1) & 1);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------------ MMA issuer
-        uint32_t iter = 0, items = 0, pcount[2] = {0, 0};
-        bool ok = true;
-        const uint32_t q_base = smem_addr(smem + kSmQ), k_base = smem_addr(smem + kSmK),
-                       v_base = smem_addr(smem + kSmV);
-        auto wait_k = [&](uint32_t g) -> bool {
-            if (!warp_wait(&bars[kKFull0 + g % kKStages], (g / kKStages) & 1)) return false;
-            tc_fence_after();
-            return true;
-        };
-        auto issue_s = [&](int u, uint32_t g) {   // S_u = Q_u K(g)^T
-            if (lane == 0) {
-                const uint32_t q_addr = q_base + u * kTile, k_addr = k_base + (g % kKStages) * kTile;
+        // One thread runs this role: no warp-collective step sits between two MMA groups, so the
+        // tensor pipe is fed as soon as the operands of the next group are ready.
+        if (lane == 0) {
+            uint32_t iter = 0, items = 0, pcount[2] = {0, 0};
+            bool ok = true;
+            const uint32_t q_base = smem_addr(smem + kSmQ), k_base = smem_addr(smem + kSmK),
+                           v_base = smem_addr(smem + kSmV);
+            auto wait_bar = [&](int b, uint32_t parity) -> bool {
+                if (!mbar_wait(&bars[b], parity)) return false;
+                tc_fence_after();
+                return true;
+            };
+            auto wait_k = [&](uint32_t g) -> bool { return wait_bar(kKFull0 + g % kKStages, (g / kKStages) & 1); };
+            // Descriptors are built once; a tile, stage or k-step moves only the start-address
+            // field (address / 16, below 2^14 for any shared-memory address).
+            const uint64_t dq = smem_desc(q_base, 16, 1024), dk = smem_desc(k_base, 16, 1024),
+                           dv = smem_desc(v_base, kPanel, 1024);
+            auto issue_s = [&](int u, uint32_t g) {   // S_u = Q_u K(g)^T
+                const uint64_t a = dq + (uint64_t)(u * (kTile >> 4)),
+                               b = dk + (uint64_t)((g % kKStages) * (kTile >> 4));
+                const uint32_t d = tmem + tmem_s(u);
 #pragma unroll
                 for (int k = 0; k < kDim / 16; ++k) {
-                    const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
-                    umma_ss(tmem + tmem_s(u), smem_desc(q_addr + off, 16, 1024),
-                            smem_desc(k_addr + off, 16, 1024), idesc_qk, k > 0);
+                    const uint64_t off = (uint64_t)(((k >> 2) * kPanel + (k & 3) * 32) >> 4);
+                    umma_ss(d, a + off, b + off, idesc_qk, k > 0);
                 }
                 umma_commit(&bars[kSFull0 + u]);
-            }
-            __syncwarp();
-        };
-        auto issue_pv = [&](int u, uint32_t g, bool first) -> bool {   // O_u += P_u V(g)
-            if (!warp_wait(&bars[kPFull0 + u], pcount[u] & 1)) return false;
-            ++pcount[u];
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t v_addr = v_base + (g % kVStages) * kTile;
+            };
+            // O_u += P_u V(g) over the first `ksteps` 16-key steps (P is zero past them)
+            auto issue_pv = [&](int u, uint32_t g, bool first, int ksteps) -> bool {
+                if (!wait_bar(kPFull0 + u, pcount[u] & 1)) return false;
+                ++pcount[u];
+                const uint64_t b = dv + (uint64_t)((g % kVStages) * (kTile >> 4));
+                const uint32_t d = tmem + tmem_o(u), a = tmem + tmem_s(u);
+                if (ksteps == kKeys / 16) {
 #pragma unroll
-                for (int k = 0; k < kKeys / 16; ++k)
-                    umma_ts(tmem + tmem_o(u), tmem + tmem_s(u) + k * 8,
-                            smem_desc(v_addr + k * 16 * 128, kPanel, 1024), idesc_pv, (!first || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < kKeys / 16; ++k)
+                        umma_ts(d, a + k * 8, b + (uint64_t)(k * 128), idesc_pv, (!first || k > 0) ? 1u : 0u);
+                } else {
+#pragma unroll 1
+                    for (int k = 0; k < ksteps; ++k)
+                        umma_ts(d, a + k * 8, b + (uint64_t)(k * 128), idesc_pv, (!first || k > 0) ? 1u : 0u);
+                }
                 umma_commit(&bars[kOReady0 + u]);
-            }
-            __syncwarp();
-            return true;
-        };
-        for (uint32_t n = 0; ok; ++n, ++items) {
-            const int it = receive_item(n);
-            if (it == -2) { ok = false; break; }
-            if (it < 0) break;
-            const Item t = decode_item(p, it);
-            if (!warp_wait(&bars[kQFull], items & 1)) { ok = false; break; }
-            tc_fence_after();
-            if (!wait_k(iter)) { ok = false; break; }
-            issue_s(0, iter);
-            if (t.two) issue_s(1, iter);
-            if (lane == 0) umma_commit(&bars[kKEmpty0 + iter % kKStages]);
-            __syncwarp();
-            for (int kt = 0; kt < t.ntiles; ++kt) {
-                const uint32_t g = iter + kt;
-                const bool last = kt + 1 == t.ntiles;
-                const bool act0 = kt < t.nt[0];
-                const int vs = g % kVStages;
-                if (!warp_wait(&bars[kVFull0 + vs], (g / kVStages) & 1)) { ok = false; break; }
-                // zero V rows past the last key any row of the pair sees (free or stale slots)
-                const int64_t valid = (t.two ? t.pmax[1] : t.pmax[0]) + 1 - (int64_t)kt * kKeys;
-                if (valid < kKeys) {
-                    unsigned char *vb = smem + kSmV + vs * kTile;
-                    const int first = (int)valid;
-                    const int n16 = (kKeys - first) * 8;            // 16-byte chunks per panel
-                    for (int i = lane; i < 2 * n16; i += 32) {
-                        const int panel = i / n16, rem = i - panel * n16;
-                        *reinterpret_cast<uint4 *>(vb + panel * kPanel + first * 128 + rem * 16) =
-                            make_uint4(0, 0, 0, 0);
+                return true;
+            };
+            for (uint32_t n = 0; ok; ++n, ++items) {
+                const int slot = n & 1;
+                if (!mbar_wait(&bars[kItemFull0 + slot], (n >> 1) & 1)) { ok = false; break; }
+                const int it = item_ring[slot];
+                mbar_arrive(&bars[kItemEmpty0 + slot]);
+                if (it < 0) break;
+                const Item t = decode_item(p, it);
+                if (!wait_bar(kQFull, items & 1)) { ok = false; break; }
+                if (!wait_k(iter)) { ok = false; break; }
+                issue_s(0, iter);
+                if (t.two) issue_s(1, iter);
+                umma_commit(&bars[kKEmpty0 + iter % kKStages]);
+                for (int kt = 0; kt < t.ntiles; ++kt) {
+                    const uint32_t g = iter + kt;
+                    const bool last = kt + 1 == t.ntiles;
+                    const bool act0 = kt < t.nt[0];
+                    const int vs = g % kVStages;
+                    if (!wait_bar(kVFull0 + vs, (g / kVStages) & 1)) { ok = false; break; }
+                    // Keys past the last one any row of the pair sees have P = 0: PV skips the 16-key
+                    // steps made only of them, and the V rows of such keys inside the last step
+                    // (free or stale slots, possibly NaN) are zeroed so that 0 * V stays 0.
+                    const int64_t valid = (t.two ? t.pmax[1] : t.pmax[0]) + 1 - (int64_t)kt * kKeys;
+                    int ksteps = kKeys / 16;
+                    if (valid < kKeys) {
+                        ksteps = (int)((valid + 15) / 16);
+                        const int first = (int)valid, end = ksteps * 16;
+                        unsigned char *vb = smem + kSmV + vs * kTile;
+                        for (int r = first; r < end; ++r)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                *reinterpret_cast<uint4 *>(vb + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                                *reinterpret_cast<uint4 *>(vb + kPanel + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                            }
+                        fence_proxy_async_smem();
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+                    if (act0 && !issue_pv(0, g, kt == 0, ksteps)) { ok = false; break; }
+                    if (!last) {
+                        if (!wait_k(g + 1)) { ok = false; break; }
+                        if (kt + 1 < t.nt[0]) issue_s(0, g + 1);
+                    }
+                    if (t.two && !issue_pv(1, g, kt == 0, ksteps)) { ok = false; break; }
+                    umma_commit(&bars[kVEmpty0 + vs]);
+                    if (!last) {
+                        if (t.two) issue_s(1, g + 1);
+                        umma_commit(&bars[kKEmpty0 + (g + 1) % kKStages]);
+                    }
                 }
-                if (act0 && !issue_pv(0, g, kt == 0)) { ok = false; break; }
-                if (!last) {
-                    if (!wait_k(g + 1)) { ok = false; break; }
-                    if (kt + 1 < t.nt[0]) issue_s(0, g + 1);
-                }
-                if (t.two && !issue_pv(1, g, kt == 0)) { ok = false; break; }
-                if (lane == 0) umma_commit(&bars[kVEmpty0 + vs]);
-                __syncwarp();
-                if (!last) {
-                    if (t.two) issue_s(1, g + 1);
-                    if (lane == 0) umma_commit(&bars[kKEmpty0 + (g + 1) % kKStages]);
-                    __syncwarp();
-                }
+                // Q is free once every S of the pair is done
+                umma_commit(&bars[kQEmpty]);
+                iter += t.ntiles;
             }
-            // Q is free once every S of the pair is done
-            if (lane == 0) umma_commit(&bars[kQEmpty]);
-            __syncwarp();
-            iter += t.ntiles;
+            if (!ok) report(p.status, PA_DEV_TIMEOUT);
+            // no tensor-core work of this CTA may be in flight when its tensor memory is freed
+            umma_commit(&bars[kDrain]);
+            mbar_wait(&bars[kDrain], 0);
         }
-        if (!ok && lane == 0) report(p.status, PA_DEV_TIMEOUT);
-        // no tensor-core work of this CTA may be in flight when its tensor memory is freed
-        if (lane == 0) umma_commit(&bars[kDrain]);
         __syncwarp();
-        mbar_wait(&bars[kDrain], 0);
     } else {
         // ------------------------------------------------------------------ softmax warps
         const int u = (warp - kSoftmax0) >> 2;          // query tile of the pair this warp serves
