@@ -3,6 +3,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -38,6 +40,39 @@ int sm_count() {
         cache[dev] = n;
     }
     return cache[dev];
+}
+
+// A high-priority stream per device on which a call's tensor-core kernel runs beside its CUDA-core
+// kernel, with the events that fork it from and join it back to the caller's stream.  Created on
+// first use and kept until exit; the fork/join enqueue is serialised across host threads.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+
+SideStream *side_stream() {
+    static SideStream side[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    SideStream &x = side[dev];
+    if (!x.join) {
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+        if (!x.stream && cudaStreamCreateWithPriority(&x.stream, cudaStreamNonBlocking, greatest) != cudaSuccess) {
+            x.stream = nullptr;
+            return nullptr;
+        }
+        if (!x.fork && cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess) {
+            x.fork = nullptr;
+            return nullptr;
+        }
+        if (cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess) {
+            x.join = nullptr;
+            return nullptr;
+        }
+    }
+    return &x;
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -173,8 +208,21 @@ pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, co
     a.tc = a.maybe_prefill && scale > 0.f && tc_supported(d);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (launch_plan(a, s) != cudaSuccess) return PA_ERR_CUDA;
-    if (a.tc && launch_tc(a, s) != cudaSuccess) return PA_ERR_CUDA;
-    if (launch_simt(a, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (a.tc) {
+        // tensor-core tiles on the high-priority side stream; the CUDA-core items take the SMs
+        // its CTAs leave; both only read the plan and write disjoint output rows
+        std::lock_guard<std::mutex> lock(g_side_mu);
+        SideStream *x = side_stream();
+        if (!x) return PA_ERR_CUDA;
+        if (cudaEventRecord(x->fork, s) != cudaSuccess || cudaStreamWaitEvent(x->stream, x->fork, 0) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (launch_tc(a, x->stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_simt(a, s) != cudaSuccess) return PA_ERR_CUDA;
+        if (cudaEventRecord(x->join, x->stream) != cudaSuccess || cudaStreamWaitEvent(s, x->join, 0) != cudaSuccess)
+            return PA_ERR_CUDA;
+    } else if (launch_simt(a, s) != cudaSuccess) {
+        return PA_ERR_CUDA;
+    }
     if (lay.max_parts > 0 && launch_combine(a, s) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
 }

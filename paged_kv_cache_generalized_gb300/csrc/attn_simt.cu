@@ -314,6 +314,12 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
                 for (int e = 0; e < E; ++e) qf[r][e] = 0.f;
             }
         }
+        // packed (even, odd) dimension pairs for the two-lane fp32 instructions
+        uint64_t q2[R][E / 2];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) q2[r][e] = f2pack(qf[r][2 * e], qf[r][2 * e + 1]);
         const int64_t Pmax = (int64_t)c + (r0 + nrows - 1) / p.group;
         const int64_t nb_lim = (Pmax + B) / B;                  // blocks holding keys 0..Pmax
         const int64_t st_lo = (int64_t)chunk * cblocks * spb;
@@ -321,13 +327,14 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
         const int64_t st_need = (Pmax + kStageTokens) / kStageTokens;
         if (st_hi > st_need) st_hi = st_need;
 
-        float m[R], l[R], acc[R][E];
+        float m[R], l[R];
+        uint64_t acc2[R][E / 2];                      // (even, odd) dimension pairs of O
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             m[r] = -INFINITY;
             l[r] = 0.f;
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
+            for (int e = 0; e < E / 2; ++e) acc2[r][e] = 0ull;
         }
 
         const int32_t *bt_row = p.bt + (int64_t)seq * p.max_blocks;
@@ -379,11 +386,17 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
                 const int key = 2 * i + half;
                 float kf[E];
                 load_f<T, E>(sk + key * D + sub * E, kf);
+                uint64_t k2[E / 2];
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) k2[e] = f2pack(kf[2 * e], kf[2 * e + 1]);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    float dot = 0.f;
+                    uint64_t d2 = 0ull;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) dot = fmaf(qf[r][e], kf[e], dot);
+                    for (int e = 0; e < E / 2; ++e) d2 = fma2(q2[r][e], k2[e], d2);
+                    float d0, d1;
+                    f2unpack(d2, d0, d1);
+                    float dot = d0 + d1;
                     dot += __shfl_xor_sync(0xffffffffu, dot, 8);
                     dot += __shfl_xor_sync(0xffffffffu, dot, 4);
                     dot += __shfl_xor_sync(0xffffffffu, dot, 2);
@@ -399,16 +412,17 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 const float mnew = fmaxf(m[r], mx);
                 const float mref = (mnew == -INFINITY) ? 0.f : mnew;
-                const float alpha = exp2f(m[r] - mref);
+                const float alpha = fast_exp2(m[r] - mref);
                 float ps = 0.f;
 #pragma unroll
                 for (int i = 0; i < kStageTokens / 2; ++i) {
-                    s[r][i] = exp2f(s[r][i] - mref);
+                    s[r][i] = fast_exp2(s[r][i] - mref);
                     ps += s[r][i];
                 }
                 l[r] = l[r] * alpha + ps;
+                const uint64_t a2 = f2pack(alpha, alpha);
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc[r][e] *= alpha;
+                for (int e = 0; e < E / 2; ++e) acc2[r][e] = mul2(acc2[r][e], a2);
                 m[r] = mnew;
             }
 #pragma unroll
@@ -417,10 +431,15 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
                 if (p0 + key > Pmax) continue;        // never read slots past the last query
                 float vf[E];
                 load_f<T, E>(sv + key * D + sub * E, vf);
+                uint64_t v2[E / 2];
 #pragma unroll
-                for (int r = 0; r < R; ++r)
+                for (int e = 0; e < E / 2; ++e) v2[e] = f2pack(vf[2 * e], vf[2 * e + 1]);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) acc[r][e] = fmaf(s[r][i], vf[e], acc[r][e]);
+                for (int r = 0; r < R; ++r) {
+                    const uint64_t p2 = f2pack(s[r][i], s[r][i]);
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e) acc2[r][e] = fma2(v2[e], p2, acc2[r][e]);
+                }
             }
             __syncwarp();
             ++consumed;
@@ -437,6 +456,11 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
             return;
         }
 
+        float acc[R][E];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) f2unpack(acc2[r][e], acc[r][2 * e], acc[r][2 * e + 1]);
         // merge the two half-warps (alternate keys)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
