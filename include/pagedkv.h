@@ -84,6 +84,12 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
  * Sequences with q_len * g >= 16 query rows per KV head run on the tcgen05 tensor-core kernel when
  * the dtype is bf16/f16, d = 128, g divides 128 and scale > 0; decode steps, short turns and
  * everything else run on the CUDA-core split-KV kernel.
+ * Streams: when some sequence takes the tensor-core kernel, that kernel runs on a library-owned
+ * high-priority stream of the current device, forked from `stream` after the planner and joined
+ * back before the call's last kernel, so that the CUDA-core work fills the SMs it leaves.  To the
+ * caller the call stays ordered on `stream` (also under stream capture, as a fork/join); host
+ * threads that call pa_forward at the same time serialise briefly on the fork/join enqueue, and
+ * their tensor-core kernels run one after another on that device's side stream.
  * ---------------------------------------------------------------------------------------- */
 typedef struct {
     int32_t dtype;              /* pa_dtype of q, out, k_cache and v_cache */
