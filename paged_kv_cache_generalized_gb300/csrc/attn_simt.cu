@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         const int c = p.ctx[i], q = p.qlen[i];
         const int64_t n = (int64_t)c + q;
         const int64_t nb = (n + p.block_size - 1) / p.block_size;
-        const bool valid = packing_ok && q >= 1 && c >= 0 && nb <= p.max_blocks;
+        const bool valid = packing_ok && q >= 1 && c >= 0 && nb <= p.max_blocks && n <= kMaxSeqTokens;
         if (packing_ok && !valid) report(p.status, PA_DEV_BAD_LENGTHS);
         int path = 0;
         if (valid) path = (p.tc && (int64_t)q * p.group >= kTcMinRows) ? 2 : 1;
@@ -384,11 +384,15 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
 #pragma unroll
             for (int i = 0; i < kStageTokens / 2; ++i) {
                 const int key = 2 * i + half;
-                float kf[E];
-                load_f<T, E>(sk + key * D + sub * E, kf);
                 uint64_t k2[E / 2];
+                if constexpr (E * sizeof(T) >= 16) {
+                    load_pairs<T, E / 2>(sk + key * D + sub * E, k2);
+                } else {
+                    float kf[E];
+                    load_f<T, E>(sk + key * D + sub * E, kf);
 #pragma unroll
-                for (int e = 0; e < E / 2; ++e) k2[e] = f2pack(kf[2 * e], kf[2 * e + 1]);
+                    for (int e = 0; e < E / 2; ++e) k2[e] = f2pack(kf[2 * e], kf[2 * e + 1]);
+                }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     uint64_t d2 = 0ull;
@@ -429,11 +433,15 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
             for (int i = 0; i < kStageTokens / 2; ++i) {
                 const int key = 2 * i + half;
                 if (p0 + key > Pmax) continue;        // never read slots past the last query
-                float vf[E];
-                load_f<T, E>(sv + key * D + sub * E, vf);
                 uint64_t v2[E / 2];
+                if constexpr (E * sizeof(T) >= 16) {
+                    load_pairs<T, E / 2>(sv + key * D + sub * E, v2);
+                } else {
+                    float vf[E];
+                    load_f<T, E>(sv + key * D + sub * E, vf);
 #pragma unroll
-                for (int e = 0; e < E / 2; ++e) v2[e] = f2pack(vf[2 * e], vf[2 * e + 1]);
+                    for (int e = 0; e < E / 2; ++e) v2[e] = f2pack(vf[2 * e], vf[2 * e + 1]);
+                }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const uint64_t p2 = f2pack(s[r][i], s[r][i]);
@@ -496,6 +504,348 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
                         *reinterpret_cast<float4 *>(po + e) =
                             make_float4(acc[r][e], acc[r][e + 1], acc[r][e + 2], acc[r][e + 3]);
                     if (sub == 0) p.parts_ml[part * R + r] = make_float2(m[r], l[r]);
+                }
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------------------------
+// GQA work-item kernel: R = 2 or 4 query rows of one KV head share every K/V stage.
+//
+// QK^T: four lanes per key, each holding a quarter of the head dimension of all R query rows, so
+// one pass covers eight keys.  The R partial dot products of a lane are summed over its four
+// quarter lanes by a transpose-reduce (each shuffle level hands half of the rows still held to
+// the partner lane), which leaves lane (quarter r, key k) with the full score of row r (R = 4;
+// rows r/2 for R = 2) in three (two) shuffles per eight keys, where a reduce of every row on
+// every lane would take sixteen.  K arrives by TMA as 128-byte panels with the 128-byte swizzle
+// (16-byte chunk c of row t stored at chunk c ^ (t mod 8)), so the eight lanes of one quarter
+// read chunks of eight different rows without a bank conflict; V arrives by one bulk copy.
+// The softmax runs on the score owners; the probabilities go through a small shared-memory
+// table to the PV lanes: half-warps take alternate keys and each lane holds D/16 dimensions of
+// the R output rows.  The rescale of the R accumulators is skipped when no row's max moved.
+// ----------------------------------------------------------------------------------------------
+template <typename T, int D>
+struct GqaStage {
+    static constexpr int kRow = D * (int)sizeof(T);         // bytes of one key row
+    static constexpr int kPanels = kRow / 128;               // 128-byte TMA panels per row
+    static constexpr int kPanelBytes = kStageTokens * 128;   // one panel of the stage's 16 rows
+    static constexpr uint32_t kK = kStageTokens * kRow;      // swizzled K panels
+    static constexpr uint32_t kV = kStageTokens * kRow;      // V rows, as in global memory
+    static constexpr uint32_t kBytes = kK + kV;              // a multiple of 1024
+};
+
+template <typename T, int D, int R>
+__global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
+    simt_gqa_kernel(const __grid_constant__ CUtensorMap kmap, SimtParams p) {
+    static_assert(R == 2 || R == 4, "two or four rows per item");
+    using S = GqaStage<T, D>;
+    constexpr int QD = D / 4;                       // dims per quarter lane (QK^T)
+    constexpr int E = D / 16;                       // dims per lane (PV)
+    constexpr int EC = 16 / (int)sizeof(T);         // elements per 16-byte chunk
+    constexpr int NJ = QD / EC;                     // chunks per quarter lane and key
+    constexpr int kPs = (kStageTokens + 1) * R;     // (p, p) pairs of a warp: 16 keys + alpha
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qd = lane >> 3, kk = lane & 7;        // QK^T roles: quarter, key
+    const int half = lane >> 4, sub = lane & 15;    // PV roles: key parity, dims
+    const int rrow = R == 4 ? qd : (qd >> 1);       // the score row this lane owns
+    const bool owner = R == 4 || (qd & 1) == 0;     // one writer per (row, key)
+    const int NST = p.nst;
+    const int nwarps = blockDim.x >> 5;
+    // shared memory: rings [warp][stage], probability tables [warp], barriers [warp][stage]
+    unsigned char *ring = smem + (size_t)warp * NST * S::kBytes;
+    float2 *ps = reinterpret_cast<float2 *>(smem + (size_t)nwarps * NST * S::kBytes) + warp * kPs;
+    float2 *alpha_s = ps + kStageTokens * R;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)nwarps * (NST * S::kBytes + kPs * 8)) +
+                     warp * NST;
+    // byte offsets (within a key row of the swizzled panels) of this lane's NJ chunks
+    int koff[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        const int ob = qd * QD * (int)sizeof(T) + j * 16;
+        koff[j] = (ob >> 7) * S::kPanelBytes + ((((ob >> 4) & 7) ^ kk) << 4);
+    }
+    if (lane == 0) {
+        for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+
+    const int B = p.block_size;
+    const int spb = B / kStageTokens;
+    // ring state, continuous across items: issue slot, consume slot and its phase, stages in flight
+    int slot_i = 0, slot_c = 0, inflight = 0;
+    uint32_t phase_c = 0;
+    const uint32_t total_items = p.counters[kSimtTotal];
+
+    while (true) {
+        int item = 0;
+        if (lane == 0) item = (int)atomicAdd(&p.counters[kSimtNext], 1u);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if ((uint32_t)item >= total_items) break;
+
+        const int seq = find_owner(p.simt_cu, p.num_seqs, item);
+        const int local = item - __ldg(p.simt_cu + seq);
+        const int K = __ldg(p.nchunk + seq);
+        const int G = __ldg(p.groups + seq);
+        const int chunk = local % K;
+        const int rest = local / K;
+        const int grp = rest % G;
+        const int kvh = rest / G;
+        const int c = __ldg(p.ctx + seq), qn = __ldg(p.qlen + seq);
+        const int64_t tok0 = __ldg(p.cu_q + seq);
+        const int rows_total = qn * p.group;
+        const int r0 = grp * R;
+        const int nrows = min(R, rows_total - r0);
+        const int n = c + qn;                        // < 2^31 (checked by the planner)
+        const int nb = (n + B - 1) / B;
+        const int cblocks = (nb + K - 1) / K;
+
+        // this lane's quarter of every query row, pre-scaled into log2 units
+        uint64_t q2[R][QD / 2];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float qf[QD];
+            if (r < nrows) {
+                const int row = r0 + r;
+                const int j = row / p.group, hh = row - j * p.group;
+                const T *qp = reinterpret_cast<const T *>(p.q) +
+                              ((tok0 + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D + qd * QD;
+                load_f<T, QD>(qp, qf);
+            } else {
+#pragma unroll
+                for (int e = 0; e < QD; ++e) qf[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < QD / 2; ++e)
+                q2[r][e] = f2pack(qf[2 * e] * p.scale_log2, qf[2 * e + 1] * p.scale_log2);
+        }
+        // causal limit of the row this lane scores (-1: a padding row, every key masked)
+        const int Pmine = rrow < nrows ? c + (r0 + rrow) / p.group : -1;
+        const int Pmax = c + (r0 + nrows - 1) / p.group;
+        const int st_lo = chunk * cblocks * spb;
+        const int st_hi = min((chunk + 1) * cblocks * spb, (Pmax + kStageTokens) / kStageTokens);
+        const int nb_lim = (Pmax + B) / B;
+
+        float m = -INFINITY, lsum = 0.f;             // of row rrow, over this lane's keys
+        uint64_t acc2[R][E / 2];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) acc2[r][e] = 0ull;
+
+        const int32_t *bt_row = p.bt + (int64_t)seq * p.max_blocks;
+        int wbase = -1000000;
+        int32_t win = 0;
+        bool timed_out = false;
+        // issue cursor: next stage, its logical block and its 16-token part within the block
+        int st_issue = st_lo, ib = st_lo / spb, isub = st_lo - (st_lo / spb) * spb;
+
+        auto issue = [&]() {
+            if (ib >= wbase + 32 || ib < wbase) {
+                wbase = ib;
+                win = (wbase + lane < nb_lim) ? __ldg(bt_row + wbase + lane) : 0;
+            }
+            int32_t phys = __shfl_sync(0xffffffffu, win, ib - wbase);
+            if (phys < 0 || (int64_t)phys >= p.num_blocks) {
+                if (lane == 0) report(p.status, PA_DEV_BAD_BLOCK_ID);
+                phys = 0;
+            }
+            if (lane == 0) {
+                unsigned char *dst = ring + (size_t)slot_i * S::kBytes;
+                const int row = kvh * B + isub * kStageTokens;     // of the block's [Hkv * B] rows
+                const int64_t off = (int64_t)phys * p.block_stride + (int64_t)row * D;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&bars[slot_i], S::kK + S::kV);
+#pragma unroll
+                for (int pn = 0; pn < S::kPanels; ++pn)
+                    tma_load_3d(dst + pn * S::kPanelBytes, &kmap, pn * (128 / (int)sizeof(T)), row, phys,
+                                &bars[slot_i]);
+                bulk_g2s(dst + S::kK, p.v + off * sizeof(T), S::kV, &bars[slot_i]);
+            }
+            slot_i = slot_i + 1 == NST ? 0 : slot_i + 1;
+            ++inflight;
+            ++st_issue;
+            if (++isub == spb) {
+                isub = 0;
+                ++ib;
+            }
+        };
+
+        while (st_issue < st_hi && inflight < NST) issue();
+
+        for (int st = st_lo; st < st_hi; ++st) {
+            if (!mbar_wait(&bars[slot_c], phase_c)) {
+                timed_out = true;
+                break;
+            }
+            const unsigned char *sk = ring + (size_t)slot_c * S::kBytes;
+            const T *sv = reinterpret_cast<const T *>(sk + S::kK);
+            const int p0 = st * kStageTokens;
+
+            // scores: lane (qd, kk) ends with row rrow's score of keys kk and 8 + kk
+            float sc[2];
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int key = it * 8 + kk;
+                const unsigned char *kr = sk + key * 128;
+                uint64_t d2[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) d2[r] = 0ull;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    uint64_t k2[EC / 2];
+                    load_pairs<T, EC / 2>(reinterpret_cast<const T *>(kr + koff[j]), k2);
+#pragma unroll
+                    for (int e = 0; e < EC / 2; ++e)
+#pragma unroll
+                        for (int r = 0; r < R; ++r) d2[r] = fma2(q2[r][j * (EC / 2) + e], k2[e], d2[r]);
+                }
+                float d[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float a, b2;
+                    f2unpack(d2[r], a, b2);
+                    d[r] = a + b2;
+                }
+                float s;
+                if constexpr (R == 4) {
+                    const bool b1 = (qd & 2) != 0, b0 = (qd & 1) != 0;
+                    float keep0 = b1 ? d[2] : d[0], keep1 = b1 ? d[3] : d[1];
+                    const float send0 = b1 ? d[0] : d[2], send1 = b1 ? d[1] : d[3];
+                    keep0 += __shfl_xor_sync(0xffffffffu, send0, 16);
+                    keep1 += __shfl_xor_sync(0xffffffffu, send1, 16);
+                    const float keep = b0 ? keep1 : keep0, send = b0 ? keep0 : keep1;
+                    s = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                } else {
+                    const bool b1 = (qd & 2) != 0;
+                    float keep = b1 ? d[1] : d[0];
+                    keep += __shfl_xor_sync(0xffffffffu, b1 ? d[0] : d[1], 16);
+                    s = keep + __shfl_xor_sync(0xffffffffu, keep, 8);
+                }
+                sc[it] = (p0 + key <= Pmine) ? s : -INFINITY;
+            }
+            // online softmax of row rrow over this stage's 16 keys
+            float mx = fmaxf(sc[0], sc[1]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            const float mnew = fmaxf(m, mx);
+            const float mref = (mnew == -INFINITY) ? 0.f : mnew;
+            const float alpha = fast_exp2(m - mref);
+            const float pe0 = fast_exp2(sc[0] - mref), pe1 = fast_exp2(sc[1] - mref);
+            lsum = lsum * alpha + (pe0 + pe1);
+            m = mnew;
+            if (owner) {
+                ps[kk * R + rrow] = make_float2(pe0, pe0);
+                ps[(8 + kk) * R + rrow] = make_float2(pe1, pe1);
+                if (kk == 0) alpha_s[rrow] = make_float2(alpha, alpha);
+            }
+            const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+            __syncwarp();
+            if (rescale) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint64_t a2 = *reinterpret_cast<const uint64_t *>(alpha_s + r);
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e) acc2[r][e] = mul2(acc2[r][e], a2);
+                }
+            }
+            // O += P V over the stage's keys; slots past the last query's key are never read
+            auto pv_key = [&](int key) {
+                uint64_t pr[R];
+#pragma unroll
+                for (int r = 0; r < R; r += 2) {
+                    const uint4 t = *reinterpret_cast<const uint4 *>(ps + key * R + r);
+                    pr[r] = (uint64_t)t.x | ((uint64_t)t.y << 32);
+                    pr[r + 1] = (uint64_t)t.z | ((uint64_t)t.w << 32);
+                }
+                uint64_t v2[E / 2];
+                if constexpr (E * sizeof(T) >= 16) {
+                    load_pairs<T, E / 2>(sv + key * D + sub * E, v2);
+                } else {
+                    float vf[E];
+                    load_f<T, E>(sv + key * D + sub * E, vf);
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e) v2[e] = f2pack(vf[2 * e], vf[2 * e + 1]);
+                }
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e)
+#pragma unroll
+                    for (int r = 0; r < R; ++r) acc2[r][e] = fma2(v2[e], pr[r], acc2[r][e]);
+            };
+            if (p0 + kStageTokens - 1 <= Pmax) {
+#pragma unroll
+                for (int i = 0; i < kStageTokens / 2; ++i) pv_key(2 * i + half);
+            } else {
+#pragma unroll 1
+                for (int key = half; p0 + key <= Pmax; key += 2) pv_key(key);
+            }
+            __syncwarp();
+            slot_c = slot_c + 1 == NST ? 0 : slot_c + 1;
+            phase_c ^= slot_c == 0 ? 1u : 0u;
+            --inflight;
+            if (st_issue < st_hi) issue();
+        }
+
+        if (timed_out) {
+            if (lane == 0) report(p.status, PA_DEV_TIMEOUT);
+            // let the copies already in flight land before the warp leaves
+            while (inflight > 0) {
+                mbar_wait(&bars[slot_c], phase_c);
+                slot_c = slot_c + 1 == NST ? 0 : slot_c + 1;
+                phase_c ^= slot_c == 0 ? 1u : 0u;
+                --inflight;
+            }
+            return;
+        }
+
+        // row statistics: sum the key lanes' partial sums, then hand (m, l) of every row to
+        // every lane; merge the two half-warps' accumulators
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
+        float mr[R], lr[R], acc[R][E];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int src = (R == 4 ? r : 2 * r) * 8;
+            mr[r] = __shfl_sync(0xffffffffu, m, src);
+            lr[r] = __shfl_sync(0xffffffffu, lsum, src);
+#pragma unroll
+            for (int e = 0; e < E / 2; ++e) f2unpack(acc2[r][e], acc[r][2 * e], acc[r][2 * e + 1]);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], 16);
+        }
+        if (half == 0) {
+            if (K == 1) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r >= nrows) continue;
+                    const int row = r0 + r;
+                    const int j = row / p.group, hh = row - j * p.group;
+                    const float inv = 1.f / lr[r];
+                    float o[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) o[e] = acc[r][e] * inv;
+                    T *op = reinterpret_cast<T *>(p.out) +
+                            ((tok0 + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D + sub * E;
+                    store_f<T, E>(op, o);
+                }
+            } else {
+                const int64_t part = (int64_t)__ldg(p.parts_cu + seq) + local;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r >= nrows) continue;
+                    float *po = p.parts_o + ((part * R + r) * D + sub * E);
+#pragma unroll
+                    for (int e = 0; e < E; e += 4)
+                        *reinterpret_cast<float4 *>(po + e) =
+                            make_float4(acc[r][e], acc[r][e + 1], acc[r][e + 2], acc[r][e + 3]);
+                    if (sub == 0) p.parts_ml[part * R + r] = make_float2(mr[r], lr[r]);
                 }
             }
         }
@@ -593,12 +943,44 @@ cudaError_t launch_simt_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s
     return cudaGetLastError();
 }
 
+template <typename T, int D, int R>
+cudaError_t launch_gqa_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s) {
+    SimtParams p = p0;
+    using S = GqaStage<T, D>;
+    // K as [num_blocks][Hkv * B rows][D], one TMA box = one 128-byte panel of 16 rows
+    CUtensorMap kmap;
+    const uint64_t es = sizeof(T);
+    if (!make_map_3d(&kmap, a.dims.dtype, a.k, D, (uint64_t)a.dims.num_kv_heads * a.dims.block_size,
+                     a.dims.num_blocks, D * es, (uint64_t)p.block_stride * es, (uint32_t)(128 / es),
+                     kStageTokens, 1))
+        return cudaErrorInvalidValue;
+    const size_t per_stage = S::kBytes + sizeof(uint64_t);
+    const size_t ps_bytes = (size_t)(kStageTokens + 1) * R * sizeof(float2);
+    const size_t budget = 210 * 1024;
+    int nst = 3;
+    int warps = (int)(budget / (nst * per_stage + ps_bytes));
+    const int warps2 = (int)(budget / (2 * per_stage + ps_bytes));
+    if (warps < kSimtMaxWarps && warps2 > warps) {
+        nst = 2;
+        warps = warps2;
+    }
+    if (warps > kSimtMaxWarps) warps = kSimtMaxWarps;
+    p.nst = nst;
+    p.bar_bytes = 0;
+    const size_t smem = 1024 + (size_t)warps * (nst * per_stage + ps_bytes);
+    auto kern = simt_gqa_kernel<T, D, R>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<a.num_sms, warps * 32, smem, s>>>(kmap, p);
+    return cudaGetLastError();
+}
+
 template <typename T, int D>
 cudaError_t launch_simt_rows(const FwdArgs &a, const SimtParams &p, cudaStream_t s) {
     switch (a.lay.rows_per_item) {
     case 1: return launch_simt_t<T, D, 1>(a, p, s);
-    case 2: return launch_simt_t<T, D, 2>(a, p, s);
-    default: return launch_simt_t<T, D, 4>(a, p, s);
+    case 2: return launch_gqa_t<T, D, 2>(a, p, s);
+    default: return launch_gqa_t<T, D, 4>(a, p, s);
     }
 }
 

@@ -74,14 +74,6 @@ constexpr int kItemConsumers = 2 + 8;
 static_assert(kNumBars * 8 + 4 + 8 <= 256, "barrier area");
 
 // ---- tcgen05 / TMA wrappers -----------------------------------------------------------------
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
-                                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-            smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
-        : "memory");
-}
 
 // Shared-memory matrix descriptor: 128-byte swizzle, version 1 (tcgen05).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -655,40 +647,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// ---- host: tensor maps ----------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-bool make_map(CUtensorMap *map, int dtype, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
-              uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b1, uint32_t b2) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
-    const cuuint32_t box[3] = {64, b1, b2};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = enc(map, dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                           3, const_cast<void *>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool tc_shape_supported(const pa_dims &d) {
@@ -698,7 +656,7 @@ bool tc_shape_supported(const pa_dims &d) {
     if (g < 1 || g > kRows || (kRows % g) != 0) return false;
     if (d.block_size < 16 || d.block_size > kKeys) return false;
     if (d.num_blocks >= (int64_t(1) << 31) - 1 || d.total_q >= (int64_t(1) << 31)) return false;
-    return encode_fn() != nullptr;
+    return tensor_maps_available();
 }
 
 cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s) {
@@ -708,12 +666,12 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s) {
     const int64_t bstride = d.kv_block_stride ? d.kv_block_stride
                                               : (int64_t)d.num_kv_heads * d.block_size * d.head_dim;
     CUtensorMap qmap, kmap, vmap;
-    if (!make_map(&qmap, d.dtype, a.q, kDim, d.num_q_heads, d.total_q, kDim * es,
-                  (uint64_t)d.num_q_heads * kDim * es, g, kRows / g) ||
-        !make_map(&kmap, d.dtype, a.k, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
-                  kDim * es, bstride * es, d.block_size, 1) ||
-        !make_map(&vmap, d.dtype, a.v, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
-                  kDim * es, bstride * es, d.block_size, 1))
+    if (!make_map_3d(&qmap, d.dtype, a.q, kDim, d.num_q_heads, d.total_q, kDim * es,
+                     (uint64_t)d.num_q_heads * kDim * es, 64, g, kRows / g) ||
+        !make_map_3d(&kmap, d.dtype, a.k, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
+                     kDim * es, bstride * es, 64, d.block_size, 1) ||
+        !make_map_3d(&vmap, d.dtype, a.v, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
+                     kDim * es, bstride * es, 64, d.block_size, 1))
         return cudaErrorInvalidValue;
     TcParams p;
     const WsLayout &L = a.lay;

@@ -2,6 +2,7 @@
 // bulk-copy PTX wrappers, bounded waits, the device status word.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -123,6 +124,50 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     return r;
 }
 
+// Widens 2*NP consecutive 16-bit (or fp32) elements to NP packed fp32 pairs (even, odd), ready
+// for the packed fp32 instructions.  bf16 -> fp32 is exact by moving the 16 bits into the high
+// half of a word (a shift for the even element, a mask for the odd one); f16 uses the hardware
+// conversion; fp32 pairs are the loaded words themselves.  16-byte aligned, 16-byte multiples.
+template <typename T> __device__ __forceinline__ uint64_t widen2(uint32_t w);
+template <> __device__ __forceinline__ uint64_t widen2<__nv_bfloat16>(uint32_t w) {
+    uint64_t r;
+    asm("{\n\t.reg .b32 lo, hi;\n\tshl.b32 lo, %1, 16;\n\tand.b32 hi, %1, 0xffff0000;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(r)
+        : "r"(w));
+    return r;
+}
+template <> __device__ __forceinline__ uint64_t widen2<__half>(uint32_t w) {
+    uint64_t r;
+    asm("{\n\t.reg .b16 h0, h1;\n\t.reg .f32 lo, hi;\n\tmov.b32 {h0, h1}, %1;\n\t"
+        "cvt.f32.f16 lo, h0;\n\tcvt.f32.f16 hi, h1;\n\tmov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(r)
+        : "r"(w));
+    return r;
+}
+
+template <typename T, int NP>
+__device__ __forceinline__ void load_pairs(const T *p, uint64_t (&out)[NP]) {
+    static_assert((2 * NP * sizeof(T)) % 16 == 0, "16-byte vectors");
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int w = 0; w < NP / 2; ++w) {
+            const uint4 v = reinterpret_cast<const uint4 *>(p)[w];
+            out[2 * w] = (uint64_t)v.x | ((uint64_t)v.y << 32);
+            out[2 * w + 1] = (uint64_t)v.z | ((uint64_t)v.w << 32);
+        }
+    } else {
+#pragma unroll
+        for (int w = 0; w < NP / 4; ++w) {
+            const uint4 v = reinterpret_cast<const uint4 *>(p)[w];
+            out[4 * w] = widen2<T>(v.x);
+            out[4 * w + 1] = widen2<T>(v.y);
+            out[4 * w + 2] = widen2<T>(v.z);
+            out[4 * w + 3] = widen2<T>(v.w);
+        }
+    }
+}
+
 // ---- mbarrier ---------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
@@ -175,6 +220,17 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, u
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_addr(smem_dst)),
         "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// ---- tiled tensor copy (TMA) global -> shared, completion on an mbarrier -----------------------
+// `map` is a __grid_constant__ kernel parameter; c0 is the innermost coordinate (elements).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
         : "memory");
 }
 

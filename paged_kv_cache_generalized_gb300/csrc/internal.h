@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI entry points (api.cu) and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -27,6 +28,8 @@ constexpr int kMaxSplits = 64;
 constexpr int64_t kMaxTargetItems = 32768;
 // Smallest KV split of a CUDA-core work item, in keys.
 constexpr int kMinSplitTokens = 256;
+// Longest sequence (cached + new tokens) a call accepts, so that token positions fit int32.
+constexpr int64_t kMaxSeqTokens = (int64_t)1 << 30;
 
 // Counters at the start of the workspace.
 enum Counter : int {
@@ -91,6 +94,12 @@ cudaError_t launch_kv_append(const kv_append_dims &d, const void *k_new, const v
 cudaError_t launch_block_copy(const block_copy_dims &d, const void *src, void *dst,
                               const int64_t *pairs, unsigned *status, int num_sms,
                               cudaStream_t s);
+
+// Tensor maps (tensor_map.cu): a 3-D tiled map (dims d0 innermost, d1, d2; byte strides of d1 and
+// d2; box b0 x b1 x b2 elements, b0 * element size = 128 bytes) with 128-byte swizzle.
+bool tensor_maps_available();
+bool make_map_3d(CUtensorMap *map, int dtype, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }

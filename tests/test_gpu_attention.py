@@ -54,6 +54,12 @@ CASES = [
     ("block64_f16", [200, 70], [1, 90], 8, 4, 128, 64, "f16", "shuffle"),
     ("block128_bf16", [300, 5], [130, 1], 4, 1, 128, 128, "bf16", "shuffle"),
     ("exact_block_multiples_bf16", [16, 31, 32, 48], [16, 1, 32, 16], 4, 4, 128, 16, "bf16", "shuffle"),
+    # CUDA-core GQA rows (2 or 4 query rows per KV head and item): short turns with ragged row
+    # groups, a group of 3 (rows split 2 + 1), fp32 at d=128, d=64
+    ("short_turns_gqa4_bf16", [100, 513, 0, 47], [3, 2, 1, 1], 16, 4, 128, 32, "bf16", "shuffle"),
+    ("gqa3_f16", [300, 45, 1200], [5, 1, 1], 6, 2, 128, 16, "f16", "shuffle"),
+    ("gqa4_f32_d128", [400, 90], [1, 3], 8, 2, 128, 16, "f32", "shuffle"),
+    ("gqa2_d64_bf16", [1000, 5, 300], [1, 1, 7], 8, 4, 64, 16, "bf16", "segments"),
 ]
 
 
