@@ -219,10 +219,11 @@ class AttnStep:
         self.flops = attn_flops(batch.ctx_lens, batch.q_lens, Hq, d)
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
         self.d2h_bytes = self.out.numel() * self.out.element_size()
-        # block_copy (if any fork) + kv_append + pa_forward's plan, CUDA-core and combine kernels
-        # (+ the tensor-core kernel when the batch has multi-token turns it supports)
+        # block_copy (if any fork) + kv_append + pa_forward's planner and CUDA-core kernel (which
+        # merges its own splits) (+ the tensor-core kernel when the batch has multi-token turns it
+        # supports)
         tc = T > batch.num_seqs and _tc_enabled(batch)
-        self.launches_per_step = (1 if len(pairs) else 0) + 1 + 3 + (1 if tc else 0)
+        self.launches_per_step = (1 if len(pairs) else 0) + 1 + 2 + (1 if tc else 0)
 
     def _copy(self, inp):
         if inp["pairs"].shape[0]:
@@ -560,7 +561,7 @@ def run_native(args):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "traffic_source": tsrc,
                 "algorithmic_bytes": step_obj.bytes_attn,
-                "kernel": "pa_forward (plan + split-KV CUDA-core attention + combine)",
+                "kernel": "pa_forward (plan + split-KV CUDA-core attention with fused split merge)",
                 "peak_source": f"hbm_gbs of {peak_src}"}
     else:
         achieved = step_obj.flops / (attn_ms * 1e-3) / 1e12
@@ -569,7 +570,7 @@ def run_native(args):
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
                 "frac": achieved / pk, "traffic": traffic, "traffic_source": tsrc,
                 "algorithmic_flops": step_obj.flops,
-                "kernel": "pa_forward (plan + tcgen05 tensor-core prefill + CUDA-core decode + combine)",
+                "kernel": "pa_forward (plan + tcgen05 tensor-core prefill + CUDA-core decode with fused split merge)",
                 "peak_source": f"bf16_tflops (burst) of {peak_src}"}
 
     cpu = None

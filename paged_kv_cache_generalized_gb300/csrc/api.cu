@@ -140,6 +140,7 @@ WsLayout ws_layout(const pa_dims &d) {
     L.rows_per_item = R;
     L.parts_ml = take((size_t)L.max_parts * R * sizeof(float) * 2);
     L.parts_o = take((size_t)L.max_parts * R * d.head_dim * sizeof(float));
+    L.unit_cnt = take((size_t)L.max_parts * sizeof(uint32_t));
     L.total = off;
     return L;
 }
@@ -223,7 +224,6 @@ pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, co
     } else if (launch_simt(a, s) != cudaSuccess) {
         return PA_ERR_CUDA;
     }
-    if (lay.max_parts > 0 && launch_combine(a, s) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
 }
 

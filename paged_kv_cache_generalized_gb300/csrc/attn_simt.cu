@@ -1,5 +1,5 @@
-// Generalized paged attention on CUDA cores: the device-side planner, the split-KV work-item
-// kernel and the split combine.
+// Generalized paged attention on CUDA cores: the device-side planner and the split-KV work-item
+// kernels (the last split of a row group to finish merges the group's partial results).
 //
 // Method: softmax(QK^T / sqrt(d_k)) V evaluated block by block through the block table
 // ("SOSP 2023論文解説: PagedAttention", section "PagedAttentionアルゴリズム", blockwise A_j and
@@ -35,6 +35,7 @@ struct PlanParams {
     const int32_t *qlen;
     uint32_t *counters;
     int32_t *cu_q, *simt_cu, *parts_cu, *comb_cu, *groups, *nchunk, *tc_cu, *tc_seq;
+    uint32_t *unit_cnt;
     unsigned *status;
     int64_t total_q;
     int64_t max_parts;
@@ -177,9 +178,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
             p.counters[kSimtTotal] = 0;
             p.counters[kCombTotal] = 0;
         }
-    } else if (tid == 0) {
-        p.counters[kSimtTotal] = (uint32_t)n_items;
-        p.counters[kCombTotal] = (uint32_t)n_comb;
+    } else {
+        if (tid == 0) {
+            p.counters[kSimtTotal] = (uint32_t)n_items;
+            p.counters[kCombTotal] = (uint32_t)n_comb;
+        }
+        // arrival counters of the split row groups
+        const int64_t n_units = n_comb / p.rows;
+        for (int64_t u = tid; u < n_units; u += kPlanThreads) p.unit_cnt[u] = 0;
     }
 
     // tensor-core tiles: sequences ranked by descending length (longest first), ties by index
@@ -240,8 +246,9 @@ struct SimtParams {
     const char *v;
     char *out;
     const int32_t *bt, *ctx, *qlen;
-    const int32_t *cu_q, *simt_cu, *parts_cu, *groups, *nchunk;
+    const int32_t *cu_q, *simt_cu, *parts_cu, *comb_cu, *groups, *nchunk;
     uint32_t *counters;
+    uint32_t *unit_cnt;
     float2 *parts_ml;
     float *parts_o;
     unsigned *status;
@@ -249,6 +256,72 @@ struct SimtParams {
     float scale_log2;                   // scale * log2(e)
     int num_seqs, q_heads, kv_heads, group, block_size, max_blocks, nst, bar_bytes;
 };
+
+// Called by a whole warp after it wrote the partial records (m, l, o) of its split of row group
+// (seq, kvh, grp).  The last of the group's K splits to get here merges the K records of every
+// row with the logsumexp rule, out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k,
+// M = max_k m_k, and writes the output rows; the others return at once.  Each writer fences its
+// records before it counts itself in; the merger fences after it and reads through L2.
+// A split whose partial records are written but not yet counted in: a warp counts itself in (and
+// merges, if it is the group's last) only after it has issued the first copies of its next item,
+// so that the merge's latency overlaps them.
+struct PendingSplit {
+    int seq, kvh, grp, G, K, r0, nrows;
+    int64_t tok0;
+    bool on;
+};
+
+template <typename T, int D, int R>
+__device__ __forceinline__ void finish_split(const SimtParams &p, int seq, int kvh, int grp, int G, int K,
+                                             int r0, int nrows, int64_t tok0, int lane) {
+    constexpr int EO = D / 32;                     // output dims per lane
+    const int64_t unit = (int64_t)__ldg(p.comb_cu + seq) / R + (int64_t)kvh * G + grp;
+    __threadfence();
+    __syncwarp();
+    uint32_t before = 0;
+    if (lane == 0) before = atomicAdd(p.unit_cnt + unit, 1u);
+    before = __shfl_sync(0xffffffffu, before, 0);
+    if (before != (uint32_t)(K - 1)) return;
+    __threadfence();
+    const int64_t part0 = (int64_t)__ldg(p.parts_cu + seq) + ((int64_t)kvh * G + grp) * K;
+    for (int r = 0; r < nrows; ++r) {
+        const float2 ml0 = lane < K ? __ldcg(p.parts_ml + (part0 + lane) * R + r)
+                                    : make_float2(-INFINITY, 0.f);
+        const float2 ml1 = lane + 32 < K ? __ldcg(p.parts_ml + (part0 + lane + 32) * R + r)
+                                         : make_float2(-INFINITY, 0.f);
+        const float M = warp_max(fmaxf(ml0.x, ml1.x));
+        const float w0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - M);
+        const float w1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
+        float L = w0 * ml0.y + w1 * ml1.y;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        float acc[EO];
+#pragma unroll
+        for (int e = 0; e < EO; ++e) acc[e] = 0.f;
+        const float *po = p.parts_o + (part0 * R + r) * D + lane * EO;
+#pragma unroll 4
+        for (int k = 0; k < K; ++k) {
+            const float w = __shfl_sync(0xffffffffu, k < 32 ? w0 : w1, k & 31);
+            float x[EO];
+            if constexpr (EO == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(po + (int64_t)k * R * D));
+                x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+            } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(po + (int64_t)k * R * D));
+                x[0] = v.x, x[1] = v.y;
+            }
+#pragma unroll
+            for (int e = 0; e < EO; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+        }
+        const float inv = 1.f / L;
+        const int row = r0 + r;
+        const int j = row / p.group, hh = row - j * p.group;
+        T *op = reinterpret_cast<T *>(p.out) + ((tok0 + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D +
+                lane * EO;
+#pragma unroll
+        for (int e = 0; e < EO; ++e) op[e] = Elem<T>::from_f(acc[e] * inv);
+    }
+}
 
 template <typename T, int D, int R>
 __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(SimtParams p) {
@@ -270,6 +343,8 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
     const int spb = B / kStageTokens;               // stages per block
     uint32_t issued = 0, consumed = 0;               // ring positions (persist across items)
     const uint32_t total_items = p.counters[kSimtTotal];
+    PendingSplit pend;
+    pend.on = false;
 
     while (true) {
         int item = 0;
@@ -369,6 +444,11 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
         };
 
         while (st_issue < st_hi && issued - consumed < (uint32_t)NST) issue(st_issue++);
+        if (pend.on) {
+            finish_split<T, D, R>(p, pend.seq, pend.kvh, pend.grp, pend.G, pend.K, pend.r0, pend.nrows,
+                                  pend.tok0, lane);
+            pend.on = false;
+        }
 
         for (int64_t st = st_lo; st < st_hi; ++st) {
             const uint32_t slot = consumed % NST;
@@ -506,8 +586,12 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
                     if (sub == 0) p.parts_ml[part * R + r] = make_float2(m[r], l[r]);
                 }
             }
+            pend = PendingSplit{seq, kvh, grp, G, K, r0, nrows, tok0, true};
         }
     }
+    if (pend.on)
+        finish_split<T, D, R>(p, pend.seq, pend.kvh, pend.grp, pend.G, pend.K, pend.r0, pend.nrows, pend.tok0,
+                              lane);
 }
 
 // ----------------------------------------------------------------------------------------------
@@ -581,6 +665,8 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
     int slot_i = 0, slot_c = 0, inflight = 0;
     uint32_t phase_c = 0;
     const uint32_t total_items = p.counters[kSimtTotal];
+    PendingSplit pend;
+    pend.on = false;
 
     while (true) {
         int item = 0;
@@ -677,6 +763,11 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
         };
 
         while (st_issue < st_hi && inflight < NST) issue();
+        if (pend.on) {
+            finish_split<T, D, R>(p, pend.seq, pend.kvh, pend.grp, pend.G, pend.K, pend.r0, pend.nrows,
+                                  pend.tok0, lane);
+            pend.on = false;
+        }
 
         for (int st = st_lo; st < st_hi; ++st) {
             if (!mbar_wait(&bars[slot_c], phase_c)) {
@@ -849,71 +940,11 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
                 }
             }
         }
+        if (K > 1) pend = PendingSplit{seq, kvh, grp, G, K, r0, nrows, tok0, true};
     }
-}
-
-// ----------------------------------------------------------------------------------------------
-// Split combine: one warp per (sequence, KV head, row group, row) whose KV range was split.
-// out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k, M = max_k m_k.
-// ----------------------------------------------------------------------------------------------
-struct CombineParams {
-    char *out;
-    const int32_t *qlen, *cu_q, *parts_cu, *comb_cu, *groups, *nchunk;
-    const uint32_t *counters;
-    const float2 *parts_ml;
-    const float *parts_o;
-    int num_seqs, q_heads, group, rows;
-};
-
-template <typename T, int D>
-__global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
-    constexpr int E = D / 32;
-    const int lane = threadIdx.x & 31;
-    const uint32_t total = p.counters[kCombTotal];
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < total;
-         u += warps) {
-        const int seq = find_owner(p.comb_cu, p.num_seqs, (int)u);
-        const int local = (int)u - __ldg(p.comb_cu + seq);
-        const int r = local % p.rows;
-        const int rest = local / p.rows;
-        const int G = __ldg(p.groups + seq);
-        const int grp = rest % G;
-        const int kvh = rest / G;
-        const int row = grp * p.rows + r;
-        if (row >= __ldg(p.qlen + seq) * p.group) continue;
-        const int K = __ldg(p.nchunk + seq);
-        const int64_t base = (int64_t)__ldg(p.parts_cu + seq) + (int64_t)(kvh * G + grp) * K;
-        float M = -INFINITY;
-        for (int k = 0; k < K; ++k) M = fmaxf(M, p.parts_ml[(base + k) * p.rows + r].x);
-        float L = 0.f, o[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = 0.f;
-        for (int k = 0; k < K; ++k) {
-            const float2 ml = p.parts_ml[(base + k) * p.rows + r];
-            const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-            L += w * ml.y;
-            const float *po = p.parts_o + ((base + k) * p.rows + r) * D + lane * E;
-            float x[E];
-#pragma unroll
-            for (int e = 0; e < E; ++e) x[e] = po[e];
-#pragma unroll
-            for (int e = 0; e < E; ++e) o[e] = fmaf(w, x[e], o[e]);
-        }
-        const float inv = 1.f / L;
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[e] *= inv;
-        const int j = row / p.group, hh = row - (row / p.group) * p.group;
-        T *op = reinterpret_cast<T *>(p.out) +
-                (((int64_t)__ldg(p.cu_q + seq) + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D +
-                lane * E;
-        if constexpr (E * sizeof(T) >= 8) {
-            store_f<T, E>(op, o);
-        } else {
-#pragma unroll
-            for (int e = 0; e < E; ++e) op[e] = Elem<T>::from_f(o[e]);
-        }
-    }
+    if (pend.on)
+        finish_split<T, D, R>(p, pend.seq, pend.kvh, pend.grp, pend.G, pend.K, pend.r0, pend.nrows, pend.tok0,
+                              lane);
 }
 
 template <typename T, int D, int R>
@@ -989,17 +1020,6 @@ cudaError_t launch_simt_dim(const FwdArgs &a, const SimtParams &p, cudaStream_t 
     return a.dims.head_dim == 64 ? launch_simt_rows<T, 64>(a, p, s) : launch_simt_rows<T, 128>(a, p, s);
 }
 
-template <typename T, int D>
-cudaError_t launch_combine_t(const FwdArgs &a, const CombineParams &p, cudaStream_t s) {
-    combine_kernel<T, D><<<a.num_sms * 4, 256, 0, s>>>(p);
-    return cudaGetLastError();
-}
-
-template <typename T>
-cudaError_t launch_combine_dim(const FwdArgs &a, const CombineParams &p, cudaStream_t s) {
-    return a.dims.head_dim == 64 ? launch_combine_t<T, 64>(a, p, s) : launch_combine_t<T, 128>(a, p, s);
-}
-
 }  // namespace
 
 cudaError_t launch_plan(const FwdArgs &a, cudaStream_t s) {
@@ -1016,6 +1036,7 @@ cudaError_t launch_plan(const FwdArgs &a, cudaStream_t s) {
     p.nchunk = reinterpret_cast<int32_t *>(a.ws + L.nchunk);
     p.tc_cu = reinterpret_cast<int32_t *>(a.ws + L.tc_cu);
     p.tc_seq = reinterpret_cast<int32_t *>(a.ws + L.tc_seq);
+    p.unit_cnt = reinterpret_cast<uint32_t *>(a.ws + L.unit_cnt);
     p.status = a.status;
     p.total_q = a.dims.total_q;
     p.max_parts = L.max_parts;
@@ -1044,9 +1065,11 @@ cudaError_t launch_simt(const FwdArgs &a, cudaStream_t s) {
     p.cu_q = reinterpret_cast<const int32_t *>(a.ws + L.cu_q);
     p.simt_cu = reinterpret_cast<const int32_t *>(a.ws + L.simt_cu);
     p.parts_cu = reinterpret_cast<const int32_t *>(a.ws + L.parts_cu);
+    p.comb_cu = reinterpret_cast<const int32_t *>(a.ws + L.comb_cu);
     p.groups = reinterpret_cast<const int32_t *>(a.ws + L.groups);
     p.nchunk = reinterpret_cast<const int32_t *>(a.ws + L.nchunk);
     p.counters = reinterpret_cast<uint32_t *>(a.ws + L.counters);
+    p.unit_cnt = reinterpret_cast<uint32_t *>(a.ws + L.unit_cnt);
     p.parts_ml = reinterpret_cast<float2 *>(a.ws + L.parts_ml);
     p.parts_o = reinterpret_cast<float *>(a.ws + L.parts_o);
     p.status = a.status;
@@ -1064,30 +1087,6 @@ cudaError_t launch_simt(const FwdArgs &a, cudaStream_t s) {
     case PA_F32: return launch_simt_dim<float>(a, p, s);
     case PA_BF16: return launch_simt_dim<__nv_bfloat16>(a, p, s);
     default: return launch_simt_dim<__half>(a, p, s);
-    }
-}
-
-cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s) {
-    const WsLayout &L = a.lay;
-    CombineParams p;
-    p.out = static_cast<char *>(a.out);
-    p.qlen = a.qlen;
-    p.cu_q = reinterpret_cast<const int32_t *>(a.ws + L.cu_q);
-    p.parts_cu = reinterpret_cast<const int32_t *>(a.ws + L.parts_cu);
-    p.comb_cu = reinterpret_cast<const int32_t *>(a.ws + L.comb_cu);
-    p.groups = reinterpret_cast<const int32_t *>(a.ws + L.groups);
-    p.nchunk = reinterpret_cast<const int32_t *>(a.ws + L.nchunk);
-    p.counters = reinterpret_cast<const uint32_t *>(a.ws + L.counters);
-    p.parts_ml = reinterpret_cast<const float2 *>(a.ws + L.parts_ml);
-    p.parts_o = reinterpret_cast<const float *>(a.ws + L.parts_o);
-    p.num_seqs = a.dims.num_seqs;
-    p.q_heads = a.dims.num_q_heads;
-    p.group = a.dims.num_q_heads / a.dims.num_kv_heads;
-    p.rows = L.rows_per_item;
-    switch (a.dims.dtype) {
-    case PA_F32: return launch_combine_dim<float>(a, p, s);
-    case PA_BF16: return launch_combine_dim<__nv_bfloat16>(a, p, s);
-    default: return launch_combine_dim<__half>(a, p, s);
     }
 }
 

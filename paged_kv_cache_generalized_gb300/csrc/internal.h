@@ -37,7 +37,7 @@ enum Counter : int {
     kSimtTotal = 1,   // number of CUDA-core items
     kTcNext = 2,      // next tensor-core tile to take
     kTcTotal = 3,     // number of tensor-core tiles
-    kCombTotal = 4,   // number of split-KV rows to combine
+    kCombTotal = 4,   // number of split-KV rows to combine (row groups x rows)
     kChunkBlocks = 5, // KV blocks per CUDA-core split
     kNumCounters = 16
 };
@@ -55,6 +55,7 @@ struct WsLayout {
     size_t tc_seq;     // int32 [S]    sequence at each rank
     size_t parts_ml;   // float2 [max_parts * R]  (running max in log2 units, sum)
     size_t parts_o;    // float  [max_parts * R * d]
+    size_t unit_cnt;   // uint32 [max_parts]  splits finished per split row group (zeroed by the planner)
     size_t total;
     int64_t max_parts;
     int rows_per_item; // R
@@ -85,7 +86,6 @@ struct FwdArgs {
 
 cudaError_t launch_plan(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_simt(const FwdArgs &a, cudaStream_t s);
-cudaError_t launch_combine(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s);
 
 cudaError_t launch_kv_append(const kv_append_dims &d, const void *k_new, const void *v_new,
