@@ -18,6 +18,12 @@ Workloads (``--workload``):
   kvmove      40-layer 5120-hidden fp16 pool (8 layers resident), 64 sessions: append, 10%
               copy-on-write copies, swap-in of 8 sessions from a pinned host pool, layer by
               layer.  Metric: GB/s moved (read + write).
+  swap_pipeline  the mixed_gqa batch as 8 layers; before each layer's attention the earliest 1/8
+              of every resumed conversation's history comes back from pinned host memory, layer
+              by layer, overlapped with the attention of the layer before (copy-engine transfer
+              into a staging slot + block_copy scatter).  Metric: attention TFLOP/s of all layers
+              with the swap-in inside the step; the JSON line also carries the serial schedule,
+              each half alone, the gather-kernel variant and swap-out.
 
 ``--impl reference`` times the float64 CPU oracle (the only reference implementation: the pages
 publish no code) on a bounded sample of the same workload and prints the same JSON line.
@@ -305,6 +311,83 @@ class KVMoveStep:
         self.step()
 
 
+class SwapPipelineStep:
+    """Layer-by-layer swap-in overlapped with attention: L layers of the mixed GQA batch in a device
+    pool [L, 2 (K,V), num_blocks, Hkv, B, d]; before layer l's attention, the earliest 1/8 of every
+    resumed conversation's cached history (that layer's K and V of those blocks) comes back from a
+    page-locked host pool [L, 2, Hn, Hkv, B, d]."""
+
+    def __init__(self, batch: W.AttnBatch, dev, layers: int, frac: float = 0.125):
+        import torch
+        import paged_kv_cache_generalized_gb300 as pkg
+        from paged_kv_cache_generalized_gb300 import swap as S
+
+        self.pkg, self.S, self.torch, self.b, self.dev, self.L = pkg, S, torch, batch, dev, layers
+        tdt = torch.bfloat16
+
+        def up(x):
+            return torch.from_numpy(np.ascontiguousarray(x)).view(torch.int16).view(tdt)
+
+        self.pool = torch.empty((layers, 2) + batch.k_cache.shape, dtype=tdt, device=dev)
+        kd, vd = up(batch.k_cache).to(dev), up(batch.v_cache).to(dev)
+        for layer in range(layers):
+            self.pool[layer, 0].copy_(kd)
+            self.pool[layer, 1].copy_(vd)
+        del kd, vd
+        blocks = W.swap_plan(batch, frac)
+        self.dev_blocks = torch.from_numpy(blocks).to(dev)
+        self.hn = len(blocks)
+        self.host = torch.empty((layers, 2, self.hn) + batch.k_cache.shape[1:], dtype=tdt).pin_memory()
+        for layer in range(layers):
+            self.host[layer].copy_(self.pool[layer][:, self.dev_blocks])
+        self.host_out = torch.empty_like(self.host).pin_memory()
+        self.hostin = {"q": up(batch.q).pin_memory(),
+                       "bt": torch.from_numpy(batch.block_tables).pin_memory(),
+                       "ctx": torch.from_numpy(batch.ctx_lens).pin_memory(),
+                       "ql": torch.from_numpy(batch.q_lens).pin_memory()}
+        self.din = {k: v.to(dev) for k, v in self.hostin.items()}
+        self.out = torch.empty((layers,) + tuple(self.din["q"].shape), dtype=tdt, device=dev)
+        self.out_host = torch.empty_like(self.out, device="cpu").pin_memory()
+        self.ws = torch.empty(max(256, pkg.forward_workspace_size(self.din["q"], self.pool[0, 0],
+                                                                 self.din["bt"], self.din["ctx"])),
+                              dtype=torch.uint8, device=dev)
+        self.block_bytes = int(np.prod(batch.k_cache.shape[1:])) * 2
+        self.swap_bytes = float(layers * 2 * self.hn * self.block_bytes)   # host bytes per step
+        self.flops = layers * attn_flops(batch.ctx_lens, batch.q_lens, batch.num_q_heads, batch.head_dim)
+        self.copy_stream = torch.cuda.Stream(dev, priority=-1)
+        self.out_stream = torch.cuda.Stream(dev, priority=0)
+
+        # the schedules, built once (their tables and staging slots are reused every step)
+        cur = torch.cuda.current_stream(dev)
+        self.sw = {(m, ser): S.LayerSwapIn(self.host, self.pool, self.dev_blocks, mode=m,
+                                           max_ctas=0 if ser else 32,
+                                           copy_stream=cur if ser else self.copy_stream)
+                   for m in ("staged", "gather") for ser in (False, True)}
+        self.out_pairs = S.swap_out_pairs(self.dev_blocks)
+
+    def attention(self, layer):
+        d = self.din
+        self.pkg.pa_forward(d["q"], self.pool[layer, 0], self.pool[layer, 1], d["bt"], d["ctx"], d["ql"],
+                            self.b.scale, out=self.out[layer], workspace=self.ws)
+
+    def attn_only(self):
+        for layer in range(self.L):
+            self.attention(layer)
+
+
+    def run(self, mode, serial=False, attention=True):
+        self.sw[(mode, serial)].run(self.attention if attention else None)
+
+    def swap_out(self, stream=None, max_ctas=0):
+        self.S.swap_out(self.pool, self.host_out, self.out_pairs, stream=stream, max_ctas=max_ctas)
+
+    def e2e_step(self):
+        for k, v in self.hostin.items():
+            self.din[k].copy_(v, non_blocking=True)
+        self.run("staged")
+        self.out_host.copy_(self.out, non_blocking=True)
+
+
 def h2d_peak_gbs(dev, nbytes=1 << 30, reps=5):
     """Page-locked host -> device copy bandwidth measured here (the swap-in roofline)."""
     import torch
@@ -343,6 +426,10 @@ WORKLOAD_TEXT = {
                  "(ctx U{256..8192}), GQA 32/8, head_dim 128, bf16, block 32",
     "longprefill": "longprefill: 8 seqs x (16384 cached + 2048 new), 40 MHA heads, head_dim 128, "
                    "bf16, block 16, ConvKV turn segments 64..1024 tokens",
+    "swap_pipeline": "swap_pipeline: the mixed_gqa batch as 8 layers (GQA 32/8, head_dim 128, bf16, block 32); "
+                     "before each layer's attention the earliest 1/8 of every resumed conversation's history "
+                     "(that layer's K and V) is swapped in from pinned host memory, layer by layer, overlapped "
+                     "with the previous layer's attention",
     "kvmove": "kvmove: 40-layer x 5120-hidden fp16 pool (0.78 MB/token), 8 layers resident, block 32, "
               "64 sessions U{512..8192} tokens, append U{1..256} tokens each, copy-on-write of 10% of "
               "blocks shared by U{2..4} sequences, swap-in of 8 sessions from pinned host memory, "
@@ -434,6 +521,9 @@ def metric_for(name):
         return ("KV movement GB/s (bytes read + written by copy-on-write, append and swap-in per step / step time)", "GB/s", True)
     if name == "decode13b":
         return ("paged-attn decode KV GB/s (algorithmic HBM bytes per step / step time)", "GB/s", True)
+    if name == "swap_pipeline":
+        return ("layer-pipelined swap-in + attention TFLOP/s (causal-exact attention FLOPs of all layers / "
+                "step time, each layer's swap-in from host memory inside the step)", "TFLOP/s", True)
     return ("paged-attn mixed-prefill TFLOP/s (causal-exact attention FLOPs / step time)", "TFLOP/s", True)
 
 
@@ -465,6 +555,7 @@ def run_reference(args):
         return
     b = {"decode13b": lambda: W.decode13b(seed=2, poison=False),
          "mixed_gqa": lambda: W.mixed_gqa(seed=3, poison=False),
+         "swap_pipeline": lambda: W.mixed_gqa(seed=3, poison=False),
          "longprefill": lambda: W.longprefill(seed=4, poison=False)}[name]()
     total = args.steps + args.warmup
     per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
@@ -703,6 +794,118 @@ def run_native_kvmove(args):
     print(json.dumps(line), flush=True)
 
 
+def run_native_swap(args):
+    """Layer-pipelined swap-in + attention (see SwapPipelineStep)."""
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    peaks, peak_src = load_peaks()
+    metric, unit, hib = metric_for("swap_pipeline")
+    half = (args.seqs or 64) // 2
+    batch = W.mixed_gqa(seed=3, n_resume=half, n_decode=half, poison=False)
+    st = SwapPipelineStep(batch, dev, args.layers)
+    h2d = h2d_peak_gbs(dev)
+    K, Wm = args.steps, args.warmup
+
+    def timed(fn, reps=K):
+        for _ in range(Wm):
+            fn()
+        torch.cuda.synchronize()
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return max_over_ranks(dist, e0.elapsed_time(e1), dev) / reps
+
+    modes = {
+        "attn_only": st.attn_only,
+        "swap_only_staged": lambda: st.run("staged", attention=False),
+        "swap_only_gather": lambda: st.run("gather", serial=True, attention=False),
+        "serial_staged": lambda: st.run("staged", serial=True),
+        "pipelined_gather": lambda: st.run("gather"),
+    }
+    ms = {k: timed(f) for k, f in modes.items()}
+    flags = st.pkg.device_status()
+    if flags:
+        raise RuntimeError(f"device status: {st.pkg.status_names(flags)}")
+    # the headline schedule, with clock samples
+    for _ in range(Wm):
+        st.run("staged")
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record()
+        for _ in range(K):
+            st.run("staged")
+        e1.record()
+        torch.cuda.synchronize()
+    ms["pipelined_staged"] = max_over_ranks(dist, e0.elapsed_time(e1), dev) / K
+    # swap-out (eviction) alone, and beside a swap-in (the swap-in on the higher-priority stream)
+    ms["swap_out"] = timed(lambda: st.swap_out())
+
+    def both():
+        cur = torch.cuda.current_stream()
+        ev = torch.cuda.Event()
+        ev.record(cur)
+        st.copy_stream.wait_event(ev)
+        st.out_stream.wait_event(ev)
+        with torch.cuda.stream(st.out_stream):
+            st.swap_out(stream=st.out_stream, max_ctas=152)
+        st.sw[("gather", False)].run(None)
+        done = torch.cuda.Event()
+        done.record(st.out_stream)
+        cur.wait_event(done)
+
+    ms["swap_in_and_out"] = timed(both)
+    e2e_ms = timed(st.e2e_step, max(5, K // 4))
+    flags = st.pkg.device_status()
+    if rank != 0:
+        return
+    Lr = st.L
+    value = st.flops * world / (ms["pipelined_staged"] * 1e-3) / 1e12
+    ideal = max(ms["attn_only"], st.swap_bytes / (h2d * 1e9) * 1e3)
+    roof = {"bound": "tensor", "achieved": value / world, "peak": peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
+            "unit": "TFLOP/s", "frac": value / world / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
+            "traffic": None, "algorithmic_flops": st.flops,
+            "kernel": f"{Lr} layers of pa_forward with each layer's staged swap-in (copy engine + block_copy scatter) inside the step",
+            "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+    swap_gb = st.swap_bytes / 1e9
+    pipe = {"layers": Lr, "swapped_blocks_per_layer": st.hn, "swap_bytes_per_step": st.swap_bytes,
+            "ms": {k: round(v, 4) for k, v in ms.items()},
+            "swap_gbs": {"staged": swap_gb / (ms["swap_only_staged"] * 1e-3),
+                         "gather": swap_gb / (ms["swap_only_gather"] * 1e-3)},
+            "swap_out_gbs": swap_gb / (ms["swap_out"] * 1e-3),
+            "swap_in_and_out_gbs": 2 * swap_gb / (ms["swap_in_and_out"] * 1e-3),
+            "h2d_peak_gbs": h2d, "h2d_peak_source": "pinned host->device copy measured in this run",
+            "ideal_ms": ideal, "frac_of_ideal": ideal / ms["pipelined_staged"],
+            "hidden_fraction": (ms["serial_staged"] - ms["pipelined_staged"]) /
+                               max(1e-9, min(ms["attn_only"], ms["swap_only_staged"]))}
+    t, kvb, fl, rows, threads = oracle_sample(batch, args.cpu_seconds)
+    cpu = {"value": fl / t / 1e12, "unit": unit, "cores": threads, "kind": "oracle",
+           "sample": f"float64 oracle on {len(rows)} whole sequence(s) of one layer of the batch, "
+                     f"{t:.1f}s; attention only (the oracle has no transfer to overlap)"}
+    h2d_bytes = st.swap_bytes + sum(v.numel() * v.element_size() for v in st.hostin.values())
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": Wm,
+            "ms_per_step": ms["pipelined_staged"], "higher_is_better": hib, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_text("swap_pipeline", args), "layers_resident": Lr,
+                       "l2": "inputs larger than L2 (pool %.1f GB)" % (st.pool.numel() * 2 / 1e9),
+                       "attn_flops_per_step": st.flops, "parallelism": f"replicas x{world}"},
+            "roofline": roof, "pipeline": pipe, "cpu_baseline": cpu,
+            "e2e": {"value": st.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": unit,
+                    "h2d_bytes_per_step": h2d_bytes,
+                    "d2h_bytes_per_step": st.out.numel() * st.out.element_size(), "ms_per_step": e2e_ms},
+            "gpu_launches": Lr * 4 * K, "device_status": flags, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -712,7 +915,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=8,
-                    help="kvmove only: layers resident on the GPU (of 40)")
+                    help="kvmove / swap_pipeline: layers resident on the GPU")
     ap.add_argument("--seqs", type=int, default=None,
                     help="number of sequences or sessions (defaults 64 / 64 / 8 / 64; smaller for profiling runs)")
     args = ap.parse_args()
@@ -722,6 +925,8 @@ def main():
         run_reference(args)
     elif args.workload == "kvmove":
         run_native_kvmove(args)
+    elif args.workload == "swap_pipeline":
+        run_native_swap(args)
     else:
         run_native(args)
 

@@ -190,6 +190,12 @@ pa_status kv_append(const kv_append_dims *dims, const void *k_new, const void *v
  * [0, src_num_blocks) / [0, dst_num_blocks) are skipped and flagged PA_DEV_BAD_PAIR.
  * src and dst may be device memory or page-locked host memory.  block_bytes, strides and both
  * base pointers must be multiples of 16 bytes.
+ *
+ * max_ctas bounds the copy's grid (256-thread CTAs, no shared memory).  0 takes the default, a
+ * persistent grid of 8 CTAs per SM, for a copy that has the GPU to itself.  A small value (a few
+ * dozen CTAs move a host-memory swap at the link's full rate) leaves the other SMs to kernels
+ * that run beside the copy on another stream, such as a layer's attention during a layer-by-layer
+ * swap-in.  Negative values are refused with PA_ERR_INVALID_ARG.
  * ---------------------------------------------------------------------------------------- */
 typedef struct {
     int64_t block_bytes;        /* bytes of one block in one plane */
@@ -201,6 +207,7 @@ typedef struct {
     int64_t src_num_blocks;
     int64_t dst_num_blocks;
     int64_t num_pairs;          /* 0 is a no-op */
+    int32_t max_ctas;           /* 0 = 8 CTAs per SM; > 0 = at most this many CTAs */
 } block_copy_dims;
 
 pa_status block_copy(const block_copy_dims *dims, const void *src, void *dst,

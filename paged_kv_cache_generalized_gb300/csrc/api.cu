@@ -153,7 +153,7 @@ using namespace pkv;
 
 extern "C" {
 
-const char *pa_version(void) { return "pagedkv 0.1 sm_103a"; }
+const char *pa_version(void) { return "pagedkv 0.2 sm_103a"; }
 
 const char *pa_status_string(pa_status s) {
     switch (s) {
@@ -265,7 +265,7 @@ pa_status block_copy(const block_copy_dims *dims, const void *src, void *dst, co
     if (!dims) return PA_ERR_INVALID_ARG;
     const block_copy_dims &d = *dims;
     if (d.num_pairs < 0 || d.num_planes < 1 || d.block_bytes <= 0 || d.src_num_blocks < 1 ||
-        d.dst_num_blocks < 1)
+        d.dst_num_blocks < 1 || d.max_ctas < 0)
         return PA_ERR_INVALID_ARG;
     if (d.num_pairs == 0) return PA_OK;
     if (!src || !dst || !pairs) return PA_ERR_INVALID_ARG;

@@ -182,6 +182,7 @@ cudaError_t launch_block_copy(const block_copy_dims &d, const void *src, void *d
     p.dst_blocks = d.dst_num_blocks;
     if (p.total_tiles == 0) return cudaSuccess;
     int64_t grid = p.total_tiles < (int64_t)num_sms * 8 ? p.total_tiles : (int64_t)num_sms * 8;
+    if (d.max_ctas > 0 && grid > d.max_ctas) grid = d.max_ctas;
     block_copy_kernel<<<(unsigned)grid, kCopyThreads, 0, s>>>(p);
     return cudaGetLastError();
 }

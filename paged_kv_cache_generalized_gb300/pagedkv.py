@@ -54,7 +54,7 @@ class BlockCopyDims(ctypes.Structure):
                 ("src_plane_stride", ctypes.c_int64), ("dst_plane_stride", ctypes.c_int64),
                 ("src_block_stride", ctypes.c_int64), ("dst_block_stride", ctypes.c_int64),
                 ("src_num_blocks", ctypes.c_int64), ("dst_num_blocks", ctypes.c_int64),
-                ("num_pairs", ctypes.c_int64)]
+                ("num_pairs", ctypes.c_int64), ("max_ctas", ctypes.c_int32)]
 
 
 class PagedKVError(RuntimeError):
@@ -216,11 +216,12 @@ def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
     _check(rc, "kv_append")
 
 
-def block_copy(src, dst, pairs, stream=None):
+def block_copy(src, dst, pairs, stream=None, max_ctas=0):
     """Copies whole blocks of every plane (see ``block_copy`` in include/pagedkv.h).
 
     src/dst: [planes, num_blocks, ...] (each block's trailing dims contiguous; src or dst may be
-    pinned host memory); pairs: int64 [P, 2] (source block, destination block) on the device."""
+    pinned host memory); pairs: int64 [P, 2] (source block, destination block) on the device.
+    max_ctas > 0 bounds the copy's grid so that kernels on other streams keep the other SMs."""
     lib = load_library()
     if src.dim() < 2 or dst.dim() < 2 or src.shape[0] != dst.shape[0]:
         raise ValueError("block_copy: src and dst must be [planes, num_blocks, ...] with equal planes")
@@ -237,7 +238,7 @@ def block_copy(src, dst, pairs, stream=None):
         raise ValueError("pairs must be contiguous int64 [P, 2]")
     dims = BlockCopyDims(block_elems * es, src.shape[0], src.stride(0) * es, dst.stride(0) * es,
                          src.stride(1) * es, dst.stride(1) * es, src.shape[1], dst.shape[1],
-                         pairs.numel() // 2)
+                         pairs.numel() // 2, int(max_ctas))
     rc = lib.block_copy(ctypes.byref(dims), _ptr(src), _ptr(dst), _ptr(pairs), _stream(stream))
     _check(rc, "block_copy")
 

@@ -422,3 +422,24 @@ def kvmove_plan(seed: int = 5, num_layers: int = 8, num_sessions: int = 64, lens
 def shrink_plan_layers(plan: KVMovePlan, num_layers: int) -> KVMovePlan:
     from dataclasses import replace
     return replace(plan, num_layers=num_layers)
+
+
+# ---------------------------------------------------------------------------------------------
+# Layer-pipelined swap-in (a batch whose resumed conversations left part of their history on the
+# CPU tier).
+# ---------------------------------------------------------------------------------------------
+
+def swap_plan(batch: AttnBatch, frac: float = 0.125) -> np.ndarray:
+    """Device blocks whose contents come back from the CPU tier before this step's attention: the
+    earliest ``frac`` of every resumed conversation's cached history (Pensieve evicts a
+    conversation's chunks from its earlier end), whole blocks only.  Host block i of the returned
+    list goes to device block ``out[i]``; a session's blocks are consecutive on the host, so each
+    layer's swapped blocks form one contiguous host region per plane."""
+    B = batch.block_size
+    out = []
+    for i in range(batch.num_seqs):
+        if int(batch.q_lens[i]) <= 1:
+            continue                                   # decode steps stayed resident
+        k = int(frac * int(batch.ctx_lens[i])) // B
+        out.extend(int(x) for x in batch.block_tables[i, :k])
+    return np.asarray(out, dtype=np.int64)

@@ -130,3 +130,5 @@ def test_append_and_copy_reject_bad_arguments(lib):
     assert lib.block_copy(ctypes.byref(c), None, None, None, None) == 0   # no pairs: no-op
     c.num_pairs = 2
     assert lib.block_copy(ctypes.byref(c), ctypes.c_void_p(0x10004), FAKE, FAKE, None) == 1
+    c.max_ctas = -1                                    # a negative grid bound is refused
+    assert lib.block_copy(ctypes.byref(c), FAKE, FAKE, FAKE, None) == 1
