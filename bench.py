@@ -24,6 +24,10 @@ Workloads (``--workload``):
               into a staging slot + block_copy scatter).  Metric: attention TFLOP/s of all layers
               with the swap-in inside the step; the JSON line also carries the serial schedule,
               each half alone, the gather-kernel variant and swap-out.
+  layout      the decode13b batch on one layer of an 8-layer pool kept block-first (all layers of
+              a block contiguous) and layer-first; swap-in of 8 sessions in both layouts, by the
+              gather kernel and by one copy-engine transfer per contiguous segment.  Metric: decode
+              KV GB/s on the block-first pool.
 
 ``--impl reference`` times the float64 CPU oracle (the only reference implementation: the pages
 publish no code) on a bounded sample of the same workload and prints the same JSON line.
@@ -388,6 +392,84 @@ class SwapPipelineStep:
         self.out_host.copy_(self.out, non_blocking=True)
 
 
+class LayoutStep:
+    """The decode batch's attention on one layer of an L-layer pool kept in two layouts --
+    layer-first [L, 2 (K,V), num_blocks, Hkv, B, d] and block-first [num_blocks, L, 2, Hkv, B, d]
+    (every layer of a block contiguous, "KVキャッシュ管理の教科書" 第14章) -- and the swap-in of the
+    blocks of some sessions from a page-locked host pool in either layout."""
+
+    def __init__(self, batch: W.AttnBatch, dev, layers: int, swap_seqs: int = 8, memcpy_blocks: int = 64):
+        import torch
+        import paged_kv_cache_generalized_gb300 as pkg
+
+        self.pkg, self.torch, self.b, self.dev, self.L = pkg, torch, batch, dev, layers
+        tdt = torch.bfloat16
+        blk = tuple(batch.k_cache.shape[1:])
+        nb = batch.k_cache.shape[0]
+
+        def up(x):
+            return torch.from_numpy(np.ascontiguousarray(x)).view(torch.int16).view(tdt)
+
+        self.mid = layers // 2
+        self.lf = torch.empty((layers, 2, nb) + blk, dtype=tdt, device=dev)
+        self.bf = torch.empty((nb, layers, 2) + blk, dtype=tdt, device=dev)
+        kd, vd = up(batch.k_cache).to(dev), up(batch.v_cache).to(dev)
+        self.lf[self.mid, 0].copy_(kd)
+        self.lf[self.mid, 1].copy_(vd)
+        self.bf[:, self.mid, 0].copy_(kd)
+        self.bf[:, self.mid, 1].copy_(vd)
+        del kd, vd
+        self.din = {"q": up(batch.q).to(dev), "bt": torch.from_numpy(batch.block_tables).to(dev),
+                    "ctx": torch.from_numpy(batch.ctx_lens).to(dev), "ql": torch.from_numpy(batch.q_lens).to(dev)}
+        self.out = torch.empty_like(self.din["q"])
+        self.ws = torch.empty(max(256, pkg.forward_workspace_size(self.din["q"], self.bf[:, 0, 0],
+                                                                 self.din["bt"], self.din["ctx"])),
+                              dtype=torch.uint8, device=dev)
+        B = batch.block_size
+        n = batch.seq_lens
+        blocks = np.concatenate([batch.block_tables[i, :(int(n[i]) + B - 1) // B] for i in range(swap_seqs)])
+        self.hn = len(blocks)
+        self.dblocks = blocks.astype(np.int64)
+        idx = np.arange(self.hn, dtype=np.int64)
+        self.pairs = torch.from_numpy(np.stack([idx, self.dblocks], 1)).to(dev)
+        self.host_lf = torch.zeros((layers, 2, self.hn) + blk, dtype=tdt).pin_memory()
+        self.host_bf = torch.zeros((self.hn, layers, 2) + blk, dtype=tdt).pin_memory()
+        self.plane_bytes = int(np.prod(blk)) * 2
+        self.swap_bytes = float(self.hn * layers * 2 * self.plane_bytes)
+        self.memcpy_blocks = min(memcpy_blocks, self.hn)
+        es = 2
+        self.bytes_attn = float(n.sum() * batch.num_kv_heads * batch.head_dim * es * 2 +
+                                2 * batch.total_q * batch.num_q_heads * batch.head_dim * es +
+                                ((n + B - 1) // B).sum() * 4 + batch.num_seqs * 8)
+
+    def attention(self, layout):
+        pool = self.lf[self.mid] if layout == "layer_first" else self.bf[:, self.mid].transpose(0, 1)
+        d = self.din
+        self.pkg.pa_forward(d["q"], pool[0], pool[1], d["bt"], d["ctx"], d["ql"], self.b.scale,
+                            out=self.out, workspace=self.ws)
+
+    def swap_gather(self, layout):
+        if layout == "layer_first":      # one launch per layer; a block is Hkv*B*d per plane
+            for layer in range(self.L):
+                self.pkg.block_copy(self.host_lf[layer], self.lf[layer], self.pairs)
+        else:                            # one launch; a block is every layer and plane at once
+            self.pkg.block_copy(self.host_bf.unsqueeze(0), self.bf.unsqueeze(0), self.pairs)
+
+    def swap_memcpy(self, layout):
+        """One copy-engine transfer per contiguous segment (the first memcpy_blocks blocks):
+        (block, layer, plane) segments layer-first, whole blocks block-first."""
+        k = self.memcpy_blocks
+        if layout == "layer_first":
+            for j in range(k):
+                t = int(self.dblocks[j])
+                for layer in range(self.L):
+                    for pl in range(2):
+                        self.lf[layer, pl, t].copy_(self.host_lf[layer, pl, j], non_blocking=True)
+        else:
+            for j in range(k):
+                self.bf[int(self.dblocks[j])].copy_(self.host_bf[j], non_blocking=True)
+
+
 def h2d_peak_gbs(dev, nbytes=1 << 30, reps=5):
     """Page-locked host -> device copy bandwidth measured here (the swap-in roofline)."""
     import torch
@@ -426,6 +508,9 @@ WORKLOAD_TEXT = {
                  "(ctx U{256..8192}), GQA 32/8, head_dim 128, bf16, block 32",
     "longprefill": "longprefill: 8 seqs x (16384 cached + 2048 new), 40 MHA heads, head_dim 128, "
                    "bf16, block 16, ConvKV turn segments 64..1024 tokens",
+    "layout": "layout: the decode13b batch on one layer of an 8-layer pool, block-first [blocks, layers, K|V, heads, "
+              "block, dim] against layer-first [layers, K|V, blocks, heads, block, dim]; swap-in of 8 sessions' "
+              "blocks in either layout (gather kernel, and one copy-engine transfer per contiguous segment)",
     "swap_pipeline": "swap_pipeline: the mixed_gqa batch as 8 layers (GQA 32/8, head_dim 128, bf16, block 32); "
                      "before each layer's attention the earliest 1/8 of every resumed conversation's history "
                      "(that layer's K and V) is swapped in from pinned host memory, layer by layer, overlapped "
@@ -521,6 +606,9 @@ def metric_for(name):
         return ("KV movement GB/s (bytes read + written by copy-on-write, append and swap-in per step / step time)", "GB/s", True)
     if name == "decode13b":
         return ("paged-attn decode KV GB/s (algorithmic HBM bytes per step / step time)", "GB/s", True)
+    if name == "layout":
+        return ("paged-attn decode KV GB/s on a block-first pool (one layer of L; all layers of a block "
+                "contiguous)", "GB/s", True)
     if name == "swap_pipeline":
         return ("layer-pipelined swap-in + attention TFLOP/s (causal-exact attention FLOPs of all layers / "
                 "step time, each layer's swap-in from host memory inside the step)", "TFLOP/s", True)
@@ -556,6 +644,7 @@ def run_reference(args):
     b = {"decode13b": lambda: W.decode13b(seed=2, poison=False),
          "mixed_gqa": lambda: W.mixed_gqa(seed=3, poison=False),
          "swap_pipeline": lambda: W.mixed_gqa(seed=3, poison=False),
+         "layout": lambda: W.decode13b(seed=2, poison=False),
          "longprefill": lambda: W.longprefill(seed=4, poison=False)}[name]()
     total = args.steps + args.warmup
     per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
@@ -906,6 +995,91 @@ def run_native_swap(args):
     print(json.dumps(line), flush=True)
 
 
+def run_native_layout(args):
+    """Block-first against layer-first pools (see LayoutStep)."""
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    peaks, peak_src = load_peaks()
+    metric, unit, hib = metric_for("layout")
+    batch = W.decode13b(seed=2, num_seqs=args.seqs or 64, poison=False)
+    st = LayoutStep(batch, dev, args.layers)
+    h2d = h2d_peak_gbs(dev)
+    K, Wm = args.steps, args.warmup
+
+    def timed(fn, reps):
+        for _ in range(Wm):
+            fn()
+        torch.cuda.synchronize()
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return max_over_ranks(dist, e0.elapsed_time(e1), dev) / reps
+
+    ms = {"attn_layer_first": timed(lambda: st.attention("layer_first"), K)}
+    for _ in range(Wm):
+        st.attention("block_first")
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record()
+        for _ in range(K):
+            st.attention("block_first")
+        e1.record()
+        torch.cuda.synchronize()
+    ms["attn_block_first"] = max_over_ranks(dist, e0.elapsed_time(e1), dev) / K
+    swap_reps = max(3, K // 100)
+    for lay in ("layer_first", "block_first"):
+        ms[f"swap_gather_{lay}"] = timed(lambda: st.swap_gather(lay), swap_reps)
+        ms[f"swap_memcpy_{lay}"] = timed(lambda: st.swap_memcpy(lay), swap_reps)
+    flags = st.pkg.device_status()
+    e2e_ms = ms["attn_block_first"]
+    if rank != 0:
+        return
+    gbs = {k: st.bytes_attn / (v * 1e-3) / 1e9 for k, v in ms.items() if k.startswith("attn")}
+    value = gbs["attn_block_first"] * world
+    roof = {"bound": "hbm", "achieved": gbs["attn_block_first"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs["attn_block_first"] / peaks["hbm_gbs"], "traffic": None,
+            "algorithmic_bytes": st.bytes_attn,
+            "kernel": f"pa_forward on one layer of a block-first {st.L}-layer pool (block stride "
+                      f"{st.L * 2 * st.plane_bytes // 1024} KiB)", "peak_source": f"hbm_gbs of {peak_src}"}
+    mb = st.memcpy_blocks
+    seg = {"layer_first": st.plane_bytes, "block_first": st.L * 2 * st.plane_bytes}
+    swap = {"blocks": st.hn, "bytes": st.swap_bytes, "h2d_peak_gbs": h2d,
+            "gather_kernel_gbs": {lay: st.swap_bytes / (ms[f"swap_gather_{lay}"] * 1e-3) / 1e9
+                                  for lay in ("layer_first", "block_first")},
+            "memcpy_per_segment": {lay: {"segment_bytes": seg[lay],
+                                         "copies": mb * (st.L * 2 if lay == "layer_first" else 1),
+                                         "gbs": mb * st.L * 2 * st.plane_bytes / (ms[f"swap_memcpy_{lay}"] * 1e-3) / 1e9}
+                                   for lay in ("layer_first", "block_first")},
+            "note": f"memcpy rows move the first {mb} blocks, one cudaMemcpyAsync per contiguous segment"}
+    t, kvb, fl, rows, threads = oracle_sample(batch, args.cpu_seconds)
+    cpu = {"value": kvb / t / 1e9, "unit": unit, "cores": threads, "kind": "oracle",
+           "sample": f"float64 oracle on {len(rows)} whole sequence(s) of the decode batch, {t:.1f}s"}
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": Wm,
+            "ms_per_step": ms["attn_block_first"], "higher_is_better": hib, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_text("layout", args), "layers": st.L,
+                       "l2": "inputs larger than L2 (two pools of %.1f GB)" % (st.lf.numel() * 2 / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "layouts": {"attn_gbs": gbs, "block_first_over_layer_first": gbs["attn_block_first"] / gbs["attn_layer_first"],
+                        "ms": {k: round(v, 4) for k, v in ms.items()}, "swap_in": swap},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                    "note": "device-resident pools; the swap-in rows above are the host transfers"},
+            "gpu_launches": 2 * K, "device_status": flags, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -927,6 +1101,8 @@ def main():
         run_native_kvmove(args)
     elif args.workload == "swap_pipeline":
         run_native_swap(args)
+    elif args.workload == "layout":
+        run_native_layout(args)
     else:
         run_native(args)
 

@@ -214,3 +214,29 @@ def test_tensor_core_path(case):
     assert pkg.device_status() == 0
     ref = oracle.paged_attention_batch(b, threads=8)
     assert_close(as_f64(out), ref, b.dtype, name)
+
+
+# ------------------------------------------------------------------------------------------------
+# Block-first pools ("KVキャッシュ管理の教科書" 第14章: all layers of a block contiguous): one
+# layer's K and V are strided views [num_blocks, Hkv, B, d] with a block stride of L * 2 * Hkv*B*d
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_block_first_pool_every_layer(dtype):
+    ctx, ql = [700, 90, 1500, 33, 2000], [40, 3, 1, 200, 1]
+    b = W.make_attn_batch("block_first", ctx, ql, 8, 2, 128, 16, dtype, seed=77)
+    L = 3
+    kv = [(b.k_cache, b.v_cache)] + [(W.random_values(b.k_cache.shape, dtype, 90 + 2 * l),
+                                      W.random_values(b.v_cache.shape, dtype, 91 + 2 * l)) for l in range(1, L)]
+    # [num_blocks, L, 2, Hkv, B, d]
+    pool = torch.stack([torch.stack([to_dev(k, dtype), to_dev(v, dtype)], 1) for k, v in kv], 1)
+    d = batch_to_dev(b)
+    for layer, (k, v) in enumerate(kv):
+        kc, vc = pool[:, layer, 0], pool[:, layer, 1]
+        assert kc.stride(0) == L * 2 * kc[0].numel()
+        out = pkg.pa_forward(d["q"], kc, vc, d["bt"], d["ctx"], d["ql"], b.scale)
+        torch.cuda.synchronize()
+        assert pkg.device_status() == 0
+        import dataclasses
+        ref = oracle.paged_attention_batch(dataclasses.replace(b, k_cache=k, v_cache=v), threads=8)
+        assert_close(as_f64(out), ref, dtype, f"block-first layer {layer}")
