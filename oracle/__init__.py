@@ -20,6 +20,12 @@ CUDA library; the only thing both sides use is the seeded input generator module
   section "Copy-on-Writeによるメモリ共有" (a shared block is copied before it is written);
   the Pensieve page, sections "GPU-CPU 2層キャッシュ構造" and "パイプライン化されたswap-in"
   (blocks moved between the CPU tier and the GPU tier).
+* ``e4m3_decode`` / ``e4m3_encode`` and the 8-bit variants of attention and append -- K and V
+  kept as FP8 E4M3 codes with one scale each ("KVキャッシュ管理の教科書" 第3章: fewer bits per
+  element as the third way to shrink the cache; 第22章: quantising KV before decoding).  The
+  format follows its published definition (1 sign, 4 exponent bits with bias 7, 3 fraction bits,
+  no infinities, S.1111.111 = NaN); encoding rounds to nearest, ties to an even code, and
+  saturates at +-448.
 * ``kv_bytes_per_token`` / ``kv_elements`` -- sizing formulas: the Pensieve page, section
   "KVキャッシュのメモリ管理" (M_kv = L x H x 2 x b), and "KVキャッシュ管理の教科書" 第3章
   (2 x batch x layers x seq x head_dim x heads elements).
@@ -39,7 +45,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lib = None
 
-DTYPE_CODES = {"f32": 0, "bf16": 1, "f16": 2}
+DTYPE_CODES = {"f32": 0, "bf16": 1, "f16": 2, "e4m3": 3}
 
 
 def build(force: bool = False) -> str:
@@ -63,16 +69,24 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def declare(lib):
+    """Argument types of the C entry points on a loaded copy of ``attention.c``."""
+    p, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    lib.oracle_paged_attention.restype = ctypes.c_int
+    lib.oracle_paged_attention.argtypes = [p, p, p, ctypes.c_int, p, p, p, i32, i32, i32, i32,
+                                           i32, i64, i32, i64, dbl, p, i64, p, ctypes.c_int]
+    lib.oracle_paged_attention_kv.restype = ctypes.c_int
+    lib.oracle_paged_attention_kv.argtypes = [p, p, p, ctypes.c_int, ctypes.c_int, dbl, dbl, p, p, p,
+                                              i32, i32, i32, i32, i32, i64, i32, i64, dbl, p, i64, p,
+                                              ctypes.c_int]
+    lib.oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
-        p, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
-        lib.oracle_paged_attention.restype = ctypes.c_int
-        lib.oracle_paged_attention.argtypes = [p, p, p, ctypes.c_int, p, p, p, i32, i32, i32, i32,
-                                               i32, i64, i32, i64, dbl, p, i64, p, ctypes.c_int]
-        lib.oracle_max_threads.restype = ctypes.c_int
-        _lib = lib
+        _lib = declare(ctypes.CDLL(build()))
     return _lib
 
 
@@ -86,12 +100,13 @@ def _ptr(a: np.ndarray):
 
 def paged_attention(q, k_cache, v_cache, dtype, block_tables, ctx_lens, q_lens, num_q_heads,
                     num_kv_heads, head_dim, block_size, scale, rows=None, threads=1,
-                    block_stride=None):
+                    block_stride=None, kv_dtype=None, k_scale=1.0, v_scale=1.0):
     """Float64 attention rows.
 
     ``q``: [T, Hq, d]; ``k_cache``/``v_cache``: [num_blocks, Hkv, B, d] (or any array whose
     block ``b`` starts at element ``b * block_stride``); storage as in the generator module
-    (float32, or uint16 bit patterns for bf16/f16).
+    (float32, or uint16 bit patterns for bf16/f16).  ``kv_dtype="e4m3"``: the caches hold uint8
+    E4M3 codes; a cached element's value is its code's value times ``k_scale`` / ``v_scale``.
     ``rows``: optional int array [R, 3] of (sequence, token within its new tokens, query head).
     Returns float64 [T, Hq, d] (all rows) or [R, d].
     """
@@ -115,18 +130,26 @@ def paged_attention(q, k_cache, v_cache, dtype, block_tables, ctx_lens, q_lens, 
         rows_a = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 3)
         out = np.empty((rows_a.shape[0], head_dim), dtype=np.float64)
         rows_p, n_rows = _ptr(rows_a), rows_a.shape[0]
-    rc = lib.oracle_paged_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), DTYPE_CODES[dtype],
-                                    _ptr(bt), _ptr(ctx), _ptr(ql), len(ctx), num_q_heads,
-                                    num_kv_heads, head_dim, block_size, num_blocks, bt.shape[1],
-                                    block_stride, float(scale), rows_p, n_rows, _ptr(out),
-                                    int(threads))
+    kvd = DTYPE_CODES[kv_dtype or dtype]
+    rc = lib.oracle_paged_attention_kv(_ptr(q), _ptr(k_cache), _ptr(v_cache), DTYPE_CODES[dtype], kvd,
+                                       float(k_scale), float(v_scale), _ptr(bt), _ptr(ctx), _ptr(ql),
+                                       len(ctx), num_q_heads, num_kv_heads, head_dim, block_size,
+                                       num_blocks, bt.shape[1], block_stride, float(scale), rows_p,
+                                       n_rows, _ptr(out), int(threads))
     if rc != 0:
         raise ValueError(f"oracle_paged_attention: invalid input (code {rc})")
     return out
 
 
-def paged_attention_batch(batch, rows=None, threads=1):
-    """``paged_attention`` on a generator-module ``AttnBatch``."""
+def paged_attention_batch(batch, rows=None, threads=1, kv=None):
+    """``paged_attention`` on a generator-module ``AttnBatch``; ``kv`` = (k_codes, v_codes,
+    k_scale, v_scale) replaces the batch's caches with E4M3 ones."""
+    if kv is not None:
+        kc, vc, ks, vs = kv
+        return paged_attention(batch.q, kc, vc, batch.dtype, batch.block_tables, batch.ctx_lens,
+                               batch.q_lens, batch.num_q_heads, batch.num_kv_heads, batch.head_dim,
+                               batch.block_size, batch.scale, rows=rows, threads=threads,
+                               kv_dtype="e4m3", k_scale=ks, v_scale=vs)
     return paged_attention(batch.q, batch.k_cache, batch.v_cache, batch.dtype, batch.block_tables,
                            batch.ctx_lens, batch.q_lens, batch.num_q_heads, batch.num_kv_heads,
                            batch.head_dim, batch.block_size, batch.scale, rows=rows,
@@ -149,6 +172,65 @@ def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, block_size):
             k_out[blk, h, off, :] = k_new[t, h, :]
             v_out[blk, h, off, :] = v_new[t, h, :]
     return k_out, v_out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 value of every E4M3 code (uint8 array), from the format's definition."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where((c >> 7) & 1, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    normal = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0)
+    sub = (m / 8.0) * 2.0 ** -6
+    v = np.where(e == 0, sub, normal)
+    v = np.where((e == 15) & (m == 7), np.nan, v)
+    return sign * v
+
+
+def _e4m3_table():
+    codes = np.arange(127, dtype=np.uint8)          # the non-negative finite codes, increasing
+    return codes, e4m3_decode(codes)
+
+
+def e4m3_encode(x, inv_scale) -> np.ndarray:
+    """E4M3 codes of ``x * inv_scale``: x widened to float32, multiplied by float32(inv_scale) in
+    float32 (one rounding), then rounded to the nearest E4M3 value, ties to the even code, with
+    magnitudes beyond 448 saturated to 448 and the sign kept (also for results rounded to zero).
+    Non-finite inputs are outside this function's domain."""
+    y = (np.asarray(x, dtype=np.float32) * np.float32(inv_scale)).astype(np.float64)
+    codes, vals = _e4m3_table()
+    a = np.abs(y)
+    hi = np.searchsorted(vals, a, side="left").clip(0, len(vals) - 1)   # first value >= a
+    lo = (hi - 1).clip(0, None)
+    d_hi = np.abs(vals[hi] - a)
+    d_lo = np.abs(a - vals[lo])
+    pick = np.where(d_lo < d_hi, lo, hi)
+    tie = d_lo == d_hi
+    pick = np.where(tie & (lo % 2 == 0), lo, np.where(tie, hi, pick))
+    pick = np.where(a >= vals[-1], len(vals) - 1, pick)
+    out = codes[pick].astype(np.uint8)
+    return np.where(np.signbit(y), out | np.uint8(0x80), out).astype(np.uint8)
+
+
+def widen_f32(x, dtype):
+    """float32 values of generator-module storage: float32 itself, or uint16 bit patterns of bf16
+    (the top half of a binary32) or f16 (IEEE binary16); both widen exactly."""
+    x = np.asarray(x)
+    if dtype == "f32":
+        return x.astype(np.float32)
+    if dtype == "bf16":
+        return (x.astype(np.uint32) << 16).view(np.float32)
+    return x.astype(np.uint16).view(np.float16).astype(np.float32)
+
+
+def kv_append_e4m3(k_new, v_new, slot_mapping, k_codes, v_codes, block_size, k_scale, v_scale,
+                   dtype):
+    """``kv_append`` into E4M3 caches: new K (V) elements of ``dtype`` are widened to float32,
+    encoded with ``e4m3_encode(x, 1 / scale)`` (the reciprocal rounded to float32) and scattered
+    to their slots."""
+    kq = e4m3_encode(widen_f32(k_new, dtype), np.float32(1.0) / np.float32(k_scale))
+    vq = e4m3_encode(widen_f32(v_new, dtype), np.float32(1.0) / np.float32(v_scale))
+    return kv_append(kq, vq, slot_mapping, k_codes, v_codes, block_size)
 
 
 def block_copy(src, dst, pairs):

@@ -30,6 +30,11 @@
  *
  * The softmax is evaluated with the usual max subtraction (exp(s - max) / sum exp(s - max)),
  * which is the same function, in float64 with C's exp().
+ *
+ *   8-bit caches -- "KVキャッシュ管理の教科書" 第3章 (fewer bits per element as the third way to
+ *   shrink the cache) and 第22章 (quantising KV before decoding).  Reading taken here: K and V
+ *   hold FP8 E4M3 codes and one scale each; a cached element's value is code value x scale, and
+ *   attention is the same function of those values.
  */
 #include <math.h>
 #include <stdint.h>
@@ -40,7 +45,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2, ORACLE_E4M3 = 3 };
 
 /* IEEE-754 binary16 -> double, from the format's definition (1 sign, 5 exponent, 10 fraction
  * bits, bias 15); every binary16 value is exactly representable in double. */
@@ -68,33 +73,53 @@ static double bf16_to_double(uint16_t b)
     return (double)f;
 }
 
+/* FP8 E4M3 -> double, from the format's definition: 1 sign, 4 exponent bits (bias 7), 3 fraction
+ * bits, subnormals at exponent 0, no infinities, S.1111.111 is NaN. */
+static double e4m3_to_double(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xf;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);                     /* subnormal: m/8 * 2^(1-7) */
+    else
+        v = ldexp((double)(m + 8), e - 10);           /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
 static double element(const void *base, int dtype, int64_t idx)
 {
     switch (dtype) {
     case ORACLE_F32: return (double)((const float *)base)[idx];
     case ORACLE_BF16: return bf16_to_double(((const uint16_t *)base)[idx]);
+    case ORACLE_E4M3: return e4m3_to_double(((const uint8_t *)base)[idx]);
     default: return half_to_double(((const uint16_t *)base)[idx]);
     }
 }
 
 /*
  * Computes the requested output rows.
- *   q        [total_q, Hq, d]            (dtype)
+ *   q        [total_q, Hq, d]            (q_dtype)
  *   k_cache  physical block b, head kh, slot s, dim x at  b*block_stride + (kh*B + s)*d + x
- *   v_cache  same layout
+ *            (kv_dtype; an element's value is multiplied by k_scale)
+ *   v_cache  same layout (value multiplied by v_scale)
  *   rows     n_rows triples (seq, token j within the sequence's new tokens, query head), or NULL
  *            for every row in order (packed token t, head h)
  *   out      n_rows * d doubles
  * Returns 0, or -1 if a row index is out of range, -2 if a block-table entry that must be read
  * is outside [0, num_blocks).
  */
-int oracle_paged_attention(const void *q, const void *k_cache, const void *v_cache, int dtype,
-                           const int32_t *block_tables, const int32_t *ctx_lens,
-                           const int32_t *q_lens, int32_t num_seqs, int32_t num_q_heads,
-                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                           int64_t num_blocks, int32_t max_blocks_per_seq, int64_t block_stride,
-                           double scale, const int64_t *rows, int64_t n_rows, double *out,
-                           int num_threads)
+int oracle_paged_attention_kv(const void *q, const void *k_cache, const void *v_cache,
+                              int q_dtype, int kv_dtype, double k_scale, double v_scale,
+                              const int32_t *block_tables, const int32_t *ctx_lens,
+                              const int32_t *q_lens, int32_t num_seqs, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int64_t num_blocks, int32_t max_blocks_per_seq, int64_t block_stride,
+                              double scale, const int64_t *rows, int64_t n_rows, double *out,
+                              int num_threads)
 {
     const int64_t d = head_dim, B = block_size;
     const int64_t group = num_q_heads / num_kv_heads;
@@ -154,7 +179,8 @@ int oracle_paged_attention(const void *q, const void *k_cache, const void *v_cac
                 int64_t kbase = phys * block_stride + (kh * B + k) * d;
                 double dot = 0.0;
                 for (int64_t x = 0; x < d; ++x)
-                    dot += element(q, dtype, qrow * d + x) * element(k_cache, dtype, kbase + x);
+                    dot += element(q, q_dtype, qrow * d + x) *
+                           (element(k_cache, kv_dtype, kbase + x) * k_scale);
                 s[p] = scale * dot;
             }
         }
@@ -181,13 +207,29 @@ int oracle_paged_attention(const void *q, const void *k_cache, const void *v_cac
                 if (p >= n) break;
                 int64_t vbase = phys * block_stride + (kh * B + k) * d;
                 double w = s[p] / denom;
-                for (int64_t x = 0; x < d; ++x) o[x] += w * element(v_cache, dtype, vbase + x);
+                for (int64_t x = 0; x < d; ++x)
+                    o[x] += w * (element(v_cache, kv_dtype, vbase + x) * v_scale);
             }
         }
         free(s);
     }
     free(cu);
     return status;
+}
+
+/* The same with q and caches in one dtype and unit scales. */
+int oracle_paged_attention(const void *q, const void *k_cache, const void *v_cache, int dtype,
+                           const int32_t *block_tables, const int32_t *ctx_lens,
+                           const int32_t *q_lens, int32_t num_seqs, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                           int64_t num_blocks, int32_t max_blocks_per_seq, int64_t block_stride,
+                           double scale, const int64_t *rows, int64_t n_rows, double *out,
+                           int num_threads)
+{
+    return oracle_paged_attention_kv(q, k_cache, v_cache, dtype, dtype, 1.0, 1.0, block_tables,
+                                     ctx_lens, q_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                     block_size, num_blocks, max_blocks_per_seq, block_stride, scale,
+                                     rows, n_rows, out, num_threads);
 }
 
 /* Number of OpenMP threads the oracle would use (1 when built without OpenMP). */

@@ -290,12 +290,7 @@ def test_pins_catch_planted_mistake(oracle_mod, name, monkeypatch):
     mutated = src.replace(old, new, 1)
     with tempfile.TemporaryDirectory() as tmp:
         so = _build_mutant(mutated, name, tmp)
-        lib = ctypes.CDLL(so)
-        p, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
-        lib.oracle_paged_attention.restype = ctypes.c_int
-        lib.oracle_paged_attention.argtypes = [p, p, p, ctypes.c_int, p, p, p, i32, i32, i32, i32,
-                                               i32, i64, i32, i64, dbl, p, i64, p, ctypes.c_int]
-        lib.oracle_max_threads.restype = ctypes.c_int
+        lib = oracle_mod.declare(ctypes.CDLL(so))
         monkeypatch.setattr(oracle_mod, "_lib", lib)
         caught = False
         for case in SDPA_CASES:
