@@ -11,6 +11,8 @@ Workloads (``--workload``):
               block 16, q_len 1, context U{512..4096}, blocks scattered in a pool with 10% free;
               6 sequences fork (copy-on-write of their partially filled last block).
               Metric: algorithmic HBM bytes / step time, GB/s.
+  decode13b_fp8  the same batch with FP8 E4M3 K/V caches (scale 1/32 for K and V): half the K/V
+              bytes per token.  Metric: GB/s (of the 8-bit bytes); the line also gives tokens/s.
   mixed_gqa   32 resumed conversations (history U{1024..16384}, new turn U{16..512}) + 32 decode
               sequences, GQA 32/8, d=128, bf16, block 32.  Metric: attention TFLOP/s (causal-exact).
   longprefill 8 x (16384 cached + 2048 new), 40 MHA heads, d=128, bf16, block 16, ConvKV-style
@@ -172,11 +174,15 @@ def _tc_enabled(batch):
 class AttnStep:
     """block_copy + kv_append + pa_forward over one AttnBatch, all inputs resident on the GPU."""
 
-    def __init__(self, batch: W.AttnBatch, dev, cow_frac=0.0, seed=0):
+    def __init__(self, batch: W.AttnBatch, dev, cow_frac=0.0, seed=0, kv8=False):
         import torch
         import paged_kv_cache_generalized_gb300 as pkg
 
         self.pkg, self.torch, self.b, self.dev = pkg, torch, batch, dev
+        # 8-bit caches: E4M3 codes of value / scale; a scale of 1/32 puts N(0,1) values in the
+        # format's normal range (|x| / scale <= 448 for |x| <= 14)
+        self.kv8 = kv8
+        self.ks = self.vs = (1.0 / 32) if kv8 else None
         tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[batch.dtype]
         self.tdt = tdt
 
@@ -210,9 +216,16 @@ class AttnStep:
         self.host["pairs"] = up(pairs).pin_memory()
         self.dev_in = {k2: v.to(dev) for k2, v in self.host.items()}
         # K and V caches are the two planes of one pool, so one block_copy moves both
-        self.pool = torch.empty((2,) + batch.k_cache.shape, dtype=tdt, device=dev)
-        self.pool[0].copy_(up(batch.k_cache, tdt))
-        self.pool[1].copy_(up(batch.v_cache, tdt))
+        if kv8:
+            self.pool = torch.empty((2,) + batch.k_cache.shape, dtype=torch.uint8, device=dev)
+            for i, x in enumerate((batch.k_cache, batch.v_cache)):
+                xf = up(x, tdt).to(dev).float() / self.ks
+                self.pool[i].copy_(xf.to(torch.float8_e4m3fn).view(torch.uint8))
+                del xf
+        else:
+            self.pool = torch.empty((2,) + batch.k_cache.shape, dtype=tdt, device=dev)
+            self.pool[0].copy_(up(batch.k_cache, tdt))
+            self.pool[1].copy_(up(batch.v_cache, tdt))
         self.k_cache, self.v_cache = self.pool[0], self.pool[1]
         self.out = torch.empty_like(self.dev_in["q"])
         self.out_host = torch.empty_like(self.host["q"]).pin_memory()
@@ -220,12 +233,13 @@ class AttnStep:
                                                                  self.dev_in["bt"], self.dev_in["ctx"])),
                               dtype=torch.uint8, device=dev)
         es = 4 if batch.dtype == "f32" else 2
+        ek = 1 if kv8 else es                           # bytes of one cached element
         Hq, Hkv, d = batch.num_q_heads, batch.num_kv_heads, batch.head_dim
         T = batch.total_q
         nb = (n + B - 1) // B
-        self.bytes_attn = float(n.sum() * Hkv * d * es * 2 + 2 * T * Hq * d * es + nb.sum() * 4 + batch.num_seqs * 8)
-        self.bytes_append = float(2 * 2 * T * Hkv * d * es + 8 * T)
-        self.bytes_copy = float(len(pairs) * 2 * 2 * Hkv * B * d * es + pairs.size * 8)
+        self.bytes_attn = float(n.sum() * Hkv * d * ek * 2 + 2 * T * Hq * d * es + nb.sum() * 4 + batch.num_seqs * 8)
+        self.bytes_append = float(2 * T * Hkv * d * (es + ek) + 8 * T)
+        self.bytes_copy = float(len(pairs) * 2 * 2 * Hkv * B * d * ek + pairs.size * 8)
         self.flops = attn_flops(batch.ctx_lens, batch.q_lens, Hq, d)
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
         self.d2h_bytes = self.out.numel() * self.out.element_size()
@@ -242,11 +256,12 @@ class AttnStep:
     def step(self, ev=None):
         inp = self.dev_in
         self._copy(inp)
-        self.pkg.kv_append(inp["k_new"], inp["v_new"], inp["slots"], self.k_cache, self.v_cache)
+        self.pkg.kv_append(inp["k_new"], inp["v_new"], inp["slots"], self.k_cache, self.v_cache,
+                           k_scale=self.ks, v_scale=self.vs)
         if ev is not None:
             ev[0].record()
         self.pkg.pa_forward(inp["q"], self.k_cache, self.v_cache, inp["bt"], inp["ctx"], inp["ql"],
-                            self.b.scale, out=self.out, workspace=self.ws)
+                            self.b.scale, out=self.out, workspace=self.ws, k_scale=self.ks, v_scale=self.vs)
         if ev is not None:
             ev[1].record()
 
@@ -488,9 +503,9 @@ def h2d_peak_gbs(dev, nbytes=1 << 30, reps=5):
 
 
 def build_attn_step(name, dev, seqs=None):
-    if name == "decode13b":
+    if name in ("decode13b", "decode13b_fp8"):
         b = W.decode13b(seed=2, num_seqs=seqs or 64, poison=False)
-        return AttnStep(b, dev, cow_frac=0.1, seed=2), b
+        return AttnStep(b, dev, cow_frac=0.1, seed=2, kv8=name.endswith("fp8")), b
     if name == "mixed_gqa":
         half = (seqs or 64) // 2
         b = W.mixed_gqa(seed=3, n_resume=half, n_decode=half, poison=False)
@@ -504,6 +519,8 @@ def build_attn_step(name, dev, seqs=None):
 WORKLOAD_TEXT = {
     "decode13b": "decode13b: 64 seqs, 40 MHA heads, head_dim 128, bf16, block 16, q_len 1, "
                  "ctx U{512..4096}, pool +10% free, 6 copy-on-write forks per step",
+    "decode13b_fp8": "decode13b_fp8: the decode13b batch with FP8 E4M3 K/V caches (scale 1/32 for K and V), "
+                     "bf16 queries and outputs",
     "mixed_gqa": "mixed_gqa: 32 resumed turns (ctx U{1024..16384}, q U{16..512}) + 32 decode "
                  "(ctx U{256..8192}), GQA 32/8, head_dim 128, bf16, block 32",
     "longprefill": "longprefill: 8 seqs x (16384 cached + 2048 new), 40 MHA heads, head_dim 128, "
@@ -606,6 +623,9 @@ def metric_for(name):
         return ("KV movement GB/s (bytes read + written by copy-on-write, append and swap-in per step / step time)", "GB/s", True)
     if name == "decode13b":
         return ("paged-attn decode KV GB/s (algorithmic HBM bytes per step / step time)", "GB/s", True)
+    if name == "decode13b_fp8":
+        return ("paged-attn decode KV GB/s with FP8 E4M3 K/V caches (algorithmic HBM bytes per step / step "
+                "time)", "GB/s", True)
     if name == "layout":
         return ("paged-attn decode KV GB/s on a block-first pool (one layer of L; all layers of a block "
                 "contiguous)", "GB/s", True)
@@ -642,6 +662,7 @@ def run_reference(args):
         print(json.dumps(line), flush=True)
         return
     b = {"decode13b": lambda: W.decode13b(seed=2, poison=False),
+         "decode13b_fp8": lambda: W.decode13b(seed=2, poison=False),
          "mixed_gqa": lambda: W.mixed_gqa(seed=3, poison=False),
          "swap_pipeline": lambda: W.mixed_gqa(seed=3, poison=False),
          "layout": lambda: W.decode13b(seed=2, poison=False),
@@ -762,10 +783,13 @@ def run_native(args):
                          f"passes allowed (all heads, all new tokens), {t:.1f}s; attention only"}
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": hib,
-            "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype, "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 q/out, e4m3 K/V, fp32 accumulate" if step_obj.kv8 else batch.dtype,
+            "data": "synthetic",
             "config": {"workload": workload_text(name, args),
                        "l2": "inputs larger than L2 (KV pool %.2f GB resident)" % (
                            (step_obj.pool.numel() * step_obj.pool.element_size()) / 1e9),
+                       "decode_tokens_per_s": batch.total_q * world / (attn_ms * 1e-3),
                        "bytes_per_step": step_bytes, "attn_flops_per_step": step_obj.flops,
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu,

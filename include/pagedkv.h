@@ -46,6 +46,15 @@ typedef enum {
 
 typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
 
+/* Storage of the K/V caches.  PA_KV_SAME: elements of the call's `dtype`.  PA_KV_E4M3: one-byte
+ * FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 fraction bits; no infinities;
+ * S.1111.111 is NaN) with one float scale for K and one for V: a cached element's value is its
+ * code's value times k_scale (v_scale).  The pages name fewer bits per element as the third way
+ * to shrink the cache ("KVキャッシュ管理の教科書" 第3章) and quantise KV before decoding
+ * (第22章); E4M3 with per-tensor scales is the plainest such format with conversions in
+ * hardware, and halves the bytes decode streams. */
+typedef enum { PA_KV_SAME = 0, PA_KV_E4M3 = 1 } pa_kv_dtype;
+
 /* Bits of the device status word (pa_get_device_status). */
 #define PA_DEV_BAD_BLOCK_ID 0x1u  /* a block-table entry that had to be read was outside the pool */
 #define PA_DEV_BAD_LENGTHS 0x2u   /* q_len < 1, ctx_len < 0, n_i > max_blocks_per_seq * B, or
@@ -81,6 +90,9 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
  *                 aligned; contents need no initialisation and are clobbered.
  * Supported: dtype f32 / bf16 / f16; d in {64, 128}; B in {16, 32, 64, 128}; Hq % Hkv == 0;
  * 16-byte aligned q, out and caches; kv_block_stride * element size a multiple of 16 bytes.
+ * E4M3 caches (kv_dtype = PA_KV_E4M3): dtype bf16 or f16, d = 128, finite k_scale, v_scale > 0;
+ * kv_block_stride counts codes (bytes); every sequence runs on the CUDA-core kernels (the
+ * tensor-core kernel needs both MMA operands of one type).
  * Sequences with q_len * g >= 16 query rows per KV head run on the tcgen05 tensor-core kernel when
  * the dtype is bf16/f16, d = 128, g divides 128 and scale > 0; decode steps, short turns and
  * everything else run on the CUDA-core split-KV kernel.
@@ -102,6 +114,9 @@ typedef struct {
     int64_t num_blocks;         /* physical blocks addressable through k_cache / v_cache */
     int32_t max_blocks_per_seq; /* row length of block_tables */
     int64_t kv_block_stride;    /* elements between physical blocks b and b+1; 0 = Hkv * B * d */
+    int32_t kv_dtype;           /* pa_kv_dtype of k_cache and v_cache (0 = `dtype`) */
+    float k_scale;              /* PA_KV_E4M3: value of a cached K element = code value * k_scale */
+    float v_scale;              /* PA_KV_E4M3: the same for V */
 } pa_dims;
 
 size_t pa_forward_workspace_size(const pa_dims *dims);
@@ -149,10 +164,16 @@ pa_status pa_forward_no_alloc(const pa_dims *dims, const void *q, const void *k_
  * >= num_blocks * B is skipped and flagged PA_DEV_BAD_SLOT.  Two tokens with the same slot in
  * one call give an unspecified one of the two.  The copy is bit-exact.
  *
+ * E4M3 caches (kv_dtype = PA_KV_E4M3; k_new/v_new in bf16, f16 or f32): each new element is
+ * widened to fp32, multiplied by the fp32 reciprocal 1/k_scale (1/v_scale), and rounded to the
+ * nearest E4M3 value, ties to the even code, magnitudes beyond 448 saturating to +-448 (the sign
+ * is kept, also when the result rounds to zero).  Non-finite inputs give unspecified codes.
+ *
  * Layouts (device memory): k_new/v_new element (l, t, h, x) at l*new_layer_stride +
  * (t*Hkv + h)*d + x; caches element (l, b, h, s, x) at l*cache_layer_stride +
- * b*kv_block_stride + (h*B + s)*d + x; slot_mapping int64 [num_tokens].
- * Rows must be 16-byte aligned (d * element size a multiple of 16).
+ * b*kv_block_stride + (h*B + s)*d + x (cache strides count codes for E4M3 caches);
+ * slot_mapping int64 [num_tokens].  Rows must be 16-byte aligned (d * element size a multiple
+ * of 16, for the new tokens and for the caches).
  * ---------------------------------------------------------------------------------------- */
 typedef struct {
     int32_t dtype;              /* pa_dtype (only the element size matters) */
@@ -165,6 +186,9 @@ typedef struct {
     int32_t num_layers;         /* >= 1 */
     int64_t new_layer_stride;   /* 0 = num_tokens * Hkv * d */
     int64_t cache_layer_stride; /* 0 = num_blocks * kv_block_stride */
+    int32_t kv_dtype;           /* pa_kv_dtype of the caches (0 = `dtype`) */
+    float k_scale;              /* PA_KV_E4M3: > 0; K is stored as code(k / k_scale) */
+    float v_scale;              /* PA_KV_E4M3: > 0 */
 } kv_append_dims;
 
 pa_status kv_append(const kv_append_dims *dims, const void *k_new, const void *v_new,

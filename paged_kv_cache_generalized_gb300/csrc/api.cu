@@ -79,6 +79,11 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 bool valid_dtype(int32_t t) { return t == PA_F32 || t == PA_BF16 || t == PA_F16; }
 
+bool valid_scale(float x) { return x > 0.f && x <= 3.4e38f; }   // finite and positive (NaN fails)
+
+// Bytes of one cached element.
+int kv_elem_bytes(int32_t dtype, int32_t kv_dtype) { return kv_dtype == PA_KV_E4M3 ? 1 : elem_bytes(dtype); }
+
 bool overlap(const void *a, size_t an, const void *b, size_t bn) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + bn && y < x + an;
@@ -95,10 +100,15 @@ pa_status check_dims(const pa_dims *d) {
     if (d->head_dim != 64 && d->head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64 && d->block_size != 128)
         return PA_ERR_UNSUPPORTED;
+    if (d->kv_dtype != PA_KV_SAME && d->kv_dtype != PA_KV_E4M3) return PA_ERR_INVALID_ARG;
+    if (d->kv_dtype == PA_KV_E4M3) {
+        if (!valid_scale(d->k_scale) || !valid_scale(d->v_scale)) return PA_ERR_INVALID_ARG;
+        if (d->dtype == PA_F32 || d->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    }
     const int64_t dense = (int64_t)d->num_kv_heads * d->block_size * d->head_dim;
     if (d->kv_block_stride != 0) {
         if (d->kv_block_stride < dense) return PA_ERR_INVALID_ARG;
-        if ((d->kv_block_stride * elem_bytes(d->dtype)) % 16) return PA_ERR_INVALID_ARG;
+        if ((d->kv_block_stride * kv_elem_bytes(d->dtype, d->kv_dtype)) % 16) return PA_ERR_INVALID_ARG;
     }
     if ((int64_t)d->max_blocks_per_seq * d->block_size > (int64_t(1) << 30)) return PA_ERR_INVALID_ARG;
     return PA_OK;
@@ -153,7 +163,7 @@ using namespace pkv;
 
 extern "C" {
 
-const char *pa_version(void) { return "pagedkv 0.2 sm_103a"; }
+const char *pa_version(void) { return "pagedkv 0.3 sm_103a"; }
 
 const char *pa_status_string(pa_status s) {
     switch (s) {
@@ -206,7 +216,7 @@ pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, co
     a.num_sms = sm_count();
     if (!a.status || a.num_sms <= 0) return PA_ERR_CUDA;
     a.maybe_prefill = d.total_q > d.num_seqs;
-    a.tc = a.maybe_prefill && scale > 0.f && tc_supported(d);
+    a.tc = a.maybe_prefill && scale > 0.f && d.kv_dtype == PA_KV_SAME && tc_supported(d);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (launch_plan(a, s) != cudaSuccess) return PA_ERR_CUDA;
     if (a.tc) {
@@ -234,17 +244,21 @@ pa_status kv_append(const kv_append_dims *dims, const void *k_new, const void *v
     if (!valid_dtype(d.dtype) || d.num_tokens < 0 || d.num_kv_heads < 1 || d.head_dim < 1 ||
         d.block_size < 1 || d.num_blocks < 1 || d.num_layers < 1)
         return PA_ERR_INVALID_ARG;
+    if (d.kv_dtype != PA_KV_SAME && d.kv_dtype != PA_KV_E4M3) return PA_ERR_INVALID_ARG;
+    if (d.kv_dtype == PA_KV_E4M3 && (!valid_scale(d.k_scale) || !valid_scale(d.v_scale)))
+        return PA_ERR_INVALID_ARG;
     if (d.num_tokens == 0) return PA_OK;
-    const int eb = elem_bytes(d.dtype);
-    if ((d.head_dim * eb) % 16) return PA_ERR_UNSUPPORTED;
+    const int eb = elem_bytes(d.dtype);                 // new tokens
+    const int cb = kv_elem_bytes(d.dtype, d.kv_dtype);  // caches
+    if ((d.head_dim * eb) % 16 || (d.head_dim * cb) % 16) return PA_ERR_UNSUPPORTED;
     if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
     if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
         !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
         return PA_ERR_INVALID_ARG;
     const int64_t dense = (int64_t)d.num_kv_heads * d.block_size * d.head_dim;
-    if (d.kv_block_stride && (d.kv_block_stride < dense || (d.kv_block_stride * eb) % 16))
+    if (d.kv_block_stride && (d.kv_block_stride < dense || (d.kv_block_stride * cb) % 16))
         return PA_ERR_INVALID_ARG;
-    if ((d.new_layer_stride * eb) % 16 || (d.cache_layer_stride * eb) % 16) return PA_ERR_INVALID_ARG;
+    if ((d.new_layer_stride * eb) % 16 || (d.cache_layer_stride * cb) % 16) return PA_ERR_INVALID_ARG;
     if (d.num_layers > 1) {
         const int64_t bs = d.kv_block_stride ? d.kv_block_stride : dense;
         if (d.new_layer_stride && d.new_layer_stride < d.num_tokens * d.num_kv_heads * d.head_dim)

@@ -253,7 +253,8 @@ struct SimtParams {
     float *parts_o;
     unsigned *status;
     int64_t num_blocks, block_stride;   // elements
-    float scale_log2;                   // scale * log2(e)
+    float scale_log2;                   // scale * log2(e) (* k_scale for E4M3 caches)
+    float v_scale;                      // 1, or the V scale of E4M3 caches
     int num_seqs, q_heads, kv_heads, group, block_size, max_blocks, nst, bar_bytes;
 };
 
@@ -323,10 +324,10 @@ __device__ __forceinline__ void finish_split(const SimtParams &p, int seq, int k
     }
 }
 
-template <typename T, int D, int R>
+template <typename T, typename TK, int D, int R>
 __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(SimtParams p) {
     constexpr int E = D / 16;                       // dims per lane
-    constexpr uint32_t kRunBytes = kStageTokens * D * sizeof(T);
+    constexpr uint32_t kRunBytes = kStageTokens * D * sizeof(TK);
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = lane >> 4, sub = lane & 15;
@@ -437,8 +438,8 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
                 unsigned char *dst = ring + (size_t)slot * 2 * kRunBytes;
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(&bars[slot], 2 * kRunBytes);
-                bulk_g2s(dst, p.k + off * sizeof(T), kRunBytes, &bars[slot]);
-                bulk_g2s(dst + kRunBytes, p.v + off * sizeof(T), kRunBytes, &bars[slot]);
+                bulk_g2s(dst, p.k + off * sizeof(TK), kRunBytes, &bars[slot]);
+                bulk_g2s(dst + kRunBytes, p.v + off * sizeof(TK), kRunBytes, &bars[slot]);
             }
             ++issued;
         };
@@ -456,8 +457,8 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
                 timed_out = true;
                 break;
             }
-            const T *sk = reinterpret_cast<const T *>(ring + (size_t)slot * 2 * kRunBytes);
-            const T *sv = reinterpret_cast<const T *>(ring + (size_t)slot * 2 * kRunBytes + kRunBytes);
+            const TK *sk = reinterpret_cast<const TK *>(ring + (size_t)slot * 2 * kRunBytes);
+            const TK *sv = reinterpret_cast<const TK *>(ring + (size_t)slot * 2 * kRunBytes + kRunBytes);
             const int64_t p0 = st * kStageTokens;
 
             float s[R][kStageTokens / 2];
@@ -465,11 +466,11 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
             for (int i = 0; i < kStageTokens / 2; ++i) {
                 const int key = 2 * i + half;
                 uint64_t k2[E / 2];
-                if constexpr (E * sizeof(T) >= 16) {
-                    load_pairs<T, E / 2>(sk + key * D + sub * E, k2);
+                if constexpr (E * sizeof(TK) >= 16 || sizeof(TK) == 1) {
+                    load_pairs<TK, E / 2>(sk + key * D + sub * E, k2);
                 } else {
                     float kf[E];
-                    load_f<T, E>(sk + key * D + sub * E, kf);
+                    load_f<TK, E>(sk + key * D + sub * E, kf);
 #pragma unroll
                     for (int e = 0; e < E / 2; ++e) k2[e] = f2pack(kf[2 * e], kf[2 * e + 1]);
                 }
@@ -514,11 +515,11 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
                 const int key = 2 * i + half;
                 if (p0 + key > Pmax) continue;        // never read slots past the last query
                 uint64_t v2[E / 2];
-                if constexpr (E * sizeof(T) >= 16) {
-                    load_pairs<T, E / 2>(sv + key * D + sub * E, v2);
+                if constexpr (E * sizeof(TK) >= 16 || sizeof(TK) == 1) {
+                    load_pairs<TK, E / 2>(sv + key * D + sub * E, v2);
                 } else {
                     float vf[E];
-                    load_f<T, E>(sv + key * D + sub * E, vf);
+                    load_f<TK, E>(sv + key * D + sub * E, vf);
 #pragma unroll
                     for (int e = 0; e < E / 2; ++e) v2[e] = f2pack(vf[2 * e], vf[2 * e + 1]);
                 }
@@ -549,12 +550,13 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
         for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int e = 0; e < E / 2; ++e) f2unpack(acc2[r][e], acc[r][2 * e], acc[r][2 * e + 1]);
-        // merge the two half-warps (alternate keys)
+        // merge the two half-warps (alternate keys); V's scale (E4M3 caches) applies to o
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             l[r] += __shfl_xor_sync(0xffffffffu, l[r], 16);
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], 16);
+            for (int e = 0; e < E; ++e)
+                acc[r][e] = (acc[r][e] + __shfl_xor_sync(0xffffffffu, acc[r][e], 16)) * p.v_scale;
         }
         if (K == 1) {
             if (half == 0) {
@@ -619,14 +621,14 @@ struct GqaStage {
     static constexpr uint32_t kBytes = kK + kV;              // a multiple of 1024
 };
 
-template <typename T, int D, int R>
+template <typename T, typename TK, int D, int R>
 __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
     simt_gqa_kernel(const __grid_constant__ CUtensorMap kmap, SimtParams p) {
     static_assert(R == 2 || R == 4, "two or four rows per item");
-    using S = GqaStage<T, D>;
+    using S = GqaStage<TK, D>;
     constexpr int QD = D / 4;                       // dims per quarter lane (QK^T)
     constexpr int E = D / 16;                       // dims per lane (PV)
-    constexpr int EC = 16 / (int)sizeof(T);         // elements per 16-byte chunk
+    constexpr int EC = 16 / (int)sizeof(TK);        // elements per 16-byte chunk
     constexpr int NJ = QD / EC;                     // chunks per quarter lane and key
     constexpr int kPs = (kStageTokens + 1) * R;     // (p, p) pairs of a warp: 16 keys + alpha
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -650,7 +652,7 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
     int koff[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-        const int ob = qd * QD * (int)sizeof(T) + j * 16;
+        const int ob = qd * QD * (int)sizeof(TK) + j * 16;
         koff[j] = (ob >> 7) * S::kPanelBytes + ((((ob >> 4) & 7) ^ kk) << 4);
     }
     if (lane == 0) {
@@ -749,9 +751,9 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
                 mbar_arrive_expect_tx(&bars[slot_i], S::kK + S::kV);
 #pragma unroll
                 for (int pn = 0; pn < S::kPanels; ++pn)
-                    tma_load_3d(dst + pn * S::kPanelBytes, &kmap, pn * (128 / (int)sizeof(T)), row, phys,
+                    tma_load_3d(dst + pn * S::kPanelBytes, &kmap, pn * (128 / (int)sizeof(TK)), row, phys,
                                 &bars[slot_i]);
-                bulk_g2s(dst + S::kK, p.v + off * sizeof(T), S::kV, &bars[slot_i]);
+                bulk_g2s(dst + S::kK, p.v + off * sizeof(TK), S::kV, &bars[slot_i]);
             }
             slot_i = slot_i + 1 == NST ? 0 : slot_i + 1;
             ++inflight;
@@ -775,7 +777,7 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
                 break;
             }
             const unsigned char *sk = ring + (size_t)slot_c * S::kBytes;
-            const T *sv = reinterpret_cast<const T *>(sk + S::kK);
+            const TK *sv = reinterpret_cast<const TK *>(sk + S::kK);
             const int p0 = st * kStageTokens;
 
             // scores: lane (qd, kk) ends with row rrow's score of keys kk and 8 + kk
@@ -790,7 +792,7 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
 #pragma unroll
                 for (int j = 0; j < NJ; ++j) {
                     uint64_t k2[EC / 2];
-                    load_pairs<T, EC / 2>(reinterpret_cast<const T *>(kr + koff[j]), k2);
+                    load_pairs<TK, EC / 2>(reinterpret_cast<const TK *>(kr + koff[j]), k2);
 #pragma unroll
                     for (int e = 0; e < EC / 2; ++e)
 #pragma unroll
@@ -856,11 +858,11 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
                     pr[r + 1] = (uint64_t)t.z | ((uint64_t)t.w << 32);
                 }
                 uint64_t v2[E / 2];
-                if constexpr (E * sizeof(T) >= 16) {
-                    load_pairs<T, E / 2>(sv + key * D + sub * E, v2);
+                if constexpr (E * sizeof(TK) >= 16 || sizeof(TK) == 1) {
+                    load_pairs<TK, E / 2>(sv + key * D + sub * E, v2);
                 } else {
                     float vf[E];
-                    load_f<T, E>(sv + key * D + sub * E, vf);
+                    load_f<TK, E>(sv + key * D + sub * E, vf);
 #pragma unroll
                     for (int e = 0; e < E / 2; ++e) v2[e] = f2pack(vf[2 * e], vf[2 * e + 1]);
                 }
@@ -909,7 +911,8 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
 #pragma unroll
             for (int e = 0; e < E / 2; ++e) f2unpack(acc2[r][e], acc[r][2 * e], acc[r][2 * e + 1]);
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[r][e] += __shfl_xor_sync(0xffffffffu, acc[r][e], 16);
+            for (int e = 0; e < E; ++e)
+                acc[r][e] = (acc[r][e] + __shfl_xor_sync(0xffffffffu, acc[r][e], 16)) * p.v_scale;
         }
         if (half == 0) {
             if (K == 1) {
@@ -947,10 +950,10 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
                               lane);
 }
 
-template <typename T, int D, int R>
+template <typename T, typename TK, int D, int R>
 cudaError_t launch_simt_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s) {
     SimtParams p = p0;
-    const size_t run = (size_t)kStageTokens * D * sizeof(T);
+    const size_t run = (size_t)kStageTokens * D * sizeof(TK);
     const size_t stage = 2 * run;
     const size_t budget = 200 * 1024;
     int nst = stage <= 8192 ? 3 : 2;
@@ -963,7 +966,7 @@ cudaError_t launch_simt_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s
     p.nst = nst;
     p.bar_bytes = (int)align_up((size_t)warps * nst * sizeof(uint64_t), 128);
     const size_t smem = p.bar_bytes + (size_t)warps * nst * stage;
-    auto kern = simt_attention_kernel<T, D, R>;
+    auto kern = simt_attention_kernel<T, TK, D, R>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -974,14 +977,14 @@ cudaError_t launch_simt_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s
     return cudaGetLastError();
 }
 
-template <typename T, int D, int R>
+template <typename T, typename TK, int D, int R>
 cudaError_t launch_gqa_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s) {
     SimtParams p = p0;
-    using S = GqaStage<T, D>;
+    using S = GqaStage<TK, D>;
     // K as [num_blocks][Hkv * B rows][D], one TMA box = one 128-byte panel of 16 rows
     CUtensorMap kmap;
-    const uint64_t es = sizeof(T);
-    if (!make_map_3d(&kmap, a.dims.dtype, a.k, D, (uint64_t)a.dims.num_kv_heads * a.dims.block_size,
+    const uint64_t es = sizeof(TK);
+    if (!make_map_3d(&kmap, sizeof(TK) == 1 ? kMapBytes : a.dims.dtype, a.k, D, (uint64_t)a.dims.num_kv_heads * a.dims.block_size,
                      a.dims.num_blocks, D * es, (uint64_t)p.block_stride * es, (uint32_t)(128 / es),
                      kStageTokens, 1))
         return cudaErrorInvalidValue;
@@ -999,25 +1002,29 @@ cudaError_t launch_gqa_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s)
     p.nst = nst;
     p.bar_bytes = 0;
     const size_t smem = 1024 + (size_t)warps * (nst * per_stage + ps_bytes);
-    auto kern = simt_gqa_kernel<T, D, R>;
+    auto kern = simt_gqa_kernel<T, TK, D, R>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<a.num_sms, warps * 32, smem, s>>>(kmap, p);
     return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, typename TK, int D>
 cudaError_t launch_simt_rows(const FwdArgs &a, const SimtParams &p, cudaStream_t s) {
     switch (a.lay.rows_per_item) {
-    case 1: return launch_simt_t<T, D, 1>(a, p, s);
-    case 2: return launch_gqa_t<T, D, 2>(a, p, s);
-    default: return launch_gqa_t<T, D, 4>(a, p, s);
+    case 1: return launch_simt_t<T, TK, D, 1>(a, p, s);
+    case 2: return launch_gqa_t<T, TK, D, 2>(a, p, s);
+    default: return launch_gqa_t<T, TK, D, 4>(a, p, s);
     }
 }
 
 template <typename T>
 cudaError_t launch_simt_dim(const FwdArgs &a, const SimtParams &p, cudaStream_t s) {
-    return a.dims.head_dim == 64 ? launch_simt_rows<T, 64>(a, p, s) : launch_simt_rows<T, 128>(a, p, s);
+    if (a.dims.kv_dtype == PA_KV_E4M3) {
+        if constexpr (sizeof(T) == 2) return launch_simt_rows<T, e4m3, 128>(a, p, s);
+        return cudaErrorInvalidValue;
+    }
+    return a.dims.head_dim == 64 ? launch_simt_rows<T, T, 64>(a, p, s) : launch_simt_rows<T, T, 128>(a, p, s);
 }
 
 }  // namespace
@@ -1076,7 +1083,9 @@ cudaError_t launch_simt(const FwdArgs &a, cudaStream_t s) {
     p.num_blocks = a.dims.num_blocks;
     const int64_t dflt = (int64_t)a.dims.num_kv_heads * a.dims.block_size * a.dims.head_dim;
     p.block_stride = a.dims.kv_block_stride ? a.dims.kv_block_stride : dflt;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const bool e4 = a.dims.kv_dtype == PA_KV_E4M3;
+    p.scale_log2 = a.scale * 1.4426950408889634f * (e4 ? a.dims.k_scale : 1.f);
+    p.v_scale = e4 ? a.dims.v_scale : 1.f;
     p.num_seqs = a.dims.num_seqs;
     p.q_heads = a.dims.num_q_heads;
     p.kv_heads = a.dims.num_kv_heads;

@@ -124,8 +124,8 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     return r;
 }
 
-// Widens 2*NP consecutive 16-bit (or fp32) elements to NP packed fp32 pairs (even, odd), ready
-// for the packed fp32 instructions.  bf16 -> fp32 is exact by moving the 16 bits into the high
+// Widens 2*NP consecutive 16-bit, fp32 or E4M3 elements to NP packed fp32 pairs (even, odd),
+// ready for the packed fp32 instructions.  bf16 -> fp32 is exact by moving the 16 bits into the high
 // half of a word (a shift for the even element, a mask for the odd one); f16 uses the hardware
 // conversion; fp32 pairs are the loaded words themselves.  16-byte aligned, 16-byte multiples.
 template <typename T> __device__ __forceinline__ uint64_t widen2(uint32_t w);
@@ -146,10 +146,56 @@ template <> __device__ __forceinline__ uint64_t widen2<__half>(uint32_t w) {
     return r;
 }
 
+// One FP8 E4M3 code (1 sign, 4 exponent bits with bias 7, 3 fraction bits), the storage element
+// of 8-bit K/V caches.
+struct e4m3 {
+    uint8_t bits;
+};
+
+// Four E4M3 codes (bytes 0..3 of w, element order) -> two packed fp32 pairs, exactly: the
+// hardware conversion to f16 pairs (every E4M3 value is an f16 value), then f16 -> f32.
+__device__ __forceinline__ void widen4_e4m3(uint32_t w, uint64_t &p01, uint64_t &p23) {
+    asm("{\n\t.reg .b16 lo, hi, a0, a1, a2, a3;\n\t.reg .b32 h0, h1;\n\t.reg .f32 f0, f1, f2, f3;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h0, lo;\n\tcvt.rn.f16x2.e4m3x2 h1, hi;\n\t"
+        "mov.b32 {a0, a1}, h0;\n\tmov.b32 {a2, a3}, h1;\n\t"
+        "cvt.f32.f16 f0, a0;\n\tcvt.f32.f16 f1, a1;\n\tcvt.f32.f16 f2, a2;\n\tcvt.f32.f16 f3, a3;\n\t"
+        "mov.b64 %0, {f0, f1};\n\tmov.b64 %1, {f2, f3};\n\t}"
+        : "=l"(p01), "=l"(p23)
+        : "r"(w));
+}
+
+// Two fp32 values -> two E4M3 codes (a in the low byte), rounded to nearest even with the
+// magnitude saturated at 448.
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float a, float b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+    return r;
+}
+
 template <typename T, int NP>
 __device__ __forceinline__ void load_pairs(const T *p, uint64_t (&out)[NP]) {
-    static_assert((2 * NP * sizeof(T)) % 16 == 0, "16-byte vectors");
-    if constexpr (sizeof(T) == 4) {
+    if constexpr (sizeof(T) == 1) {            // E4M3 codes: 8-byte or 16-byte vectors
+        static_assert((2 * NP) % 8 == 0, "8-byte vectors");
+        if constexpr ((2 * NP) % 16 == 0) {
+#pragma unroll
+            for (int w = 0; w < NP / 8; ++w) {
+                const uint4 v = reinterpret_cast<const uint4 *>(p)[w];
+                widen4_e4m3(v.x, out[8 * w], out[8 * w + 1]);
+                widen4_e4m3(v.y, out[8 * w + 2], out[8 * w + 3]);
+                widen4_e4m3(v.z, out[8 * w + 4], out[8 * w + 5]);
+                widen4_e4m3(v.w, out[8 * w + 6], out[8 * w + 7]);
+            }
+        } else {
+#pragma unroll
+            for (int w = 0; w < NP / 4; ++w) {
+                const uint2 v = reinterpret_cast<const uint2 *>(p)[w];
+                widen4_e4m3(v.x, out[4 * w], out[4 * w + 1]);
+                widen4_e4m3(v.y, out[4 * w + 2], out[4 * w + 3]);
+            }
+        }
+    } else if constexpr (sizeof(T) == 4) {
+        static_assert((2 * NP * sizeof(T)) % 16 == 0, "16-byte vectors");
 #pragma unroll
         for (int w = 0; w < NP / 2; ++w) {
             const uint4 v = reinterpret_cast<const uint4 *>(p)[w];
@@ -157,6 +203,7 @@ __device__ __forceinline__ void load_pairs(const T *p, uint64_t (&out)[NP]) {
             out[2 * w + 1] = (uint64_t)v.z | ((uint64_t)v.w << 32);
         }
     } else {
+        static_assert((2 * NP * sizeof(T)) % 16 == 0, "16-byte vectors");
 #pragma unroll
         for (int w = 0; w < NP / 4; ++w) {
             const uint4 v = reinterpret_cast<const uint4 *>(p)[w];

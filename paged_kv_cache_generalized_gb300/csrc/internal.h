@@ -97,6 +97,8 @@ cudaError_t launch_block_copy(const block_copy_dims &d, const void *src, void *d
 
 // Tensor maps (tensor_map.cu): a 3-D tiled map (dims d0 innermost, d1, d2; byte strides of d1 and
 // d2; box b0 x b1 x b2 elements, b0 * element size = 128 bytes) with 128-byte swizzle.
+// dtype code of make_map_3d for one-byte elements (E4M3 caches)
+constexpr int kMapBytes = 100;
 bool tensor_maps_available();
 bool make_map_3d(CUtensorMap *map, int dtype, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                  uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);

@@ -38,9 +38,10 @@ bool make_map_3d(CUtensorMap *map, int dtype, const void *base, uint64_t d0, uin
     const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
     const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapDataType t = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                  : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType t = dtype == PA_F32      ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                  : dtype == PA_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                  : dtype == kMapBytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUresult r = enc(map, t, 3, const_cast<void *>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

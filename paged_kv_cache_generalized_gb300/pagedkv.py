@@ -26,6 +26,9 @@ STATUS_BITS = {
     0x10: "PA_DEV_TIMEOUT",
 }
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+PA_KV_SAME, PA_KV_E4M3 = 0, 1
+# K/V caches of one-byte E4M3 codes may be given as uint8 or as torch's float8_e4m3fn
+_E4M3 = tuple(t for t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if t is not None)
 _ELEM = {torch.float32: 4, torch.bfloat16: 2, torch.float16: 2}
 
 EXPORTED = ("pa_forward_workspace_size", "pa_forward", "pa_forward_no_alloc", "kv_append",
@@ -38,7 +41,8 @@ class PaDims(ctypes.Structure):
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int64), ("max_blocks_per_seq", ctypes.c_int32),
-                ("kv_block_stride", ctypes.c_int64)]
+                ("kv_block_stride", ctypes.c_int64), ("kv_dtype", ctypes.c_int32),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class KvAppendDims(ctypes.Structure):
@@ -46,7 +50,8 @@ class KvAppendDims(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64),
                 ("kv_block_stride", ctypes.c_int64), ("num_layers", ctypes.c_int32),
-                ("new_layer_stride", ctypes.c_int64), ("cache_layer_stride", ctypes.c_int64)]
+                ("new_layer_stride", ctypes.c_int64), ("cache_layer_stride", ctypes.c_int64),
+                ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class BlockCopyDims(ctypes.Structure):
@@ -122,38 +127,50 @@ def _cache_geometry(cache: torch.Tensor):
     return nb, hkv, bs, d, cache.stride(0)
 
 
-def forward_dims(q, k_cache, block_tables, ctx_lens) -> PaDims:
+def _kv_kind(cache, dtype, k_scale, v_scale):
+    """(kv_dtype, k_scale, v_scale) of a cache tensor: E4M3 codes need both scales."""
+    if cache.dtype in _E4M3:
+        if k_scale is None or v_scale is None:
+            raise ValueError("E4M3 caches need k_scale and v_scale")
+        return PA_KV_E4M3, float(k_scale), float(v_scale)
+    if cache.dtype != dtype:
+        raise ValueError("q and caches must share a dtype (or the caches hold E4M3 codes)")
+    return PA_KV_SAME, 1.0, 1.0
+
+
+def forward_dims(q, k_cache, block_tables, ctx_lens, k_scale=None, v_scale=None) -> PaDims:
     nb, hkv, bs, d, bstride = _cache_geometry(k_cache)
     T, hq, dq = q.shape
     if dq != d:
         raise ValueError("q and cache head_dim differ")
+    kind, ks, vs = _kv_kind(k_cache, q.dtype, k_scale, v_scale)
     return PaDims(_DTYPES[q.dtype], ctx_lens.shape[0], T, hq, hkv, d, bs, nb,
-                  block_tables.shape[1], bstride)
+                  block_tables.shape[1], bstride, kind, ks, vs)
 
 
 def forward_workspace_size(q, k_cache, block_tables, ctx_lens) -> int:
-    dims = forward_dims(q, k_cache, block_tables, ctx_lens)
+    dims = forward_dims(q, k_cache, block_tables, ctx_lens, 1.0, 1.0)
     return int(load_library().pa_forward_workspace_size(ctypes.byref(dims)))
 
 
 def pa_forward(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale=None, out=None,
-               workspace=None, stream=None):
+               workspace=None, stream=None, k_scale=None, v_scale=None):
     """Generalized paged attention (see ``pa_forward`` in include/pagedkv.h).
 
-    q: [T, Hq, d]; k_cache/v_cache: [num_blocks, Hkv, B, d] (same dtype as q); block_tables:
-    int32 [S, max_blocks]; ctx_lens/q_lens: int32 [S].  Returns ``out`` ([T, Hq, d])."""
+    q: [T, Hq, d]; k_cache/v_cache: [num_blocks, Hkv, B, d] in q's dtype, or E4M3 codes (uint8 or
+    float8_e4m3fn) with ``k_scale`` / ``v_scale``; block_tables: int32 [S, max_blocks];
+    ctx_lens/q_lens: int32 [S].  Returns ``out`` ([T, Hq, d])."""
     lib = load_library()
     if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
         raise ValueError("k_cache and v_cache must have the same shape and strides")
-    for t in (k_cache, v_cache):
-        if t.dtype != q.dtype:
-            raise ValueError("q and caches must share a dtype")
+    if v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must share a dtype")
     for t in (block_tables, ctx_lens, q_lens):
         if t.dtype != torch.int32 or not t.is_contiguous():
             raise ValueError("block_tables, ctx_lens and q_lens must be contiguous int32")
     if not q.is_contiguous():
         raise ValueError("q must be contiguous [T, Hq, d]")
-    dims = forward_dims(q, k_cache, block_tables, ctx_lens)
+    dims = forward_dims(q, k_cache, block_tables, ctx_lens, k_scale, v_scale)
     if scale is None:
         scale = 1.0 / float(dims.head_dim) ** 0.5
     if out is None:
@@ -170,14 +187,14 @@ def pa_forward(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale=None, 
 
 
 def pa_forward_no_alloc(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale=None, out=None,
-                        stream=None):
+                        stream=None, k_scale=None, v_scale=None):
     """pa_forward with the library's own fixed-size scratch (see ``pa_forward_no_alloc`` in
     include/pagedkv.h): for callers that cannot allocate device memory.  Raises if the batch
     needs more scratch than the library holds."""
     lib = load_library()
     if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
         raise ValueError("k_cache and v_cache must have the same shape and strides")
-    dims = forward_dims(q, k_cache, block_tables, ctx_lens)
+    dims = forward_dims(q, k_cache, block_tables, ctx_lens, k_scale, v_scale)
     if scale is None:
         scale = 1.0 / float(dims.head_dim) ** 0.5
     if out is None:
@@ -189,11 +206,12 @@ def pa_forward_no_alloc(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, sca
     return out
 
 
-def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
+def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None, k_scale=None, v_scale=None):
     """Writes new tokens' K/V into their slots (see ``kv_append`` in include/pagedkv.h).
 
     Single layer: k_new [T, Hkv, d], caches [num_blocks, Hkv, B, d].  Several layers: k_new
-    [L, T, Hkv, d], caches [L, num_blocks, Hkv, B, d] (layer and block dims may be strided)."""
+    [L, T, Hkv, d], caches [L, num_blocks, Hkv, B, d] (layer and block dims may be strided).
+    E4M3 caches (uint8 or float8_e4m3fn) quantise the new tokens with ``k_scale`` / ``v_scale``."""
     lib = load_library()
     if k_new.dim() == 3:
         k_new, v_new, k_cache, v_cache = (x.unsqueeze(0) for x in (k_new, v_new, k_cache, v_cache))
@@ -209,8 +227,12 @@ def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
         raise ValueError("kv_append: each layer of k_new must be contiguous [T, Hkv, d]")
     if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous():
         raise ValueError("slot_mapping must be contiguous int64")
+    if k_cache.dtype != v_cache.dtype:
+        raise ValueError("kv_append: k_cache and v_cache must share a dtype")
+    kind, ks, vs = _kv_kind(k_cache, k_new.dtype, k_scale, v_scale)
     dims = KvAppendDims(_DTYPES[k_new.dtype], T, hkv, d, bs, nb, bstride, L,
-                        k_new.stride(0) if L > 1 else 0, k_cache.stride(0) if L > 1 else 0)
+                        k_new.stride(0) if L > 1 else 0, k_cache.stride(0) if L > 1 else 0,
+                        kind, ks, vs)
     rc = lib.kv_append(ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
                        _ptr(k_cache), _ptr(v_cache), _stream(stream))
     _check(rc, "kv_append")

@@ -132,3 +132,28 @@ def test_append_and_copy_reject_bad_arguments(lib):
     assert lib.block_copy(ctypes.byref(c), ctypes.c_void_p(0x10004), FAKE, FAKE, None) == 1
     c.max_ctas = -1                                    # a negative grid bound is refused
     assert lib.block_copy(ctypes.byref(c), FAKE, FAKE, FAKE, None) == 1
+
+
+def test_e4m3_caches_reject_bad_scales_and_unsupported_shapes(lib):
+    from paged_kv_cache_generalized_gb300.pagedkv import KvAppendDims, PaDims
+
+    d = PaDims(dtype=1, num_seqs=1, total_q=1, num_q_heads=8, num_kv_heads=8, head_dim=128,
+               block_size=16, num_blocks=10, max_blocks_per_seq=4, kv_block_stride=0, kv_dtype=1,
+               k_scale=0.5, v_scale=0.5)
+    assert lib.pa_forward_workspace_size(ctypes.byref(d)) > 0
+    for field, value, code in (("k_scale", 0.0, 1), ("v_scale", -1.0, 1), ("k_scale", float("nan"), 1),
+                               ("v_scale", float("inf"), 1), ("kv_dtype", 2, 1), ("dtype", 0, 2),
+                               ("head_dim", 64, 2)):
+        bad = PaDims.from_buffer_copy(d)
+        setattr(bad, field, value)
+        assert lib.pa_forward_workspace_size(ctypes.byref(bad)) == 0, field
+        rc = lib.pa_forward(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.1),
+                            ctypes.c_void_p(0x20000), FAKE, 1 << 30, None)
+        assert rc == code, (field, rc)
+    a = KvAppendDims(dtype=1, num_tokens=4, num_kv_heads=2, head_dim=64, block_size=16, num_blocks=8,
+                     kv_block_stride=0, num_layers=1, new_layer_stride=0, cache_layer_stride=0,
+                     kv_dtype=1, k_scale=0.0, v_scale=1.0)
+    assert lib.kv_append(ctypes.byref(a), FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1   # zero scale
+    a.k_scale = 1.0
+    a.head_dim = 8                                     # 8 codes per row: not a 16-byte vector
+    assert lib.kv_append(ctypes.byref(a), FAKE, FAKE, FAKE, FAKE, FAKE, None) == 2

@@ -1,0 +1,120 @@
+"""GPU parity of the 8-bit cache path (FP8 E4M3 codes, one scale for K and one for V) against the
+float64 oracle, through the C ABI: the quantising append bit for bit, attention on E4M3 caches
+within the bf16 tolerances (every row of small cases, sampled rows of the full decode batch).
+
+Cache contents are N(0,1) values (the generator module's) encoded by the oracle's E4M3 encoder,
+so the codes span the format's normal and subnormal range the way real K/V do."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_generalized_gb300 as pkg
+from paged_kv_cache_generalized_gb300 import workloads as W
+
+from gpu_util import as_f64, assert_close, gather_rows, sample_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    pkg.device_status()
+    yield
+
+
+def _codes(shape, scale, seed):
+    x = W.normal_f32(shape, seed)
+    return oracle.e4m3_encode(x, np.float32(1.0) / np.float32(scale))
+
+
+def _fp8_batch(name, ctx, ql, hq, hkv, B, dtype, ks, vs, seed, **kw):
+    b = W.make_attn_batch(name, ctx, ql, hq, hkv, 128, B, dtype, seed=seed, poison=False, **kw)
+    kc = _codes(b.k_cache.shape, ks, seed + 1)
+    vc = _codes(b.v_cache.shape, vs, seed + 2)
+    return b, kc, vc
+
+
+def _run(b, kc, vc, ks, vs):
+    q = to_dev(b.q, b.dtype)
+    out = pkg.pa_forward(q, torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(),
+                         to_dev(b.block_tables), to_dev(b.ctx_lens), to_dev(b.q_lens), b.scale,
+                         k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkg.device_status() == 0
+    return out
+
+
+CASES = [
+    # name, ctx, q, Hq, Hkv, B, dtype, k_scale, v_scale
+    ("decode_mha", [512, 1000, 37, 4096, 15], [1] * 5, 8, 8, 16, "bf16", 1 / 32, 1 / 16),
+    ("decode_gqa4", [700, 33, 2000, 0], [1] * 4, 16, 4, 32, "bf16", 0.05, 0.02),
+    ("decode_gqa2_f16", [300, 129, 64], [1] * 3, 8, 4, 16, "f16", 1 / 64, 1 / 64),
+    ("turns_on_cuda_cores", [300, 0, 129], [40, 33, 5], 8, 2, 16, "bf16", 0.03, 0.03),
+    ("mha_turns", [100, 7], [20, 3], 4, 4, 64, "bf16", 1.0 / 8, 0.25),
+    ("long_split", [16000, 9000], [1, 1], 8, 8, 32, "bf16", 1 / 32, 1 / 32),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_attention_on_e4m3_caches(case):
+    name, ctx, ql, hq, hkv, B, dtype, ks, vs = case
+    b, kc, vc = _fp8_batch(name, ctx, ql, hq, hkv, B, dtype, ks, vs, seed=len(name) * 13)
+    out = _run(b, kc, vc, ks, vs)
+    ref = oracle.paged_attention_batch(b, threads=8, kv=(kc, vc, ks, vs))
+    assert_close(as_f64(out), ref, dtype, name)
+
+
+def _uniform_codes(shape, seed):
+    """Codes drawn uniformly over the 254 non-NaN codes (fast at full size)."""
+    c = (W.random_bits16(shape, seed) & 0xFF).astype(np.uint8)
+    c[(c & 0x7F) == 0x7F] ^= 0x01                       # S.1111.111 -> S.1111.110 (+-448)
+    return c
+
+
+def test_attention_on_e4m3_caches_decode13b_full_size():
+    b = W.decode13b(poison=False)
+    ks, vs = 1 / 512, 1 / 256                           # |values| <= 0.875, 1.75
+    kc, vc = _uniform_codes(b.k_cache.shape, 71), _uniform_codes(b.v_cache.shape, 72)
+    out = _run(b, kc, vc, ks, vs)
+    rows = sample_rows(b, 256, seed=3)
+    ref = oracle.paged_attention_batch(b, rows=rows, threads=16, kv=(kc, vc, ks, vs))
+    assert_close(gather_rows(out, b, rows), ref, b.dtype, "decode13b e4m3")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_append_quantises_bit_exact(dtype):
+    b = W.make_attn_batch("fp8app", [20, 3, 45], [5, 2, 17], 4, 2, 128, 16, dtype, seed=19, poison=False)
+    ks, vs = 0.02, 0.5
+    k0 = W.random_bits16(b.k_cache.shape, 4).astype(np.uint8)
+    v0 = W.random_bits16(b.v_cache.shape, 5).astype(np.uint8)
+    kn = W.normal_f32(b.k_new.shape, 6) * 3
+    vn = W.normal_f32(b.v_new.shape, 7) * 300          # some values saturate
+    kn_s, vn_s = W.to_storage(kn, dtype), W.to_storage(vn, dtype)
+    kc, vc = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
+    pkg.kv_append(to_dev(kn_s, dtype), to_dev(vn_s, dtype), to_dev(b.slot_mapping), kc, vc,
+                  k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkg.device_status() == 0
+    ek, ev = oracle.kv_append_e4m3(kn_s, vn_s, b.slot_mapping, k0, v0, b.block_size, ks, vs, dtype)
+    assert np.array_equal(kc.cpu().numpy(), ek)
+    assert np.array_equal(vc.cpu().numpy(), ev)
+
+
+def test_append_then_attend_matches_oracle():
+    """The whole 8-bit step: bf16 new tokens quantised into the caches, then attention over them."""
+    b = W.make_attn_batch("fp8step", [300, 64, 1000], [1, 40, 1], 16, 4, 128, 16, "bf16", seed=23,
+                          poison=False)
+    ks, vs = 1 / 40, 1 / 20
+    k0, v0 = _codes(b.k_cache.shape, ks, 24), _codes(b.v_cache.shape, vs, 25)
+    kc, vc = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
+    pkg.kv_append(to_dev(b.k_new, "bf16"), to_dev(b.v_new, "bf16"), to_dev(b.slot_mapping), kc, vc,
+                  k_scale=ks, v_scale=vs)
+    out = pkg.pa_forward(to_dev(b.q, "bf16"), kc, vc, to_dev(b.block_tables), to_dev(b.ctx_lens),
+                         to_dev(b.q_lens), b.scale, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkg.device_status() == 0
+    ek, ev = oracle.kv_append_e4m3(b.k_new, b.v_new, b.slot_mapping, k0, v0, b.block_size, ks, vs, "bf16")
+    assert np.array_equal(kc.cpu().numpy(), ek) and np.array_equal(vc.cpu().numpy(), ev)
+    ref = oracle.paged_attention_batch(b, threads=8, kv=(ek, ev, ks, vs))
+    assert_close(as_f64(out), ref, "bf16", "append then attend")
