@@ -789,7 +789,7 @@ def run_native(args):
             "config": {"workload": workload_text(name, args),
                        "l2": "inputs larger than L2 (KV pool %.2f GB resident)" % (
                            (step_obj.pool.numel() * step_obj.pool.element_size()) / 1e9),
-                       "decode_tokens_per_s": batch.total_q * world / (attn_ms * 1e-3),
+                       "query_tokens_per_s": batch.total_q * world / (attn_ms * 1e-3),
                        "bytes_per_step": step_bytes, "attn_flops_per_step": step_obj.flops,
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu,
