@@ -285,42 +285,63 @@ __device__ __forceinline__ void finish_split(const SimtParams &p, int seq, int k
     if (before != (uint32_t)(K - 1)) return;
     __threadfence();
     const int64_t part0 = (int64_t)__ldg(p.parts_cu + seq) + ((int64_t)kvh * G + grp) * K;
-    for (int r = 0; r < nrows; ++r) {
-        const float2 ml0 = lane < K ? __ldcg(p.parts_ml + (part0 + lane) * R + r)
-                                    : make_float2(-INFINITY, 0.f);
-        const float2 ml1 = lane + 32 < K ? __ldcg(p.parts_ml + (part0 + lane + 32) * R + r)
+    // lane k (and k + 32) reads split k's (m, l) of every row, then every row's weights and
+    // denominators follow from warp reductions; the rows' o records of one split are read in the
+    // same step, so R loads (times the unroll) are in flight at once
+    float w0[R], w1[R], inv[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const bool ok = r < nrows;
+        const float2 a0 = ok && lane < K ? __ldcg(p.parts_ml + (part0 + lane) * R + r)
                                          : make_float2(-INFINITY, 0.f);
-        const float M = warp_max(fmaxf(ml0.x, ml1.x));
-        const float w0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - M);
-        const float w1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
-        float L = w0 * ml0.y + w1 * ml1.y;
+        const float2 a1 = ok && lane + 32 < K ? __ldcg(p.parts_ml + (part0 + lane + 32) * R + r)
+                                              : make_float2(-INFINITY, 0.f);
+        const float M = warp_max(fmaxf(a0.x, a1.x));
+        w0[r] = a0.x == -INFINITY ? 0.f : exp2f(a0.x - M);
+        w1[r] = a1.x == -INFINITY ? 0.f : exp2f(a1.x - M);
+        float L = w0[r] * a0.y + w1[r] * a1.y;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        float acc[EO];
+        inv[r] = 1.f / L;
+    }
+    float acc[R][EO];
 #pragma unroll
-        for (int e = 0; e < EO; ++e) acc[e] = 0.f;
-        const float *po = p.parts_o + (part0 * R + r) * D + lane * EO;
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int e = 0; e < EO; ++e) acc[r][e] = 0.f;
+    const float *po = p.parts_o + part0 * R * D + lane * EO;
 #pragma unroll 4
-        for (int k = 0; k < K; ++k) {
-            const float w = __shfl_sync(0xffffffffu, k < 32 ? w0 : w1, k & 31);
+    for (int k = 0; k < K; ++k) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float w = __shfl_sync(0xffffffffu, k < 32 ? w0[r] : w1[r], k & 31);
             float x[EO];
-            if constexpr (EO == 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(po + (int64_t)k * R * D));
-                x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+            if (r < nrows) {
+                const float *src = po + ((int64_t)k * R + r) * D;
+                if constexpr (EO == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                    x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                    x[0] = v.x, x[1] = v.y;
+                }
             } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2 *>(po + (int64_t)k * R * D));
-                x[0] = v.x, x[1] = v.y;
+#pragma unroll
+                for (int e = 0; e < EO; ++e) x[e] = 0.f;
             }
 #pragma unroll
-            for (int e = 0; e < EO; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+            for (int e = 0; e < EO; ++e) acc[r][e] = fmaf(w, x[e], acc[r][e]);
         }
-        const float inv = 1.f / L;
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if (r >= nrows) continue;
         const int row = r0 + r;
         const int j = row / p.group, hh = row - j * p.group;
         T *op = reinterpret_cast<T *>(p.out) + ((tok0 + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D +
                 lane * EO;
 #pragma unroll
-        for (int e = 0; e < EO; ++e) op[e] = Elem<T>::from_f(acc[e] * inv);
+        for (int e = 0; e < EO; ++e) op[e] = Elem<T>::from_f(acc[r][e] * inv[r]);
     }
 }
 
@@ -693,25 +714,6 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
         const int nb = (n + B - 1) / B;
         const int cblocks = (nb + K - 1) / K;
 
-        // this lane's quarter of every query row, pre-scaled into log2 units
-        uint64_t q2[R][QD / 2];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float qf[QD];
-            if (r < nrows) {
-                const int row = r0 + r;
-                const int j = row / p.group, hh = row - j * p.group;
-                const T *qp = reinterpret_cast<const T *>(p.q) +
-                              ((tok0 + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D + qd * QD;
-                load_f<T, QD>(qp, qf);
-            } else {
-#pragma unroll
-                for (int e = 0; e < QD; ++e) qf[e] = 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < QD / 2; ++e)
-                q2[r][e] = f2pack(qf[2 * e] * p.scale_log2, qf[2 * e + 1] * p.scale_log2);
-        }
         // causal limit of the row this lane scores (-1: a padding row, every key masked)
         const int Pmine = rrow < nrows ? c + (r0 + rrow) / p.group : -1;
         const int Pmax = c + (r0 + nrows - 1) / p.group;
@@ -769,6 +771,26 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
             finish_split<T, D, R>(p, pend.seq, pend.kvh, pend.grp, pend.G, pend.K, pend.r0, pend.nrows,
                                   pend.tok0, lane);
             pend.on = false;
+        }
+        // the queries are loaded after the merge, which then has their registers for its loads
+        // this lane's quarter of every query row, pre-scaled into log2 units
+        uint64_t q2[R][QD / 2];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float qf[QD];
+            if (r < nrows) {
+                const int row = r0 + r;
+                const int j = row / p.group, hh = row - j * p.group;
+                const T *qp = reinterpret_cast<const T *>(p.q) +
+                              ((tok0 + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D + qd * QD;
+                load_f<T, QD>(qp, qf);
+            } else {
+#pragma unroll
+                for (int e = 0; e < QD; ++e) qf[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < QD / 2; ++e)
+                q2[r][e] = f2pack(qf[2 * e] * p.scale_log2, qf[2 * e + 1] * p.scale_log2);
         }
 
         for (int st = st_lo; st < st_hi; ++st) {
