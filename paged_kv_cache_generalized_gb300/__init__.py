@@ -4,5 +4,6 @@ The work runs in ``libpagedkv.so`` (hand-written CUDA behind a C ABI, ``include/
 this package holds the in-tree build, a thin ctypes binding and the seeded workload generators.
 Calls raise if the library has not been built: there is no CPU fallback.
 """
-from .pagedkv import (PagedKVError, block_copy, device_status, forward_workspace_size,  # noqa: F401
-                      kv_append, library_path, load_library, pa_forward, status_names, version)
+from .pagedkv import (PA_KV_E4M3, PA_KV_SAME, PagedKVError, block_copy, device_status,  # noqa: F401
+                      forward_workspace_size, kv_append, library_path, load_library, pa_forward,
+                      pa_forward_no_alloc, status_names, version)

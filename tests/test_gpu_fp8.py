@@ -118,3 +118,37 @@ def test_append_then_attend_matches_oracle():
     assert np.array_equal(kc.cpu().numpy(), ek) and np.array_equal(vc.cpu().numpy(), ev)
     ref = oracle.paged_attention_batch(b, threads=8, kv=(ek, ev, ks, vs))
     assert_close(as_f64(out), ref, "bf16", "append then attend")
+
+
+def test_append_quantises_every_layer_of_a_pool():
+    """A [L, 2, num_blocks, Hkv, B, d] pool of E4M3 codes: one call quantises every layer's new
+    tokens into that layer's K and V planes (strided views)."""
+    b = W.make_attn_batch("fp8layers", [30, 7], [4, 3], 4, 2, 128, 16, "bf16", seed=29, poison=False)
+    L, ks, vs = 3, 0.05, 0.2
+    pool0 = (W.random_bits16((L, 2) + b.k_cache.shape, 30) & 0xFF).astype(np.uint8)
+    new = [W.to_storage(W.normal_f32((2,) + b.k_new.shape, 31 + l), "bf16") for l in range(L)]
+    pool = torch.from_numpy(pool0).cuda()
+    kn = torch.stack([to_dev(x[0], "bf16") for x in new])
+    vn = torch.stack([to_dev(x[1], "bf16") for x in new])
+    pkg.kv_append(kn, vn, to_dev(b.slot_mapping), pool[:, 0], pool[:, 1], k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkg.device_status() == 0
+    got = pool.cpu().numpy()
+    for l in range(L):
+        ek, ev = oracle.kv_append_e4m3(new[l][0], new[l][1], b.slot_mapping, pool0[l, 0], pool0[l, 1],
+                                       b.block_size, ks, vs, "bf16")
+        assert np.array_equal(got[l, 0], ek) and np.array_equal(got[l, 1], ev), f"layer {l}"
+
+
+def test_no_alloc_entry_point_on_e4m3_caches():
+    b, kc, vc = _fp8_batch("fp8noalloc", [600, 31, 2000], [1, 1, 1], 16, 4, 32, "bf16", 1 / 16, 1 / 16, seed=41)
+    q = to_dev(b.q, "bf16")
+    args = (q, torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(), to_dev(b.block_tables),
+            to_dev(b.ctx_lens), to_dev(b.q_lens), b.scale)
+    a = pkg.pa_forward(*args, k_scale=1 / 16, v_scale=1 / 16)
+    c = pkg.pa_forward_no_alloc(*args, k_scale=1 / 16, v_scale=1 / 16)
+    torch.cuda.synchronize()
+    assert pkg.device_status() == 0
+    assert torch.equal(a, c)
+    ref = oracle.paged_attention_batch(b, threads=8, kv=(kc, vc, 1 / 16, 1 / 16))
+    assert_close(as_f64(c), ref, "bf16", "no-alloc e4m3")
