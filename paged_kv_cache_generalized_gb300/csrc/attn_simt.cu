@@ -531,10 +531,10 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
                 for (int e = 0; e < E / 2; ++e) acc2[r][e] = mul2(acc2[r][e], a2);
                 m[r] = mnew;
             }
-#pragma unroll
-            for (int i = 0; i < kStageTokens / 2; ++i) {
+            // O += p V; slots past the last query's key are never read (only a sequence's last
+            // stage can hold such keys, so full stages skip the test)
+            auto pv_key = [&](int i) {
                 const int key = 2 * i + half;
-                if (p0 + key > Pmax) continue;        // never read slots past the last query
                 uint64_t v2[E / 2];
                 if constexpr (E * sizeof(TK) >= 16 || sizeof(TK) == 1) {
                     load_pairs<TK, E / 2>(sv + key * D + sub * E, v2);
@@ -550,6 +550,14 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
 #pragma unroll
                     for (int e = 0; e < E / 2; ++e) acc2[r][e] = fma2(v2[e], p2, acc2[r][e]);
                 }
+            };
+            if (p0 + kStageTokens - 1 <= Pmax) {
+#pragma unroll
+                for (int i = 0; i < kStageTokens / 2; ++i) pv_key(i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kStageTokens / 2; ++i)
+                    if (p0 + 2 * i + half <= Pmax) pv_key(i);
             }
             __syncwarp();
             ++consumed;
