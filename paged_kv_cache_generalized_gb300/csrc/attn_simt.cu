@@ -781,10 +781,13 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
             pend.on = false;
         }
         // the queries are loaded after the merge, which then has their registers for its loads
-        // this lane's quarter of every query row, pre-scaled into log2 units
+        // this lane's quarter of every query row, pre-scaled into log2 units, in the lane's own row
+        // order: slot sl holds row rrow ^ sl, so the transpose-reduce below keeps slots 0 (and 1)
+        // and sends the others without selecting
         uint64_t q2[R][QD / 2];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
+        for (int sl = 0; sl < R; ++sl) {
+            const int r = rrow ^ sl;
             float qf[QD];
             if (r < nrows) {
                 const int row = r0 + r;
@@ -798,7 +801,7 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
             }
 #pragma unroll
             for (int e = 0; e < QD / 2; ++e)
-                q2[r][e] = f2pack(qf[2 * e] * p.scale_log2, qf[2 * e + 1] * p.scale_log2);
+                q2[sl][e] = f2pack(qf[2 * e] * p.scale_log2, qf[2 * e + 1] * p.scale_log2);
         }
 
         for (int st = st_lo; st < st_hi; ++st) {
@@ -835,19 +838,17 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
                     f2unpack(d2[r], a, b2);
                     d[r] = a + b2;
                 }
+                // d[sl] is row rrow ^ sl.  R = 4: the partner across lane bit 4 (rows rrow ^ 2, ^3)
+                // sends its slots 2, 3 = this lane's rows rrow, rrow ^ 1; across bit 3 the partner
+                // (row rrow ^ 1) sends its slot 1 = row rrow.  R = 2: across bit 4 the other row's
+                // lanes send slot 1 = row rrow; across bit 3 both lanes hold the same row.
                 float s;
                 if constexpr (R == 4) {
-                    const bool b1 = (qd & 2) != 0, b0 = (qd & 1) != 0;
-                    float keep0 = b1 ? d[2] : d[0], keep1 = b1 ? d[3] : d[1];
-                    const float send0 = b1 ? d[0] : d[2], send1 = b1 ? d[1] : d[3];
-                    keep0 += __shfl_xor_sync(0xffffffffu, send0, 16);
-                    keep1 += __shfl_xor_sync(0xffffffffu, send1, 16);
-                    const float keep = b0 ? keep1 : keep0, send = b0 ? keep0 : keep1;
-                    s = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                    const float keep0 = d[0] + __shfl_xor_sync(0xffffffffu, d[2], 16);
+                    const float keep1 = d[1] + __shfl_xor_sync(0xffffffffu, d[3], 16);
+                    s = keep0 + __shfl_xor_sync(0xffffffffu, keep1, 8);
                 } else {
-                    const bool b1 = (qd & 2) != 0;
-                    float keep = b1 ? d[1] : d[0];
-                    keep += __shfl_xor_sync(0xffffffffu, b1 ? d[0] : d[1], 16);
+                    const float keep = d[0] + __shfl_xor_sync(0xffffffffu, d[1], 16);
                     s = keep + __shfl_xor_sync(0xffffffffu, keep, 8);
                 }
                 sc[it] = (p0 + key <= Pmine) ? s : -INFINITY;
