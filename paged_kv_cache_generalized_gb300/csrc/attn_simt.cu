@@ -12,10 +12,13 @@
 //
 // GB300 design: one warp owns one work item (a KV head, up to R query rows of one sequence that
 // share it, and a range of KV blocks).  The warp streams its K/V through a private ring of
-// shared-memory stages filled by bulk asynchronous copies (cp.async.bulk, one 16-token run of a
-// (block, head) per copy, completion on an mbarrier), so each SM keeps ~100+ KB of HBM reads in
-// flight.  Half-warps take alternate keys; each lane holds d/16 dimensions, reductions are
-// warp shuffles.  Work items are taken from a global counter (persistent grid).
+// shared-memory stages filled by asynchronous copies with mbarrier completion, so each SM keeps
+// ~200 KB of HBM reads in flight.  Work items are taken from a global counter (persistent grid).
+// Two kernels: simt_attention_kernel for one query row per KV head (MHA decode; half-warps take
+// alternate keys, each lane holds d/16 dimensions, reductions are warp shuffles, one bulk copy per
+// 16-token run of a (block, head)), and simt_gqa_kernel for 2 or 4 rows (below).  Both read K/V
+// caches of the query's dtype or of one-byte E4M3 codes (the scales fold into the query scale
+// and into o).
 #include <math.h>
 
 #include "common.cuh"
@@ -258,11 +261,6 @@ struct SimtParams {
     int num_seqs, q_heads, kv_heads, group, block_size, max_blocks, nst, bar_bytes;
 };
 
-// Called by a whole warp after it wrote the partial records (m, l, o) of its split of row group
-// (seq, kvh, grp).  The last of the group's K splits to get here merges the K records of every
-// row with the logsumexp rule, out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k,
-// M = max_k m_k, and writes the output rows; the others return at once.  Each writer fences its
-// records before it counts itself in; the merger fences after it and reads through L2.
 // A split whose partial records are written but not yet counted in: a warp counts itself in (and
 // merges, if it is the group's last) only after it has issued the first copies of its next item,
 // so that the merge's latency overlaps them.
@@ -272,6 +270,11 @@ struct PendingSplit {
     bool on;
 };
 
+// Called by a whole warp after it wrote the partial records (m, l, o) of its split of row group
+// (seq, kvh, grp).  The last of the group's K splits to get here merges the K records of every
+// row with the logsumexp rule, out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k,
+// M = max_k m_k, and writes the output rows; the others return at once.  Each writer fences its
+// records before it counts itself in; the merger fences after it and reads through L2.
 template <typename T, int D, int R>
 __device__ __forceinline__ void finish_split(const SimtParams &p, int seq, int kvh, int grp, int G, int K,
                                              int r0, int nrows, int64_t tok0, int lane) {
