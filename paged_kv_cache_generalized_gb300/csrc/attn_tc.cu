@@ -16,6 +16,9 @@
 // The MMA warp interleaves the two tiles -- PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) -- so the tensor
 // cores work on one tile while the other tile's softmax runs.  The running max is only moved (and
 // O_t rescaled in tensor memory) when it grows by more than 2^8; the final O / l is exact anyway.
+// A lone tile (odd tile count per KV head) with 4 or more KV tiles runs its key range as two
+// halves in the pair's two slots (both from the one Q tile, each half with its own K/V loads),
+// merged in the epilogue by the logsumexp rule, so that it too overlaps softmax with the MMAs.
 //
 // Warp roles (352 threads, one CTA per SM, persistent; items claimed from a global counter):
 //   warp 0      TMA producer for Q (both tiles, once per item) and K: per 128-key tile one 3-D
@@ -61,13 +64,18 @@ constexpr int kSmQ = 0;                          // two Q tiles
 constexpr int kSmK = kSmQ + 2 * kTile;
 constexpr int kSmV = kSmK + kKStages * kTile;
 constexpr int kSmBar = kSmV + kVStages * kTile;
-constexpr int kSmBytes = kSmBar + 256 + 1024;    // barriers, tensor-memory slot, alignment slack
+constexpr int kSmMerge = kSmBar + 256;           // (m, l) of a split tile's second half, per row
+constexpr int kSmBytes = kSmMerge + kRows * 8 + 64 + 1024;   // + split counters, alignment slack
+// A lone query tile (no partner tile in its sequence and KV head) with at least this many KV
+// tiles is split: the two halves of its key range run as the pair's two tiles and are merged
+// in the epilogue, so its softmax overlaps the tensor cores as a pair's does.
+constexpr int kSplitMinTiles = 4;
 
 enum Bar {
     kKFull0 = 0, kKEmpty0 = kKFull0 + kKStages, kVFull0 = kKEmpty0 + kKStages,
     kVEmpty0 = kVFull0 + kVStages, kSFull0 = kVEmpty0 + kVStages, kPFull0 = kSFull0 + 2,
     kOReady0 = kPFull0 + 2, kQFull = kOReady0 + 2, kQEmpty, kDrain, kItemFull0, kItemEmpty0 = kItemFull0 + 2,
-    kNumBars = kItemEmpty0 + 2
+    kMerge = kItemEmpty0 + 2, kMergeDone, kNumBars
 };
 // Items are claimed by the K producer and handed to the other ten warps through a two-slot ring.
 constexpr int kItemConsumers = 2 + 8;
@@ -234,11 +242,15 @@ struct TcParams {
 
 // One work item: query tiles qt0 = 2*pi and qt1 = 2*pi + 1 (if it exists) of one (sequence,
 // KV head).  Tile 1 holds later rows, so its causal range (and KV tile count) covers tile 0's.
+// A split item is one query tile whose key range runs in two halves, KV tiles [0, h) in slot 0
+// and [h, nt) in slot 1 (kt0 = first KV tile of each slot), both slots using query tile 0.
 struct Item {
-    int seq, kvh, ntiles;         // ntiles: KV tiles of the pair (those of its last tile)
+    int seq, kvh, ntiles;         // ntiles: MMA steps (KV tiles of the longer slot)
+    int nload;                    // K (and V) tiles loaded for the item
     int64_t tok0;
     bool two;                     // tile 1 exists
-    int j0[2], rows_valid[2], nt[2];
+    bool split;                   // a lone tile run as two halves of its key range
+    int j0[2], rows_valid[2], nt[2], kt0[2];
     int64_t pmin[2], pmax[2];
 };
 
@@ -264,8 +276,25 @@ __device__ __forceinline__ Item decode_item(const TcParams &p, int it) {
         t.pmax[u] = c + t.j0[u] + (t.rows_valid[u] - 1) / p.group;
         t.nt[u] = (int)((t.pmax[u] + kKeys) / kKeys);
     }
-    t.ntiles = t.two ? t.nt[1] : t.nt[0];
+    t.split = !t.two && t.nt[0] >= kSplitMinTiles;
+    t.kt0[0] = t.kt0[1] = 0;
+    if (t.split) {
+        const int h = t.nt[0] / 2;
+        t.kt0[1] = h;
+        t.nt[1] = t.nt[0] - h;
+        t.nt[0] = h;
+    }
+    t.ntiles = t.two || t.split ? t.nt[1] : t.nt[0];
+    t.nload = t.split ? t.nt[0] + t.nt[1] : t.ntiles;
     return t;
+}
+
+// KV tile of an item's ld-th K/V load.  A split item interleaves its halves: load 2i + u is
+// slot u's i-th tile while both slots run, then slot 1's remaining tiles follow in order.
+__device__ __forceinline__ int load_tile(const Item &t, int ld) {
+    if (!t.split) return ld;
+    const int c0 = t.nt[0];
+    return ld < 2 * c0 ? ((ld & 1) ? c0 + (ld >> 1) : (ld >> 1)) : ld;
 }
 
 // Physical block of each lane's block in KV tile kt (lanes < blocks of the tile), clamped.
@@ -283,6 +312,64 @@ __device__ __forceinline__ int tile_block(const TcParams &p, const int32_t *bt_r
         }
     }
     return phys;
+}
+
+// Epilogue of a split tile (a lone query tile whose key range ran as two halves, one per slot).
+// The slot-1 warp hands its rows' (m, l) to the slot-0 warp of the same tensor-memory lanes and
+// waits until that warp has read its O; the slot-0 warp merges the halves with the logsumexp
+// rule, out = (2^(m0-M) O_0 + 2^(m1-M) O_1) / (2^(m0-M) l_0 + 2^(m1-M) l_1), M = max(m0, m1)
+// (both finite: every row sees keys in both halves), and writes the row (orow, if stored).
+// Returns false if a wait timed out.  Not inlined, so that the softmax loop's registers are
+// allocated without it.
+template <typename T>
+__device__ __noinline__ bool split_epilogue(int u, uint64_t *bars, float2 *merge_ml, uint32_t *nsplit, int row,
+                                            int lane, uint32_t lane_base, float m, float l, T *orow) {
+    const uint32_t ns = *nsplit;
+    if (u == 1) {
+        merge_ml[row] = make_float2(m, l);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kMerge]);
+        const bool merged = warp_wait(&bars[kMergeDone], ns & 1);
+        if (lane == 0) *nsplit = ns + 1;
+        __syncwarp();
+        tc_fence_after();
+        return merged;
+    }
+    if (!warp_wait(&bars[kMerge], ns & 1)) return false;
+    if (lane == 0) *nsplit = ns + 1;
+    __syncwarp();
+    tc_fence_after();
+    const float2 ml1 = merge_ml[row];
+    const float M = fmaxf(m, ml1.x);
+    const float w0 = fast_exp2(m - M), w1 = fast_exp2(ml1.x - M);
+    const float inv = 1.f / (w0 * l + w1 * ml1.y);
+    const float a0 = w0 * inv, a1 = w1 * inv;
+#pragma unroll 1
+    for (int c = 0; c < kDim / 32; ++c) {
+        uint32_t r0[32], r1[32];
+        tmem_load32(lane_base + tmem_o(0) + c * 32, r0);
+        tmem_load32(lane_base + tmem_o(1) + c * 32, r1);
+        if (orow) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float x[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    x[i] = a0 * __uint_as_float(r0[q4 * 8 + i]) + a1 * __uint_as_float(r1[q4 * 8 + i]);
+                uint4 v;
+                v.x = pack2<T>(x[0], x[1]);
+                v.y = pack2<T>(x[2], x[3]);
+                v.z = pack2<T>(x[4], x[5]);
+                v.w = pack2<T>(x[6], x[7]);
+                *reinterpret_cast<uint4 *>(orow + c * 32 + q4 * 8) = v;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kMergeDone]);
+    return true;
 }
 
 template <typename T>
@@ -305,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t count = 1;
             if (b == kPFull0 || b == kPFull0 + 1) count = 4;
             if (b == kItemEmpty0 || b == kItemEmpty0 + 1) count = kItemConsumers;
+            if (b == kMerge || b == kMergeDone) count = 4;
             mbar_init(&bars[b], count);
         }
         mbar_fence_init();
@@ -382,10 +470,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t pmax = t.two ? t.pmax[1] : t.pmax[0];
             const int32_t *bt_row = p.bt + (int64_t)t.seq * p.max_blocks;
             int nblk_next = 0;
-            int phys_next = tile_block(p, bt_row, pmax, 0, bpt, lane, nblk_next);
-            for (int kt = 0; kt < t.ntiles; ++kt, ++iter) {
+            int phys_next = tile_block(p, bt_row, pmax, load_tile(t, 0), bpt, lane, nblk_next);
+            for (int ld = 0; ld < t.nload; ++ld, ++iter) {
                 const int phys = phys_next, nblk = nblk_next;
-                if (kt + 1 < t.ntiles) phys_next = tile_block(p, bt_row, pmax, kt + 1, bpt, lane, nblk_next);
+                if (ld + 1 < t.nload)
+                    phys_next = tile_block(p, bt_row, pmax, load_tile(t, ld + 1), bpt, lane, nblk_next);
                 const int s = iter % nst;
                 const uint32_t use = iter / nst;
                 if (use > 0 && !warp_wait(&bars[empty0 + s], (use - 1) & 1)) { ok = false; break; }
@@ -425,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // field (address / 16, below 2^14 for any shared-memory address).
             const uint64_t dq = smem_desc(q_base, 16, 1024), dk = smem_desc(k_base, 16, 1024),
                            dv = smem_desc(v_base, kPanel, 1024);
-            auto issue_s = [&](int u, uint32_t g) {   // S_u = Q_u K(g)^T
-                const uint64_t a = dq + (uint64_t)(u * (kTile >> 4)),
+            auto issue_s_from = [&](int u, uint32_t g, int qs) {   // S_u = Q_qs K(g)^T
+                const uint64_t a = dq + (uint64_t)(qs * (kTile >> 4)),
                                b = dk + (uint64_t)((g % kKStages) * (kTile >> 4));
                 const uint32_t d = tmem + tmem_s(u);
 #pragma unroll
@@ -454,6 +543,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(&bars[kOReady0 + u]);
                 return true;
             };
+            // V rows [first, 16 * ceil(first / 16)) of stage vs (free or stale slots past the last
+            // key, possibly NaN) are zeroed so that P = 0 times them stays 0; returns the 16-key
+            // steps that hold keys
+            auto zero_tail = [&](int vs, int64_t valid) -> int {
+                if (valid >= kKeys) return kKeys / 16;
+                const int ksteps = (int)((valid + 15) / 16);
+                const int first = (int)valid, end = ksteps * 16;
+                unsigned char *vb = smem + kSmV + vs * kTile;
+                for (int r = first; r < end; ++r)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        *reinterpret_cast<uint4 *>(vb + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(vb + kPanel + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                fence_proxy_async_smem();
+                return ksteps;
+            };
             for (uint32_t n = 0; ok; ++n, ++items) {
                 const int slot = n & 1;
                 if (!mbar_wait(&bars[kItemFull0 + slot], (n >> 1) & 1)) { ok = false; break; }
@@ -462,9 +568,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it < 0) break;
                 const Item t = decode_item(p, it);
                 if (!wait_bar(kQFull, items & 1)) { ok = false; break; }
+                if (t.split) {
+                    // Slot u runs its own KV tiles against Q slot 0, in the order PV_0(i), S_0(i+1),
+                    // PV_1(i), S_1(i+1) of a pair; every S and PV has its own K or V load (load
+                    // position ld(u, i) of the item), released as soon as it is done.
+                    const int c0 = t.nt[0], c1 = t.nt[1];
+                    auto ld = [&](int u, int i) -> uint32_t { return iter + (uint32_t)(i < c0 ? 2 * i + u : c0 + i); };
+                    for (int u = 0; u < 2 && ok; ++u) {
+                        if (!wait_k(ld(u, 0))) { ok = false; break; }
+                        issue_s_from(u, ld(u, 0), 0);
+                        umma_commit(&bars[kKEmpty0 + ld(u, 0) % kKStages]);
+                    }
+                    for (int i = 0; i < c1 && ok; ++i) {
+                        for (int u = 0; u < 2; ++u) {
+                            const int cnt = u ? c1 : c0;
+                            if (i >= cnt) continue;
+                            const uint32_t g = ld(u, i);
+                            const int vs = g % kVStages;
+                            if (!wait_bar(kVFull0 + vs, (g / kVStages) & 1)) { ok = false; break; }
+                            const int ksteps = (u == 1 && i == c1 - 1)
+                                                   ? zero_tail(vs, t.pmax[0] + 1 - (int64_t)(t.kt0[1] + i) * kKeys)
+                                                   : kKeys / 16;
+                            if (!issue_pv(u, g, i == 0, ksteps)) { ok = false; break; }
+                            umma_commit(&bars[kVEmpty0 + vs]);
+                            if (i + 1 < cnt) {
+                                if (!wait_k(ld(u, i + 1))) { ok = false; break; }
+                                issue_s_from(u, ld(u, i + 1), 0);
+                                umma_commit(&bars[kKEmpty0 + ld(u, i + 1) % kKStages]);
+                            }
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(&bars[kQEmpty]);
+                    iter += t.nload;
+                    continue;
+                }
                 if (!wait_k(iter)) { ok = false; break; }
-                issue_s(0, iter);
-                if (t.two) issue_s(1, iter);
+                issue_s_from(0, iter, 0);
+                if (t.two) issue_s_from(1, iter, 1);
                 umma_commit(&bars[kKEmpty0 + iter % kKStages]);
                 for (int kt = 0; kt < t.ntiles; ++kt) {
                     const uint32_t g = iter + kt;
@@ -492,12 +633,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (act0 && !issue_pv(0, g, kt == 0, ksteps)) { ok = false; break; }
                     if (!last) {
                         if (!wait_k(g + 1)) { ok = false; break; }
-                        if (kt + 1 < t.nt[0]) issue_s(0, g + 1);
+                        if (kt + 1 < t.nt[0]) issue_s_from(0, g + 1, 0);
                     }
                     if (t.two && !issue_pv(1, g, kt == 0, ksteps)) { ok = false; break; }
                     umma_commit(&bars[kVEmpty0 + vs]);
                     if (!last) {
-                        if (t.two) issue_s(1, g + 1);
+                        if (t.two) issue_s_from(1, g + 1, 1);
                         umma_commit(&bars[kKEmpty0 + (g + 1) % kKStages]);
                     }
                 }
@@ -519,6 +660,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const uint32_t s_tmem = lane_base + tmem_s(u), o_tmem = lane_base + tmem_o(u);
         const float c_log2 = p.scale_log2;            // > 0 (other scales use CUDA cores)
+        uint32_t *nsplit = reinterpret_cast<uint32_t *>(smem + kSmMerge + kRows * 8) + warp;  // split items so far
+        if (lane == 0) *nsplit = 0;
+        __syncwarp();
         uint32_t scount = 0;                           // S / PV tiles of this query tile so far
         bool ok = true;
         for (uint32_t n = 0; ok; ++n) {
@@ -526,14 +670,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it == -2) { ok = false; break; }
             if (it < 0) break;
             const Item t = decode_item(p, it);
-            if (u == 1 && !t.two) continue;
+            if (u == 1 && !t.two && !t.split) continue;
             const int64_t pmin = t.pmin[u], pmax = t.pmax[u];
-            const int nt = t.nt[u];
+            const int kt_end = t.kt0[u] + t.nt[u];
             const int j = t.j0[u] + row / p.group, hh = row % p.group;
             int64_t prow = pmin + row / p.group;
             if (prow > pmax) prow = pmax;               // padding rows: finite, never stored
             float m = -INFINITY, l = 0.f;
-            for (int kt = 0; kt < nt; ++kt, ++scount) {
+            for (int kt = t.kt0[u]; kt < kt_end; ++kt, ++scount) {
                 if (!warp_wait(&bars[kSFull0 + u], scount & 1)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t raw[kKeys];
@@ -587,7 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // tensor-memory loads/stores are warp-collective: the whole warp rescales when any
                 // of its rows must (alpha = 1 for the others), after the previous PV is complete
-                if (kt > 0 && __any_sync(0xffffffffu, rescale)) {
+                // (l > 0 after the slot's first tile: every row sees a key there)
+                if (l > 0.f && __any_sync(0xffffffffu, rescale)) {
                     if (!warp_wait(&bars[kOReady0 + u], (scount - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
                     const float alpha = rescale ? fast_exp2(m - muse) : 1.f;
@@ -613,10 +758,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // epilogue: O / l -> out, after this tile's last PV
             if (!warp_wait(&bars[kOReady0 + u], (scount - 1) & 1)) { ok = false; break; }
             tc_fence_after();
-            const float inv = 1.f / l;
             const bool store = row < t.rows_valid[u];
             T *orow = reinterpret_cast<T *>(p.out) +
                       ((t.tok0 + j) * p.q_heads + (int64_t)t.kvh * p.group + hh) * kDim;
+            if (t.split) {
+                if (!split_epilogue<T>(u, bars, reinterpret_cast<float2 *>(smem + kSmMerge), nsplit, row, lane,
+                                       lane_base, m, l, store ? orow : nullptr)) {
+                    ok = false;
+                    break;
+                }
+                continue;
+            }
+            const float inv = 1.f / l;
 #pragma unroll 1
             for (int c = 0; c < kDim / 32; ++c) {
                 uint32_t r[32];
