@@ -18,7 +18,9 @@
 // alternate keys, each lane holds d/16 dimensions, reductions are warp shuffles, one bulk copy per
 // 16-token run of a (block, head)), and simt_gqa_kernel for 2 or 4 rows (below).  Both read K/V
 // caches of the query's dtype or of one-byte E4M3 codes (the scales fold into the query scale
-// and into o).
+// and into o).  On E4M3 caches the one-row kernel converts the codes to f16 pairs in hardware and
+// feeds them, with an f16 copy of the query (scaled by a power of two) or of P, to mixed-precision
+// FMAs with fp32 accumulators: no f16 -> fp32 widening per element.
 #include <math.h>
 
 #include "common.cuh"
@@ -351,6 +353,10 @@ __device__ __forceinline__ void finish_split(const SimtParams &p, int seq, int k
 template <typename T, typename TK, int D, int R>
 __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(SimtParams p) {
     constexpr int E = D / 16;                       // dims per lane
+    // E4M3 caches: codes become f16 pairs in hardware and meet the query (as f16) in
+    // mixed-precision FMAs with fp32 accumulators; no f16 -> fp32 conversion per element
+    constexpr bool kE4 = sizeof(TK) == 1;
+    static_assert(!kE4 || E == 8, "E4M3 caches: head_dim 128");
     constexpr uint32_t kRunBytes = kStageTokens * D * sizeof(TK);
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -420,6 +426,26 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
         for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int e = 0; e < E / 2; ++e) q2[r][e] = f2pack(qf[r][2 * e], qf[r][2 * e + 1]);
+        // E4M3 caches: each query row as f16 pairs, scaled by the power of two that puts its
+        // largest component in [2^14, 2^15) (far from f16 overflow and underflow); qmul undoes it
+        uint32_t qh[R][E / 2];
+        float qmul[R];
+        if constexpr (kE4) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float mx = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) mx = fmaxf(mx, fabsf(qf[r][e]));
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                int ex = ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14;
+                ex = max(-100, min(100, ex));
+                const float down = __int_as_float((127 - ex) << 23);
+                qmul[r] = __int_as_float((127 + ex) << 23);
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) qh[r][e] = h2_from_f32(qf[r][2 * e] * down, qf[r][2 * e + 1] * down);
+            }
+        }
         const int64_t Pmax = (int64_t)c + (r0 + nrows - 1) / p.group;
         const int64_t nb_lim = (Pmax + B) / B;                  // blocks holding keys 0..Pmax
         const int64_t st_lo = (int64_t)chunk * cblocks * spb;
@@ -489,6 +515,25 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
 #pragma unroll
             for (int i = 0; i < kStageTokens / 2; ++i) {
                 const int key = 2 * i + half;
+                if constexpr (kE4) {
+                    const uint2 kw = *reinterpret_cast<const uint2 *>(sk + key * D + sub * E);
+                    uint32_t kh[4];
+                    e4m3x4_to_h2(kw.x, kh[0], kh[1]);
+                    e4m3x4_to_h2(kw.y, kh[2], kh[3]);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) fma_h2(qh[r][e], kh[e], d0, d1);
+                        float dot = d0 + d1;
+                        dot += __shfl_xor_sync(0xffffffffu, dot, 8);
+                        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+                        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                        s[r][i] = (p0 + key <= Pr[r]) ? dot * qmul[r] : -INFINITY;
+                    }
+                    continue;
+                }
                 uint64_t k2[E / 2];
                 if constexpr (E * sizeof(TK) >= 16 || sizeof(TK) == 1) {
                     load_pairs<TK, E / 2>(sk + key * D + sub * E, k2);
@@ -538,6 +583,24 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32) simt_attention_kernel(Simt
             // stage can hold such keys, so full stages skip the test)
             auto pv_key = [&](int i) {
                 const int key = 2 * i + half;
+                if constexpr (kE4) {
+                    const uint2 vw = *reinterpret_cast<const uint2 *>(sv + key * D + sub * E);
+                    uint32_t vh[4];
+                    e4m3x4_to_h2(vw.x, vh[0], vh[1]);
+                    e4m3x4_to_h2(vw.y, vh[2], vh[3]);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint16_t ph = f16_from_f32(s[r][i]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float a, b;
+                            f2unpack(acc2[r][e], a, b);
+                            fma_h2s(vh[e], ph, a, b);
+                            acc2[r][e] = f2pack(a, b);
+                        }
+                    }
+                    return;
+                }
                 uint64_t v2[E / 2];
                 if constexpr (E * sizeof(TK) >= 16 || sizeof(TK) == 1) {
                     load_pairs<TK, E / 2>(sv + key * D + sub * E, v2);

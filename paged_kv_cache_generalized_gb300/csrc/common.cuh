@@ -165,6 +165,41 @@ __device__ __forceinline__ void widen4_e4m3(uint32_t w, uint64_t &p01, uint64_t 
         : "r"(w));
 }
 
+// Four E4M3 codes (bytes 0..3 of w) -> two f16 pairs (elements 0, 1 and 2, 3), exactly.
+__device__ __forceinline__ void e4m3x4_to_h2(uint32_t w, uint32_t &h01, uint32_t &h23) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h01), "=r"(h23)
+        : "r"(w));
+}
+
+// Mixed-precision FMAs with f16 operands and fp32 accumulators (products of f16 values are exact
+// in fp32, so each step rounds once): d0 += a.lo * b.lo and d1 += a.hi * b.hi.
+__device__ __forceinline__ void fma_h2(uint32_t a, uint32_t b, float &d0, float &d1) {
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\tfma.rn.f32.f16 %1, a1, b1, %1;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "r"(a), "r"(b));
+}
+// d0 += a.lo * s and d1 += a.hi * s for an f16 scalar s.
+__device__ __forceinline__ void fma_h2s(uint32_t a, uint16_t s, float &d0, float &d1) {
+    asm("{\n\t.reg .b16 a0, a1;\n\tmov.b32 {a0, a1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, %3, %0;\n\tfma.rn.f32.f16 %1, a1, %3, %1;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "r"(a), "h"(s));
+}
+// fp32 -> f16 (round to nearest even) and two fp32 -> one f16 pair (a in the low half).
+__device__ __forceinline__ uint16_t f16_from_f32(float a) {
+    uint16_t r;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(a));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2_from_f32(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
 // Two fp32 values -> two E4M3 codes (a in the low byte), rounded to nearest even with the
 // magnitude saturated at 448.
 __device__ __forceinline__ uint16_t e4m3x2_from_f32(float a, float b) {
