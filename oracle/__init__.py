@@ -26,6 +26,9 @@ CUDA library; the only thing both sides use is the seeded input generator module
   format follows its published definition (1 sign, 4 exponent bits with bias 7, 3 fraction bits,
   no infinities, S.1111.111 = NaN); encoding rounds to nearest, ties to an even code, and
   saturates at +-448.
+* ``oracle.kitty`` -- 2-bit pages with promoted 4-bit key channels ("KVキャッシュ管理の教科書"
+  第22章, Kitty): the page quantiser, the record's bytes, and decode attention on the dequantised
+  pages plus the unquantised residual page (float64, through ``paged_attention``).
 * ``kv_bytes_per_token`` / ``kv_elements`` -- sizing formulas: the Pensieve page, section
   "KVキャッシュのメモリ管理" (M_kv = L x H x 2 x b), and "KVキャッシュ管理の教科書" 第3章
   (2 x batch x layers x seq x head_dim x heads elements).
@@ -45,7 +48,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lib = None
 
-DTYPE_CODES = {"f32": 0, "bf16": 1, "f16": 2, "e4m3": 3}
+DTYPE_CODES = {"f32": 0, "bf16": 1, "f16": 2, "e4m3": 3, "f64": 4}
 
 
 def build(force: bool = False) -> str:

@@ -35,6 +35,9 @@
  *   shrink the cache) and 第22章 (quantising KV before decoding).  Reading taken here: K and V
  *   hold FP8 E4M3 codes and one scale each; a cached element's value is code value x scale, and
  *   attention is the same function of those values.
+ *
+ *   float64 caches hold values that are not float32 numbers (the dequantised 2-bit pages of the
+ *   Kitty row, "KVキャッシュ管理の教科書" 第22章); attention is again the same function.
  */
 #include <math.h>
 #include <stdint.h>
@@ -45,7 +48,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2, ORACLE_E4M3 = 3 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2, ORACLE_E4M3 = 3, ORACLE_F64 = 4 };
 
 /* IEEE-754 binary16 -> double, from the format's definition (1 sign, 5 exponent, 10 fraction
  * bits, bias 15); every binary16 value is exactly representable in double. */
@@ -96,6 +99,7 @@ static double element(const void *base, int dtype, int64_t idx)
     case ORACLE_F32: return (double)((const float *)base)[idx];
     case ORACLE_BF16: return bf16_to_double(((const uint16_t *)base)[idx]);
     case ORACLE_E4M3: return e4m3_to_double(((const uint8_t *)base)[idx]);
+    case ORACLE_F64: return ((const double *)base)[idx];
     default: return half_to_double(((const uint16_t *)base)[idx]);
     }
 }
