@@ -238,6 +238,86 @@ pa_status block_copy(const block_copy_dims *dims, const void *src, void *dst,
                      const int64_t *pairs, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * 2-bit paged KV cache with promoted 4-bit key channels ("KVキャッシュ管理の教科書", 第22章, on
+ * Kitty; 第3章 names fewer bits per element as the third way to shrink the cache).
+ *
+ * What the chapter fixes: K and V at 2 bits per element; the key channels whose mean magnitude
+ * along the token direction is in the top 12.5-25 % promoted to 4 bits; a dense tensor of every
+ * channel's low 2 bits plus a sparse tensor of only the promoted channels' high 2 bits; one
+ * quantisation group of 128 tokens, which is one page of the paged cache, quantised once per 128
+ * decode steps.  Readings taken for what it leaves open:
+ *   - asymmetric min/max quantisation: K per channel over the page's 128 tokens, V per token over
+ *     the head's d channels; code(x) = round-half-even((x - min) / s) clamped to [0, L] with
+ *     s = (max - min) / L, L = 3, or 15 on a promoted key channel; s = 0 codes every element 0;
+ *     a cached element's value is code * s + min (promoted key code = low + 4 * high);
+ *   - the decisions that produce integers are taken in float32: the subtraction, the division and
+ *     the magnitude sum (|k| added over the page's tokens in token order) round to nearest;
+ *   - the P promoted channels are those with the largest magnitude sums, ties going to the lower
+ *     channel index; P = 16 (12.5 %) or 32 (25 %) of d = 128;
+ *   - a sequence of n tokens has floor(n / 128) quantised pages; its last n % 128 tokens stay in a
+ *     residual page of the query's dtype (an ordinary 128-token cache block, written by kv_append
+ *     with block_size 128) until it fills and kv_quantize_pages turns it into a quantised page.
+ *
+ * Record of one (page, KV head): pa_kitty_record_bytes(128, P) = 10272 + 32 P bytes (10784 or
+ * 11296; 2.76 bits per cached element at P = 32), little-endian, at these byte offsets:
+ *   [0, 512)          K scale s_x, float32, channel x = 0..127
+ *   [512, 1024)       K minimum, float32 per channel
+ *   [1024, 1536)      V scale, float32 per token t = 0..127
+ *   [1536, 2048)      V minimum, float32 per token
+ *   [2048, 2080)      promoted channel ids, uint8, ascending in slots 0..P-1, later slots 0
+ *   [2080, 6176)      K low 2 bits: token t, channel x at byte 2080 + 32 t + x / 4, bits 2 (x % 4)
+ *   [6176, 6176+32P)  K high 2 bits of promoted slot k: byte 6176 + (P/4) t + k / 4, bits 2 (k % 4)
+ *   [6176+32P, +4096) V codes: token t, channel x at byte 32 t + x / 4, bits 2 (x % 4)
+ * A page pool is [num_pages, Hkv, record] (record-major, 16-byte aligned); residual pools are
+ * [num_res_pages, Hkv, 128, 128] of `dtype`.
+ * ---------------------------------------------------------------------------------------- */
+#define PA_KITTY_PAGE_TOKENS 128
+
+typedef struct {
+    int32_t dtype;              /* PA_BF16 or PA_F16: q, out and the residual pages */
+    int32_t num_seqs;           /* >= 1; q and out are [num_seqs, Hq, d] (decode: q_len = 1) */
+    int32_t num_q_heads;        /* Hq */
+    int32_t num_kv_heads;       /* Hkv, divides Hq */
+    int32_t head_dim;           /* d = 128 */
+    int32_t promoted;           /* P = 16 or 32 */
+    int64_t num_pages;          /* records in the page pool (per KV head) */
+    int64_t num_res_pages;      /* blocks in the residual pools */
+    int32_t max_pages_per_seq;  /* row length of block_tables */
+} pa_kitty_dims;
+
+/* Bytes of one (page, KV head) record, or 0 for an unsupported (head_dim, promoted). */
+size_t pa_kitty_record_bytes(int32_t head_dim, int32_t promoted);
+
+/* kv_quantize_pages: for every pair (s, t) = (pairs[2k], pairs[2k+1]) and every KV head h,
+ * quantise the 128 tokens of residual page s (res_k / res_v [s][h]) into record t of `pages`, by
+ * the rules above (bit-exact: same bytes on every run).  pairs is int64 device memory; ids
+ * outside [0, num_res_pages) / [0, num_pages) are skipped and flagged PA_DEV_BAD_PAIR.
+ * Destinations must be distinct.  Non-finite inputs give unspecified records. */
+pa_status kv_quantize_pages(const pa_kitty_dims *dims, const void *res_k, const void *res_v,
+                            const int64_t *pairs, int64_t num_pairs, void *pages,
+                            pa_stream_t stream);
+
+size_t pa_kitty_workspace_size(const pa_kitty_dims *dims);
+
+/* pa_forward_kitty: decode attention (q_len = 1 for every sequence) over quantised pages.
+ * Sequence i has n_i = ctx_lens[i] + 1 tokens, the new token's K/V already written (into its
+ * residual page, or quantised with it when it filled the page).  block_tables[i][p] for
+ * p < floor(n_i / 128) is a record id in `pages`; when n_i % 128 > 0, block_tables[i][floor(n_i /
+ * 128)] is a residual page id in res_k / res_v.  For query head h (KV head h / g):
+ *     out[i, h, :] = sum_{p < n_i} softmax_p(scale * q[i, h, :] . K_i[p]) V_i[p]
+ * with K_i[p], V_i[p] the dequantised values (or the residual page's values).  Arithmetic: the
+ * dot products take the query times each channel's scale rounded to f16 and the codes exactly,
+ * with fp32 accumulation; P times the V scale is rounded to f16 in the weighted V sum.
+ * Workspace: pa_kitty_workspace_size(dims) bytes, 256-byte aligned, contents clobbered.
+ * q_lens[i] != 1, ctx_lens[i] < 0 or n_i > max_pages_per_seq * 128 -> that sequence's rows are
+ * not written, PA_DEV_BAD_LENGTHS; a page or residual id outside its pool -> that page is
+ * skipped, PA_DEV_BAD_BLOCK_ID.  num_seqs <= 8192. */
+pa_status pa_forward_kitty(const pa_kitty_dims *dims, const void *q, const void *pages,
+                           const void *res_k, const void *res_v, const int32_t *block_tables,
+                           const int32_t *ctx_lens, const int32_t *q_lens, float scale, void *out,
+                           void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * pa_get_device_status: synchronise `stream`, return the current device's status bits
  * (PA_DEV_*) accumulated since the last call in *flags, and clear them.  Returns PA_ERR_DEVICE
  * when any bit was set, PA_ERR_CUDA when the synchronisation failed, else PA_OK.

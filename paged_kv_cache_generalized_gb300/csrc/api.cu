@@ -16,6 +16,8 @@ __device__ unsigned g_device_status;
 
 constexpr int kMaxDevices = 64;
 
+}  // namespace
+
 // The status word's device address for the current device (looked up once per device; host
 // code must not use the symbol itself as an address).
 unsigned *status_ptr() {
@@ -41,6 +43,8 @@ int sm_count() {
     }
     return cache[dev];
 }
+
+namespace {
 
 // A high-priority stream per device on which a call's tensor-core kernel runs beside its CUDA-core
 // kernel, with the events that fork it from and join it back to the caller's stream.  Created on

@@ -188,6 +188,13 @@ __device__ __forceinline__ void fma_h2s(uint32_t a, uint16_t s, float &d0, float
         : "+f"(d0), "+f"(d1)
         : "r"(a), "h"(s));
 }
+// The same with bf16 operands: d0 += a.lo * b.lo and d1 += a.hi * b.hi (products exact in fp32).
+__device__ __forceinline__ void fma_bf2(uint32_t a, uint32_t b, float &d0, float &d1) {
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %1, a1, b1, %1;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "r"(a), "r"(b));
+}
 // fp32 -> f16 (round to nearest even) and two fp32 -> one f16 pair (a in the low half).
 __device__ __forceinline__ uint16_t f16_from_f32(float a) {
     uint16_t r;

@@ -103,6 +103,10 @@ bool tensor_maps_available();
 bool make_map_3d(CUtensorMap *map, int dtype, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                  uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
 
+// The current device's status word (device address) and SM count; nullptr / 0 on failure.
+unsigned *status_ptr();
+int sm_count();
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
 

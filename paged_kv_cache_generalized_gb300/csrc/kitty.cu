@@ -1,0 +1,839 @@
+// 2-bit paged KV cache with promoted 4-bit key channels ("KVキャッシュ管理の教科書", 第22章, on
+// Kitty): the page quantiser and decode attention over quantised pages.  The record format and
+// the readings taken where the chapter leaves a step open are in include/pagedkv.h.
+//
+// kitty_quantize_kernel: one CTA of 128 threads per (pair, KV head).  K pass: thread x owns
+// channel x -- float32 magnitude sum over the tokens in order, min, max; the promoted set is the
+// P channels of largest sum (rank by comparison with every other channel, ties to the lower id);
+// codes by float32 subtract, divide and round-half-even; 16 channels' low bits meet in one word
+// through shuffles, high bits through shared-memory ORs.  V pass: one warp per token, a lane per
+// 4 channels, min/max by shuffles.
+//
+// kitty_decode_kernel: persistent, 8 warps per CTA, one CTA per SM.  Phase 1 streams the
+// quantised pages: a work item is (sequence, query head, up to kChunkPages pages); each warp runs
+// a 2-stage ring of whole (page, KV head) records filled by bulk copies with mbarrier completion,
+// and claims its next item while the current one computes, so the ring runs across items.  Per
+// page the warp folds each channel's scale into the query (a_x = scale * q_x * s_x, and
+// b = scale * sum_x q_x min_x), so a key's score is b + sum_x a_x code_x.  The codes are never
+// unpacked: masking a 2-bit field of a 32-bit word in place leaves, in each 16-bit half, an f16
+// subnormal equal to code * 2^(2j - 24) (j = the field's position in the half), which a
+// mixed-precision FMA multiplies by a_x pre-scaled by 2^-2j as f16 -- one AND per two codes and one
+// FMA per code, fp32 accumulators.  One lane per key for QK^T; for PV a lane owns 16 channels
+// of every fourth key, and P * s_t (rounded to f16) meets the V codes the same way; the V minimum
+// contributes sum_t p_t min_t.  Phase 2 runs each sequence's residual page (fewer than 128
+// unquantised tokens) as one more item with plain loads.  Items of one row merge by the
+// logsumexp rule: the last split to finish reads the others' (m, l, o) records through L2.
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kPageTokens = 128;
+constexpr int kDim = 128;
+constexpr int kOffKs = 0, kOffKm = 512, kOffVs = 1024, kOffVm = 1536, kOffPid = 2048, kOffKlo = 2080;
+constexpr int kOffKhi = kOffKlo + 32 * kPageTokens;               // 6176
+constexpr int kChunkPages = 4;                                    // pages per decode work item
+constexpr int kDecWarps = 8;
+constexpr int kStages = 2;
+constexpr int kPartFloats = 132;                                  // m, l, 2 pad, o[128]
+constexpr int kMaxSeqs = 8192;
+constexpr int kScratchBytes = 512 + 64 * 4 + 16 * 4;              // a_x fp32, f16 pairs lo, hi
+
+__host__ __device__ constexpr int record_bytes(int P) { return 10272 + 32 * P; }
+__host__ __device__ constexpr int off_vc(int P) { return kOffKhi + 32 * P; }
+
+// ---- quantiser ---------------------------------------------------------------------------------
+struct QuantParams {
+    const void *res_k, *res_v;
+    const int64_t *pairs;
+    uint8_t *pages;
+    int64_t num_pairs, num_pages, num_res;
+    int kv_heads;
+    unsigned *status;
+};
+
+template <typename T, int P>
+__global__ void __launch_bounds__(128) kitty_quantize_kernel(QuantParams p) {
+    constexpr int kHiWords = P / 16;                 // 32-bit words of high bits per token
+    __shared__ float s_mag[kDim];
+    __shared__ int s_cnt[4];
+    __shared__ uint32_t s_hi[kPageTokens * kHiWords];
+    const int x = threadIdx.x, lane = x & 31, warp = x >> 5;
+    const int64_t pair = blockIdx.x;
+    const int h = blockIdx.y;
+    const int64_t src = p.pairs[2 * pair], dst = p.pairs[2 * pair + 1];
+    if (src < 0 || src >= p.num_res || dst < 0 || dst >= p.num_pages) {
+        if (x == 0) report(p.status, PA_DEV_BAD_PAIR);
+        return;
+    }
+    const size_t plane = (size_t)kPageTokens * kDim;
+    const T *rk = reinterpret_cast<const T *>(p.res_k) + ((size_t)src * p.kv_heads + h) * plane;
+    const T *rv = reinterpret_cast<const T *>(p.res_v) + ((size_t)src * p.kv_heads + h) * plane;
+    uint8_t *rec = p.pages + ((size_t)dst * p.kv_heads + h) * record_bytes(P);
+    for (int i = x; i < kPageTokens * kHiWords; i += 128) s_hi[i] = 0u;
+
+    // K pass 1: channel x's magnitude sum (tokens in order), minimum and maximum, in float32
+    float mag = 0.f, mn = INFINITY, mx = -INFINITY;
+    for (int t = 0; t < kPageTokens; ++t) {
+        const float v = Elem<T>::to_f(rk[t * kDim + x]);
+        mag = __fadd_rn(mag, fabsf(v));
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+    }
+    s_mag[x] = mag;
+    __syncthreads();
+    int rank = 0;
+    for (int y = 0; y < kDim; ++y) {
+        const float my = s_mag[y];
+        rank += (my > mag) || (my == mag && y < x);
+    }
+    const bool prom = rank < P;
+    const unsigned ball = __ballot_sync(0xffffffffu, prom);
+    if (lane == 0) s_cnt[warp] = __popc(ball);
+    __syncthreads();
+    int slot = __popc(ball & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) slot += s_cnt[w];
+    const float L = prom ? 15.f : 3.f;
+    const float s = __fdiv_rn(__fsub_rn(mx, mn), L);
+    reinterpret_cast<float *>(rec + kOffKs)[x] = s;
+    reinterpret_cast<float *>(rec + kOffKm)[x] = mn;
+    if (prom) rec[kOffPid + slot] = (uint8_t)x;
+    if (x >= P && x < 32) rec[kOffPid + x] = 0;
+
+    // K pass 2: codes; 16 channels' low bits form one word of the dense tensor
+    for (int t = 0; t < kPageTokens; ++t) {
+        const float v = Elem<T>::to_f(rk[t * kDim + x]);
+        uint32_t c = 0;
+        if (s != 0.f) c = (uint32_t)fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v, mn), s)), 0.f), L);
+        uint32_t w = (c & 3u) << (2 * (x & 15));
+        w |= __shfl_xor_sync(0xffffffffu, w, 1);
+        w |= __shfl_xor_sync(0xffffffffu, w, 2);
+        w |= __shfl_xor_sync(0xffffffffu, w, 4);
+        w |= __shfl_xor_sync(0xffffffffu, w, 8);
+        if ((x & 15) == 0) reinterpret_cast<uint32_t *>(rec + kOffKlo + t * 32)[x >> 4] = w;
+        if (prom) atomicOr(&s_hi[t * kHiWords + (slot >> 4)], (c >> 2) << (2 * (slot & 15)));
+    }
+    __syncthreads();
+    for (int i = x; i < kPageTokens * kHiWords; i += 128)
+        reinterpret_cast<uint32_t *>(rec + kOffKhi)[i] = s_hi[i];
+
+    // V: one warp per token, lane l owns channels 4l..4l+3
+    for (int t = warp; t < kPageTokens; t += 4) {
+        float v[4];
+        load_f<T, 4>(rv + t * kDim + 4 * lane, v);
+        float lo = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
+        float hi = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        const float sv = __fdiv_rn(__fsub_rn(hi, lo), 3.f);
+        uint32_t b = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            uint32_t c = 0;
+            if (sv != 0.f) c = (uint32_t)fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[e], lo), sv)), 0.f), 3.f);
+            b |= c << (2 * e);
+        }
+        uint32_t w = b << (8 * (lane & 3));
+        w |= __shfl_xor_sync(0xffffffffu, w, 1);
+        w |= __shfl_xor_sync(0xffffffffu, w, 2);
+        if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(rec + off_vc(P) + t * 32)[lane >> 2] = w;
+        if (lane == 0) {
+            reinterpret_cast<float *>(rec + kOffVs)[t] = sv;
+            reinterpret_cast<float *>(rec + kOffVm)[t] = lo;
+        }
+    }
+}
+
+// ---- decode attention ----------------------------------------------------------------------
+struct DecParams {
+    const void *q;
+    const uint8_t *pages;
+    const void *res_k, *res_v;
+    const int32_t *bt, *ctx, *qlen;
+    void *out;
+    float scale_log2;                  // scale * log2(e): scores in log2 units
+    int num_seqs, q_heads, kv_heads, group, max_pages, max_chunks;
+    int64_t num_pages, num_res;
+    uint32_t *counters;                // [0] next quantised item, [1] next residual item
+    uint32_t *arrive;                  // [num_seqs * q_heads] splits finished per row
+    float *parts;                      // [rows * max_chunks * kPartFloats] split records
+    unsigned *status;
+};
+
+__device__ __forceinline__ float wsum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// 2^e for e in [-126, 127].
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// The binary exponent of a positive finite float (its value in [2^e, 2^(e+1))), or -127 for 0
+// and subnormals.
+__device__ __forceinline__ int exponent_of(float a) { return ((__float_as_int(a) >> 23) & 0xff) - 127; }
+
+// Tokens of sequence s (cached + the new one), or -1 when its lengths are invalid.
+__device__ __forceinline__ int seq_tokens(const DecParams &p, int s) {
+    const int c = __ldg(p.ctx + s), ql = __ldg(p.qlen + s);
+    if (ql != 1 || c < 0 || (int64_t)c + 1 > (int64_t)p.max_pages * kPageTokens) return -1;
+    return c + 1;
+}
+
+__device__ __forceinline__ int quant_chunks(int n) {
+    return n <= 0 ? 0 : (n / kPageTokens + kChunkPages - 1) / kChunkPages;
+}
+
+struct Item {
+    int seq, h, kvh, k, p0, p1, nch;
+    bool valid;
+};
+
+// Claims the next quantised-page item: items are numbered sequence by sequence (prefix s_cu),
+// within a sequence head-major, so the chunks of one row are claimed back to back.
+__device__ __forceinline__ Item claim_quant(const DecParams &p, const int *s_cu, int lane) {
+    Item it;
+    it.valid = false;
+    uint32_t i = 0;
+    if (lane == 0) i = atomicAdd(p.counters, 1u);
+    i = __shfl_sync(0xffffffffu, i, 0);
+    if (i >= (uint32_t)s_cu[p.num_seqs]) return it;
+    int lo = 0, hi = p.num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((uint32_t)s_cu[mid] <= i) lo = mid;
+        else hi = mid - 1;
+    }
+    const int n = seq_tokens(p, lo);
+    const int nq = quant_chunks(n);
+    const int w = (int)i - s_cu[lo];
+    it.seq = lo;
+    it.h = w / nq;
+    it.k = w - it.h * nq;
+    it.kvh = it.h / p.group;
+    it.p0 = it.k * kChunkPages;
+    it.p1 = min(it.p0 + kChunkPages, n / kPageTokens);
+    it.nch = nq + (n % kPageTokens != 0);
+    it.valid = true;
+    return it;
+}
+
+// Called by a whole warp after it wrote split k's record of `row`.  The last of the row's nch
+// splits to arrive merges them, out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k, and writes
+// the output row (lane l: channels 4l..4l+3).
+template <typename T>
+__device__ void merge_row(const DecParams &p, int row, int nch, int lane) {
+    __threadfence();
+    __syncwarp();
+    uint32_t before = 0;
+    if (lane == 0) before = atomicAdd(p.arrive + row, 1u);
+    before = __shfl_sync(0xffffffffu, before, 0);
+    if (before != (uint32_t)(nch - 1)) return;
+    __threadfence();
+    const float *base = p.parts + (size_t)row * p.max_chunks * kPartFloats;
+    float M = -INFINITY;
+    for (int k = lane; k < nch; k += 32) M = fmaxf(M, __ldcg(base + (size_t)k * kPartFloats));
+    M = warp_max(M);
+    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int k = 0; k < nch; ++k) {
+        const float *r = base + (size_t)k * kPartFloats;
+        const float m = __ldcg(r), l = __ldcg(r + 1);
+        const float4 o = __ldcg(reinterpret_cast<const float4 *>(r + 4) + lane);
+        const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+        L = fmaf(w, l, L);
+        acc[0] = fmaf(w, o.x, acc[0]);
+        acc[1] = fmaf(w, o.y, acc[1]);
+        acc[2] = fmaf(w, o.z, acc[2]);
+        acc[3] = fmaf(w, o.w, acc[3]);
+    }
+    const float inv = 1.f / L;
+    float v[4] = {acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv};
+    store_f<T, 4>(reinterpret_cast<T *>(p.out) + (size_t)row * kDim + 4 * lane, v);
+}
+
+// Mixed-precision FMA on a pair of 16-bit elements of the query's type.
+template <typename T> __device__ __forceinline__ void fma_pair(uint32_t a, uint32_t b, float &d0, float &d1);
+template <> __device__ __forceinline__ void fma_pair<__nv_bfloat16>(uint32_t a, uint32_t b, float &d0, float &d1) {
+    fma_bf2(a, b, d0, d1);
+}
+template <> __device__ __forceinline__ void fma_pair<__half>(uint32_t a, uint32_t b, float &d0, float &d1) {
+    fma_h2(a, b, d0, d1);
+}
+
+// Shared memory of the decode kernel: per warp kStages records and a scratch area, the ring's
+// mbarriers, then the per-sequence item prefix.
+__host__ __device__ constexpr size_t dec_smem_bytes(int P, int num_seqs) {
+    return (size_t)kDecWarps * (kStages * record_bytes(P) + kScratchBytes) + kDecWarps * kStages * 8 +
+           (size_t)(num_seqs + 1) * 4;
+}
+
+template <typename T, int P>
+__global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecParams p) {
+    constexpr int REC = record_bytes(P);
+    constexpr int kHiPairs = P / 2;                   // f16 pairs of promoted slots
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_part[kDecWarps * 32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned char *ring = smem + (size_t)warp * kStages * REC;
+    unsigned char *scratch = smem + (size_t)kDecWarps * kStages * REC + warp * kScratchBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kDecWarps * (kStages * REC + kScratchBytes)) +
+                     warp * kStages;
+    int *s_cu = reinterpret_cast<int *>(smem + (size_t)kDecWarps * (kStages * REC + kScratchBytes) +
+                                        kDecWarps * kStages * 8);
+    float *s_a = reinterpret_cast<float *>(scratch);                       // a_x, fp32
+    uint16_t *s_lo = reinterpret_cast<uint16_t *>(scratch + 512);          // 64 f16 pairs
+    uint16_t *s_hi = reinterpret_cast<uint16_t *>(scratch + 512 + 256);    // 16 f16 pairs
+
+    // item prefix over sequences: sequence s has quant_chunks(n_s) * q_heads quantised items
+    {
+        const int S = p.num_seqs;
+        const int per = (S + kDecWarps * 32 - 1) / (kDecWarps * 32);
+        const int lo = min(S, tid * per), hi = min(S, lo + per);
+        int sum = 0;
+        for (int s = lo; s < hi; ++s) {
+            const int n = seq_tokens(p, s);
+            if (n < 0 && blockIdx.x == 0) report(p.status, PA_DEV_BAD_LENGTHS);
+            sum += quant_chunks(n) * p.q_heads;
+        }
+        s_part[tid] = sum;
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+            mbar_fence_init();
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int v[kDecWarps], t = 0;
+#pragma unroll
+            for (int i = 0; i < kDecWarps; ++i) {
+                v[i] = s_part[lane * kDecWarps + i];
+                t += v[i];
+            }
+            int incl = t;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            int run = incl - t;
+#pragma unroll
+            for (int i = 0; i < kDecWarps; ++i) {
+                s_part[lane * kDecWarps + i] = run;
+                run += v[i];
+            }
+            if (lane == 31) s_cu[S] = run;
+        }
+        __syncthreads();
+        int run = s_part[tid];
+        for (int s = lo; s < hi; ++s) {
+            s_cu[s] = run;
+            run += quant_chunks(seq_tokens(p, s)) * p.q_heads;
+        }
+        __syncthreads();
+    }
+
+    // ---- phase 1: quantised pages ----
+    Item cur = claim_quant(p, s_cu, lane), nxt;
+    nxt.valid = false;
+    bool have_nxt = false, iss_nxt = false, dead = false;
+    int iss_pg = cur.p0;
+    uint32_t issued = 0, done = 0;
+
+    auto page_id = [&](const Item &it, int pg) -> int64_t {
+        const int32_t id = __ldg(p.bt + (int64_t)it.seq * p.max_pages + pg);
+        return (id < 0 || id >= p.num_pages) ? -1 : id;
+    };
+    // Issues the copy of the next page (of the current item, else of the next one, which it
+    // claims when needed); false when there is nothing to issue.
+    auto issue = [&]() -> bool {
+        if (!cur.valid) return false;
+        if (iss_pg >= (iss_nxt ? nxt.p1 : cur.p1)) {
+            if (iss_nxt) return false;
+            if (!have_nxt) {
+                nxt = claim_quant(p, s_cu, lane);
+                have_nxt = true;
+            }
+            if (!nxt.valid) return false;
+            iss_nxt = true;
+            iss_pg = nxt.p0;
+        }
+        const Item &it = iss_nxt ? nxt : cur;
+        int64_t id = page_id(it, iss_pg);
+        if (id < 0) id = 0;      // a bad id still fills the stage (the ring stays in step); compute skips it
+        const int slot = issued % kStages;
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[slot], REC);
+            bulk_g2s(ring + slot * REC, p.pages + ((size_t)id * p.kv_heads + it.kvh) * REC, REC, &bars[slot]);
+        }
+        ++issued;
+        ++iss_pg;
+        return true;
+    };
+
+    while (issued - done < kStages && issue()) {
+    }
+    while (cur.valid) {
+        const int row = cur.seq * p.q_heads + cur.h;
+        float qs[4];
+        load_f<T, 4>(reinterpret_cast<const T *>(p.q) + (size_t)row * kDim + 4 * lane, qs);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qs[e] *= p.scale_log2;
+        float m_run = -INFINITY, l_l = 0.f, bv_l = 0.f;
+        float o[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = 0.f;
+        int F_cur = 0;
+        bool have_F = false;
+
+        for (int pg = cur.p0; pg < cur.p1; ++pg) {
+            const int slot = done % kStages;
+            if (!mbar_wait(&bars[slot], (done / kStages) & 1u)) {
+                report(p.status, PA_DEV_TIMEOUT);
+                dead = true;
+                break;
+            }
+            const unsigned char *st = ring + slot * REC;
+            if (page_id(cur, pg) < 0) {
+                if (lane == 0) report(p.status, PA_DEV_BAD_BLOCK_ID);
+            } else {
+                // page prologue: a_x = scale q_x s_x, b = scale sum_x q_x min_x; f16 pairs of a_x
+                // scaled by 2^(E - 2 (x % 4)), E putting max |a| in [2^12, 2^13)
+                const float4 ks = reinterpret_cast<const float4 *>(st + kOffKs)[lane];
+                const float4 km = reinterpret_cast<const float4 *>(st + kOffKm)[lane];
+                const float a[4] = {qs[0] * ks.x, qs[1] * ks.y, qs[2] * ks.z, qs[3] * ks.w};
+                const float b = wsum(qs[0] * km.x + qs[1] * km.y + qs[2] * km.z + qs[3] * km.w);
+                const float amax = warp_max(fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3]))));
+                const int E = amax > 0.f ? max(-100, min(100, 12 - exponent_of(amax))) : 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int x = 4 * lane + e;
+                    s_a[x] = a[e];
+                    s_lo[((x >> 4) * 8 + (x & 7)) * 2 + ((x >> 3) & 1)] = f16_from_f32(a[e] * pow2f(E - 2 * e));
+                }
+                __syncwarp();
+                if (lane < P) {
+                    const int x = st[kOffPid + lane];
+                    s_hi[((lane >> 4) * 8 + (lane & 7)) * 2 + ((lane >> 3) & 1)] =
+                        f16_from_f32(4.f * s_a[x] * pow2f(E - 2 * (lane & 3)));
+                }
+                __syncwarp();
+                uint32_t alo[64], ahi[kHiPairs];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const uint4 w = reinterpret_cast<const uint4 *>(s_lo)[i];
+                    alo[4 * i] = w.x, alo[4 * i + 1] = w.y, alo[4 * i + 2] = w.z, alo[4 * i + 3] = w.w;
+                }
+#pragma unroll
+                for (int i = 0; i < kHiPairs / 4; ++i) {
+                    const uint4 w = reinterpret_cast<const uint4 *>(s_hi)[i];
+                    ahi[4 * i] = w.x, ahi[4 * i + 1] = w.y, ahi[4 * i + 2] = w.z, ahi[4 * i + 3] = w.w;
+                }
+                const float zmul = pow2f(24 - E);
+                // V: F puts the largest token scale in [2^14, 2^15); o is kept in units of 2^F
+                const float4 vs4 = reinterpret_cast<const float4 *>(st + kOffVs)[lane];
+                const float vmax = warp_max(fmaxf(fmaxf(vs4.x, vs4.y), fmaxf(vs4.z, vs4.w)));
+                const int F = vmax > 0.f ? max(-60, min(60, 14 - exponent_of(vmax))) : 0;
+                if (!have_F) {
+                    F_cur = F;
+                    have_F = true;
+                } else if (F != F_cur) {
+                    const float r = pow2f(F - F_cur);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[i] *= r;
+                    F_cur = F;
+                }
+                const float psc = pow2f(F_cur);
+                const int u = lane >> 3, wv = lane & 7;
+
+#pragma unroll 1
+                for (int pass = 0; pass < kPageTokens / 32; ++pass) {
+                    const int t = pass * 32 + lane;
+                    // QK^T, one key per lane
+                    const uint4 *kl = reinterpret_cast<const uint4 *>(st + kOffKlo + t * 32);
+                    const uint4 w0 = kl[0], w1 = kl[1];
+                    const uint32_t kw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                    uint32_t hw[P / 16];
+                    if constexpr (P == 32) {
+                        const uint2 h2 = *reinterpret_cast<const uint2 *>(st + kOffKhi + t * 8);
+                        hw[0] = h2.x;
+                        hw[1] = h2.y;
+                    } else {
+                        hw[0] = *reinterpret_cast<const uint32_t *>(st + kOffKhi + t * 4);
+                    }
+                    float acc[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll
+                    for (int wd = 0; wd < 8; ++wd) {
+                        const uint32_t x = kw[wd], y = x >> 8;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            fma_h2(alo[wd * 8 + j], x & (0x00030003u << (2 * j)), acc[2 * j], acc[2 * j + 1]);
+                            fma_h2(alo[wd * 8 + 4 + j], y & (0x00030003u << (2 * j)), acc[8 + 2 * j], acc[9 + 2 * j]);
+                        }
+                    }
+#pragma unroll
+                    for (int wd = 0; wd < P / 16; ++wd) {
+                        const uint32_t x = hw[wd], y = x >> 8;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            fma_h2(ahi[wd * 8 + j], x & (0x00030003u << (2 * j)), acc[2 * j], acc[2 * j + 1]);
+                            fma_h2(ahi[wd * 8 + 4 + j], y & (0x00030003u << (2 * j)), acc[8 + 2 * j], acc[9 + 2 * j]);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 8; i > 0; i >>= 1)
+#pragma unroll
+                        for (int k = 0; k < i; ++k) acc[k] += acc[k + i];
+                    const float z = fmaf(acc[0], zmul, b);
+                    // online softmax
+                    const float mloc = warp_max(z);
+                    if (mloc > m_run) {
+                        const float al = fast_exp2(m_run - mloc);
+                        l_l *= al;
+                        bv_l *= al;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] *= al;
+                        m_run = mloc;
+                    }
+                    const float pz = fast_exp2(z - m_run);
+                    l_l += pz;
+                    bv_l = fmaf(pz, reinterpret_cast<const float *>(st + kOffVm)[t], bv_l);
+                    const uint32_t ph = f16_from_f32(pz * reinterpret_cast<const float *>(st + kOffVs)[t] * psc);
+                    // PV: lane (u, wv) takes word wv (channels 16 wv .. 16 wv + 15) of keys 4 i + u
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int tok = 4 * i + u;
+                        const uint16_t pt = (uint16_t)__shfl_sync(0xffffffffu, ph, tok);
+                        const uint32_t x = *reinterpret_cast<const uint32_t *>(st + off_vc(P) + (pass * 32 + tok) * 32 + wv * 4);
+                        const uint32_t y = x >> 8;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            fma_h2s(x & (0x00030003u << (2 * j)), pt, o[2 * j], o[2 * j + 1]);
+                            fma_h2s(y & (0x00030003u << (2 * j)), pt, o[8 + 2 * j], o[9 + 2 * j]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            ++done;
+            issue();
+        }
+        if (dead) break;
+
+        // item epilogue: o[2 jj + h] holds channel 16 wv + jj + 8 h in units of 2^(2 (jj % 4) - 24 + F)
+        const float l = wsum(l_l), bv = wsum(bv_l);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            o[i] += __shfl_xor_sync(0xffffffffu, o[i], 8);
+            o[i] += __shfl_xor_sync(0xffffffffu, o[i], 16);
+        }
+        float res[16];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const float f = pow2f(24 - 2 * (jj & 3) - F_cur);
+            res[jj] = fmaf(o[2 * jj], f, bv);
+            res[jj + 8] = fmaf(o[2 * jj + 1], f, bv);
+        }
+        if (cur.nch == 1) {
+            if (lane < 8) {
+                const float inv = 1.f / l;
+                float v0[8], v1[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v0[i] = res[i] * inv, v1[i] = res[8 + i] * inv;
+                T *dst = reinterpret_cast<T *>(p.out) + (size_t)row * kDim + 16 * lane;
+                store_f<T, 8>(dst, v0);
+                store_f<T, 8>(dst + 8, v1);
+            }
+        } else {
+            float *rec = p.parts + ((size_t)row * p.max_chunks + cur.k) * kPartFloats;
+            if (lane < 8) {
+                float4 *dst = reinterpret_cast<float4 *>(rec + 4 + 16 * lane);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dst[i] = make_float4(res[4 * i], res[4 * i + 1], res[4 * i + 2], res[4 * i + 3]);
+            }
+            if (lane == 0) {
+                rec[0] = m_run;
+                rec[1] = l;
+            }
+            merge_row<T>(p, row, cur.nch, lane);
+        }
+
+        // next item (claimed already if the ring ran ahead into it)
+        if (!have_nxt) {
+            nxt = claim_quant(p, s_cu, lane);
+            have_nxt = true;
+        }
+        cur = nxt;
+        have_nxt = false;
+        if (iss_nxt) iss_nxt = false;
+        else iss_pg = cur.p0;
+        while (issued - done < kStages && issue()) {
+        }
+    }
+    if (dead) {
+        // drain this warp's copies in flight (bounded) and stop
+        for (; done < issued; ++done) mbar_wait(&bars[done % kStages], (done / kStages) & 1u);
+        return;
+    }
+
+    // ---- phase 2: residual pages (the last n % 128 tokens of each sequence, unquantised) ----
+    const uint32_t rows = (uint32_t)p.num_seqs * p.q_heads;
+    while (true) {
+        uint32_t j = 0;
+        if (lane == 0) j = atomicAdd(p.counters + 1, 1u);
+        j = __shfl_sync(0xffffffffu, j, 0);
+        if (j >= rows) break;
+        const int seq = j / p.q_heads, h = j - seq * p.q_heads;
+        const int n = seq_tokens(p, seq);
+        if (n < 0 || n % kPageTokens == 0) continue;
+        const int nt = n % kPageTokens, nfull = n / kPageTokens;
+        const int nch = quant_chunks(n) + 1;
+        const int32_t rid = __ldg(p.bt + (int64_t)seq * p.max_pages + nfull);
+        float m_run = -INFINITY, l_l = 0.f;
+        uint64_t o2[2] = {0ull, 0ull};               // channels 4 lane .. 4 lane + 3
+        if (rid < 0 || rid >= p.num_res) {
+            if (lane == 0) report(p.status, PA_DEV_BAD_BLOCK_ID);
+        } else {
+            const size_t plane = (size_t)kPageTokens * kDim;
+            const T *rk = reinterpret_cast<const T *>(p.res_k) + ((size_t)rid * p.kv_heads + h / p.group) * plane;
+            const T *rv = reinterpret_cast<const T *>(p.res_v) + ((size_t)rid * p.kv_heads + h / p.group) * plane;
+            uint32_t qp[64];
+            const uint4 *qsrc = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + (size_t)j * kDim);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint4 w = __ldg(qsrc + i);
+                qp[4 * i] = w.x, qp[4 * i + 1] = w.y, qp[4 * i + 2] = w.z, qp[4 * i + 3] = w.w;
+            }
+            for (int t0 = 0; t0 < nt; t0 += 32) {
+                const int t = t0 + lane;
+                float z = -INFINITY;
+                if (t < nt) {
+                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    const uint4 *kr = reinterpret_cast<const uint4 *>(rk + (size_t)t * kDim);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint4 w = __ldg(kr + i);
+                        fma_pair<T>(qp[4 * i], w.x, acc[0], acc[1]);
+                        fma_pair<T>(qp[4 * i + 1], w.y, acc[2], acc[3]);
+                        fma_pair<T>(qp[4 * i + 2], w.z, acc[4], acc[5]);
+                        fma_pair<T>(qp[4 * i + 3], w.w, acc[6], acc[7]);
+                    }
+                    z = (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]))) * p.scale_log2;
+                }
+                const float mloc = warp_max(z);
+                if (mloc > m_run) {
+                    const float al = fast_exp2(m_run - mloc);
+                    l_l *= al;
+                    const uint64_t al2 = f2pack(al, al);
+                    o2[0] = mul2(o2[0], al2);
+                    o2[1] = mul2(o2[1], al2);
+                    m_run = mloc;
+                }
+                const float pz = t < nt ? fast_exp2(z - m_run) : 0.f;
+                l_l += pz;
+                const int cnt = min(32, nt - t0);
+                const T *vb = rv + (size_t)t0 * kDim + 4 * lane;
+#pragma unroll 4
+                for (int k = 0; k < cnt; ++k) {
+                    const float pk = __shfl_sync(0xffffffffu, pz, k);
+                    const uint2 w = __ldg(reinterpret_cast<const uint2 *>(vb + (size_t)k * kDim));
+                    const uint64_t pk2 = f2pack(pk, pk);
+                    o2[0] = fma2(widen2<T>(w.x), pk2, o2[0]);
+                    o2[1] = fma2(widen2<T>(w.y), pk2, o2[1]);
+                }
+            }
+        }
+        const float l = wsum(l_l);
+        float res[4];
+        f2unpack(o2[0], res[0], res[1]);
+        f2unpack(o2[1], res[2], res[3]);
+        if (nch == 1) {
+            if (rid >= 0 && rid < p.num_res) {
+                const float inv = 1.f / l;
+                float v[4] = {res[0] * inv, res[1] * inv, res[2] * inv, res[3] * inv};
+                store_f<T, 4>(reinterpret_cast<T *>(p.out) + (size_t)j * kDim + 4 * lane, v);
+            }
+        } else {
+            float *rec = p.parts + ((size_t)j * p.max_chunks + (nch - 1)) * kPartFloats;
+            reinterpret_cast<float4 *>(rec + 4)[lane] = make_float4(res[0], res[1], res[2], res[3]);
+            if (lane == 0) {
+                rec[0] = m_run;
+                rec[1] = l;
+            }
+            merge_row<T>(p, (int)j, nch, lane);
+        }
+    }
+}
+
+// ---- launchers ---------------------------------------------------------------------------------
+constexpr int kMaxDevs = 64;
+
+template <typename T, int P>
+cudaError_t launch_decode_t(const DecParams &d, int num_sms, cudaStream_t s) {
+    static bool configured[kMaxDevs];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevs) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(kitty_decode_kernel<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)dec_smem_bytes(P, kMaxSeqs));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    kitty_decode_kernel<T, P><<<num_sms, kDecWarps * 32, dec_smem_bytes(P, d.num_seqs), s>>>(d);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_decode(const DecParams &d, int P, int num_sms, cudaStream_t s) {
+    return P == 16 ? launch_decode_t<T, 16>(d, num_sms, s) : launch_decode_t<T, 32>(d, num_sms, s);
+}
+
+template <typename T>
+cudaError_t launch_quantize(const QuantParams &q, int P, cudaStream_t s) {
+    const dim3 grid((unsigned)q.num_pairs, (unsigned)q.kv_heads);
+    if (P == 16) kitty_quantize_kernel<T, 16><<<grid, 128, 0, s>>>(q);
+    else kitty_quantize_kernel<T, 32><<<grid, 128, 0, s>>>(q);
+    return cudaGetLastError();
+}
+
+bool is_aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+pa_status check_kitty_dims(const pa_kitty_dims *d) {
+    if (!d) return PA_ERR_INVALID_ARG;
+    if (d->dtype != PA_BF16 && d->dtype != PA_F16) return d->dtype == PA_F32 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
+    if (d->num_seqs < 1 || d->num_q_heads < 1 || d->num_kv_heads < 1 || d->max_pages_per_seq < 1)
+        return PA_ERR_INVALID_ARG;
+    if (d->num_q_heads % d->num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (d->num_pages < 0 || d->num_res_pages < 0) return PA_ERR_INVALID_ARG;
+    if (d->head_dim != kDim || (d->promoted != 16 && d->promoted != 32)) return PA_ERR_UNSUPPORTED;
+    if (d->num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)d->num_seqs * d->num_q_heads;
+    const int64_t chunks = ((int64_t)d->max_pages_per_seq + kChunkPages - 1) / kChunkPages + 1;
+    if (rows * chunks >= ((int64_t)1 << 31)) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+struct KittyWs {
+    size_t arrive, parts, zero_bytes, total;
+    int max_chunks;
+};
+
+KittyWs kitty_ws(const pa_kitty_dims &d) {
+    KittyWs w;
+    const size_t rows = (size_t)d.num_seqs * d.num_q_heads;
+    w.max_chunks = (d.max_pages_per_seq + kChunkPages - 1) / kChunkPages + 1;
+    w.arrive = 256;
+    w.parts = w.arrive + align_up(rows * 4, 256);
+    w.zero_bytes = w.parts;
+    w.total = w.parts + rows * w.max_chunks * kPartFloats * sizeof(float);
+    return w;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+size_t pa_kitty_record_bytes(int32_t head_dim, int32_t promoted) {
+    if (head_dim != kDim || (promoted != 16 && promoted != 32)) return 0;
+    return (size_t)record_bytes(promoted);
+}
+
+size_t pa_kitty_workspace_size(const pa_kitty_dims *dims) {
+    if (check_kitty_dims(dims) != PA_OK) return 0;
+    return kitty_ws(*dims).total;
+}
+
+pa_status kv_quantize_pages(const pa_kitty_dims *dims, const void *res_k, const void *res_v,
+                            const int64_t *pairs, int64_t num_pairs, void *pages, pa_stream_t stream) {
+    const pa_status st = check_kitty_dims(dims);
+    if (st != PA_OK) return st;
+    if (num_pairs < 0 || num_pairs > 0x7fffffff) return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!res_k || !res_v || !pairs || !pages) return PA_ERR_INVALID_ARG;
+    if (!is_aligned(res_k, 16) || !is_aligned(res_v, 16) || !is_aligned(pages, 16) || !is_aligned(pairs, 8))
+        return PA_ERR_INVALID_ARG;
+    QuantParams q;
+    q.res_k = res_k;
+    q.res_v = res_v;
+    q.pairs = pairs;
+    q.pages = static_cast<uint8_t *>(pages);
+    q.num_pairs = num_pairs;
+    q.num_pages = dims->num_pages;
+    q.num_res = dims->num_res_pages;
+    q.kv_heads = dims->num_kv_heads;
+    q.status = status_ptr();
+    if (!q.status) return PA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = dims->dtype == PA_BF16 ? launch_quantize<__nv_bfloat16>(q, dims->promoted, s)
+                                                 : launch_quantize<__half>(q, dims->promoted, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_forward_kitty(const pa_kitty_dims *dims, const void *q, const void *pages,
+                           const void *res_k, const void *res_v, const int32_t *block_tables,
+                           const int32_t *ctx_lens, const int32_t *q_lens, float scale, void *out,
+                           void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+    const pa_status st = check_kitty_dims(dims);
+    if (st != PA_OK) return st;
+    const pa_kitty_dims &d = *dims;
+    if (!q || !pages || !res_k || !res_v || !block_tables || !ctx_lens || !q_lens || !out)
+        return PA_ERR_INVALID_ARG;
+    if (!is_aligned(q, 16) || !is_aligned(out, 16) || !is_aligned(pages, 16) || !is_aligned(res_k, 16) ||
+        !is_aligned(res_v, 16))
+        return PA_ERR_INVALID_ARG;
+    if (!is_aligned(block_tables, 4) || !is_aligned(ctx_lens, 4) || !is_aligned(q_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    const size_t row_bytes = (size_t)d.num_seqs * d.num_q_heads * kDim * 2;
+    const char *qc = static_cast<const char *>(q), *oc = static_cast<const char *>(out);
+    if (qc < oc + row_bytes && oc < qc + row_bytes) return PA_ERR_INVALID_ARG;
+    const KittyWs w = kitty_ws(d);
+    if (!workspace || workspace_bytes < w.total || !is_aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+    DecParams p;
+    p.q = q;
+    p.pages = static_cast<const uint8_t *>(pages);
+    p.res_k = res_k;
+    p.res_v = res_v;
+    p.bt = block_tables;
+    p.ctx = ctx_lens;
+    p.qlen = q_lens;
+    p.out = out;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.num_seqs = d.num_seqs;
+    p.q_heads = d.num_q_heads;
+    p.kv_heads = d.num_kv_heads;
+    p.group = d.num_q_heads / d.num_kv_heads;
+    p.max_pages = d.max_pages_per_seq;
+    p.max_chunks = w.max_chunks;
+    p.num_pages = d.num_pages;
+    p.num_res = d.num_res_pages;
+    char *ws = static_cast<char *>(workspace);
+    p.counters = reinterpret_cast<uint32_t *>(ws);
+    p.arrive = reinterpret_cast<uint32_t *>(ws + w.arrive);
+    p.parts = reinterpret_cast<float *>(ws + w.parts);
+    p.status = status_ptr();
+    const int sms = sm_count();
+    if (!p.status || sms <= 0) return PA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, w.zero_bytes, s) != cudaSuccess) return PA_ERR_CUDA;
+    const cudaError_t e = d.dtype == PA_BF16 ? launch_decode<__nv_bfloat16>(p, d.promoted, sms, s)
+                                             : launch_decode<__half>(p, d.promoted, sms, s);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // extern "C"

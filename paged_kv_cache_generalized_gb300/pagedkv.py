@@ -32,7 +32,10 @@ _E4M3 = tuple(t for t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if
 _ELEM = {torch.float32: 4, torch.bfloat16: 2, torch.float16: 2}
 
 EXPORTED = ("pa_forward_workspace_size", "pa_forward", "pa_forward_no_alloc", "kv_append",
-            "block_copy", "pa_get_device_status", "pa_status_string", "pa_version")
+            "block_copy", "pa_get_device_status", "pa_status_string", "pa_version",
+            "pa_kitty_record_bytes", "pa_kitty_workspace_size", "kv_quantize_pages",
+            "pa_forward_kitty")
+KITTY_PAGE_TOKENS = 128
 NO_ALLOC_WORKSPACE_BYTES = 32 * 1024 * 1024
 
 
@@ -60,6 +63,14 @@ class BlockCopyDims(ctypes.Structure):
                 ("src_block_stride", ctypes.c_int64), ("dst_block_stride", ctypes.c_int64),
                 ("src_num_blocks", ctypes.c_int64), ("dst_num_blocks", ctypes.c_int64),
                 ("num_pairs", ctypes.c_int64), ("max_ctas", ctypes.c_int32)]
+
+
+class KittyDims(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("promoted", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64), ("num_res_pages", ctypes.c_int64),
+                ("max_pages_per_seq", ctypes.c_int32)]
 
 
 class PagedKVError(RuntimeError):
@@ -97,6 +108,15 @@ def load_library(path: str | None = None):
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_version.restype = ctypes.c_char_p
+    lib.pa_kitty_record_bytes.restype = sz
+    lib.pa_kitty_record_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    lib.pa_kitty_workspace_size.restype = sz
+    lib.pa_kitty_workspace_size.argtypes = [ctypes.POINTER(KittyDims)]
+    lib.kv_quantize_pages.restype = ctypes.c_int
+    lib.kv_quantize_pages.argtypes = [ctypes.POINTER(KittyDims), P, P, P, ctypes.c_int64, P, P]
+    lib.pa_forward_kitty.restype = ctypes.c_int
+    lib.pa_forward_kitty.argtypes = [ctypes.POINTER(KittyDims), P, P, P, P, P, P, P, ctypes.c_float,
+                                     P, P, sz, P]
     _lib = lib
     return lib
 
@@ -203,6 +223,73 @@ def pa_forward_no_alloc(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, sca
                                  _ptr(block_tables), _ptr(ctx_lens), _ptr(q_lens),
                                  ctypes.c_float(scale), _ptr(out), _stream(stream))
     _check(rc, "pa_forward_no_alloc")
+    return out
+
+
+def kitty_record_bytes(promoted: int, head_dim: int = 128) -> int:
+    """Bytes of one (page, KV head) record of the 2-bit page format (0 if unsupported)."""
+    return int(load_library().pa_kitty_record_bytes(head_dim, promoted))
+
+
+def kitty_dims(q_or_res, pages, promoted, num_q_heads=None, num_seqs=1, res_pages=None,
+               max_pages_per_seq=1) -> KittyDims:
+    """KittyDims from the page pool ([num_pages, Hkv, record] uint8) and a residual pool
+    ([num_res, Hkv, 128, d])."""
+    if pages.dim() != 3 or pages.dtype != torch.uint8 or not pages.is_contiguous():
+        raise ValueError("pages must be contiguous uint8 [num_pages, Hkv, record_bytes]")
+    if res_pages is None or res_pages.dim() != 4 or not res_pages.is_contiguous():
+        raise ValueError("residual pages must be contiguous [num_res, Hkv, 128, d]")
+    if res_pages.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("residual pages must be bf16 or f16")
+    hkv = pages.shape[1]
+    return KittyDims(_DTYPES[res_pages.dtype], int(num_seqs), int(num_q_heads or hkv), int(hkv),
+                     int(res_pages.shape[3]), int(promoted), int(pages.shape[0]),
+                     int(res_pages.shape[0]), int(max_pages_per_seq))
+
+
+def kv_quantize_pages(res_k, res_v, pairs, pages, promoted, stream=None):
+    """Quantises residual page s into record t of ``pages`` for every (s, t) row of ``pairs``
+    (int64 [P, 2]), every KV head (see ``kv_quantize_pages`` in include/pagedkv.h)."""
+    lib = load_library()
+    if res_v.shape != res_k.shape or res_v.dtype != res_k.dtype:
+        raise ValueError("res_k and res_v must match")
+    if pairs.dtype != torch.int64 or not pairs.is_contiguous():
+        raise ValueError("pairs must be contiguous int64 [P, 2]")
+    dims = kitty_dims(None, pages, promoted, res_pages=res_k)
+    rc = lib.kv_quantize_pages(ctypes.byref(dims), _ptr(res_k), _ptr(res_v), _ptr(pairs),
+                               ctypes.c_int64(pairs.numel() // 2), _ptr(pages), _stream(stream))
+    _check(rc, "kv_quantize_pages")
+    return pages
+
+
+def pa_forward_kitty(q, pages, res_k, res_v, block_tables, ctx_lens, q_lens, promoted, scale=None,
+                     out=None, workspace=None, stream=None):
+    """Decode attention over 2-bit pages with promoted 4-bit key channels plus each sequence's
+    residual page (see ``pa_forward_kitty`` in include/pagedkv.h).  q: [S, Hq, 128]; pages:
+    uint8 [num_pages, Hkv, record]; res_k/res_v: [num_res, Hkv, 128, 128] in q's dtype;
+    block_tables int32 [S, max_pages]; ctx_lens/q_lens int32 [S] (q_lens all 1)."""
+    lib = load_library()
+    for t in (block_tables, ctx_lens, q_lens):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError("block_tables, ctx_lens and q_lens must be contiguous int32")
+    if not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be contiguous [S, Hq, d]")
+    if res_v.shape != res_k.shape or res_k.dtype != q.dtype or res_v.dtype != q.dtype:
+        raise ValueError("residual pages must match each other and q's dtype")
+    dims = kitty_dims(q, pages, promoted, num_q_heads=q.shape[1], num_seqs=q.shape[0],
+                      res_pages=res_k, max_pages_per_seq=block_tables.shape[1])
+    if scale is None:
+        scale = 1.0 / float(dims.head_dim) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    need = int(lib.pa_kitty_workspace_size(ctypes.byref(dims)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.pa_forward_kitty(ctypes.byref(dims), _ptr(q), _ptr(pages), _ptr(res_k), _ptr(res_v),
+                              _ptr(block_tables), _ptr(ctx_lens), _ptr(q_lens),
+                              ctypes.c_float(scale), _ptr(out), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "pa_forward_kitty")
     return out
 
 

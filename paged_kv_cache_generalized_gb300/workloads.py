@@ -443,3 +443,84 @@ def swap_plan(batch: AttnBatch, frac: float = 0.125) -> np.ndarray:
         k = int(frac * int(batch.ctx_lens[i])) // B
         out.extend(int(x) for x in batch.block_tables[i, :k])
     return np.asarray(out, dtype=np.int64)
+
+
+@dataclass
+class KittyBatch:
+    """A decode batch over 2-bit pages with promoted key channels ("KVキャッシュ管理の教科書"
+    第22章, Kitty), before quantisation: every full 128-token page's tokens sit in a staging pool
+    in the residual-page format (``stage_k``/``stage_v`` [num_full, Hkv, 128, d]); ``pairs`` maps
+    staging page s to its record id t in a pool of ``num_pages`` records.  Each sequence's last
+    n % 128 tokens sit in residual page ``block_tables[i][n // 128]`` of ``res_k``/``res_v`` (later
+    slots NaN-poisoned: never read).  Sequence i has n_i = ctx_lens[i] + 1 tokens; q is
+    [S, Hq, d]."""
+    name: str
+    dtype: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    promoted: int
+    scale: float
+    q: np.ndarray
+    ctx_lens: np.ndarray
+    q_lens: np.ndarray
+    stage_k: np.ndarray
+    stage_v: np.ndarray
+    pairs: np.ndarray
+    num_pages: int
+    res_k: np.ndarray
+    res_v: np.ndarray
+    block_tables: np.ndarray
+    page_of: list = field(default_factory=list)   # per sequence: staging ids of its full pages
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.ctx_lens)
+
+
+def make_kitty_batch(name, ctx_lens, num_q_heads, num_kv_heads, promoted, dtype="bf16", seed=7,
+                     slack=0.1, head_dim=128):
+    T = 128
+    rng = np.random.Generator(np.random.PCG64(seed + 300))
+    ctx = np.asarray(ctx_lens, dtype=np.int32)
+    n = ctx.astype(np.int64) + 1
+    nfull = n // T
+    num_full = int(nfull.sum())
+    has_tail = (n % T) > 0
+    num_res = int(has_tail.sum()) + 2
+    num_pages = int(np.ceil(num_full * (1 + slack))) + 1
+    S = len(ctx)
+    maxp = int(((n + T - 1) // T).max())
+    stage_k = random_values((num_full, num_kv_heads, T, head_dim), dtype, seed * 1000 + 1)
+    stage_v = random_values((num_full, num_kv_heads, T, head_dim), dtype, seed * 1000 + 2)
+    rec_ids = rng.permutation(num_pages)[:num_full]
+    pairs = np.stack([np.arange(num_full), rec_ids], axis=1).astype(np.int64)
+    res_k = random_values((num_res, num_kv_heads, T, head_dim), dtype, seed * 1000 + 3)
+    res_v = random_values((num_res, num_kv_heads, T, head_dim), dtype, seed * 1000 + 4)
+    res_ids = rng.permutation(num_res)
+    bt = np.full((S, maxp), -1, dtype=np.int32)
+    page_of = []
+    j = r = 0
+    for i in range(S):
+        page_of.append(list(range(j, j + int(nfull[i]))))
+        bt[i, :nfull[i]] = rec_ids[j:j + nfull[i]]
+        j += int(nfull[i])
+        if has_tail[i]:
+            rid = int(res_ids[r])
+            r += 1
+            bt[i, nfull[i]] = rid
+            tail = int(n[i] % T)
+            res_k[rid, :, tail:] = nan_value(dtype)
+            res_v[rid, :, tail:] = nan_value(dtype)
+    q = random_values((S, num_q_heads, head_dim), dtype, seed * 1000 + 5)
+    return KittyBatch(name, dtype, num_q_heads, num_kv_heads, head_dim, promoted,
+                      1.0 / float(np.sqrt(head_dim)), q, ctx, np.ones(S, np.int32), stage_k,
+                      stage_v, pairs, num_pages, res_k, res_v, bt, page_of)
+
+
+def decode13b_kitty(seed: int = 2, num_seqs: int = 64, lo: int = 512, hi: int = 4096, promoted: int = 32,
+                    **kw) -> KittyBatch:
+    """The decode13b batch (40 MHA heads, head_dim 128, bf16, context U{lo..hi}) over 2-bit pages
+    with ``promoted`` 4-bit key channels."""
+    ctx = decode13b_lengths(seed, num_seqs, lo, hi)
+    return make_kitty_batch("decode13b_kitty", ctx, 40, 40, promoted, seed=seed, **kw)

@@ -157,3 +157,49 @@ def test_e4m3_caches_reject_bad_scales_and_unsupported_shapes(lib):
     a.k_scale = 1.0
     a.head_dim = 8                                     # 8 codes per row: not a 16-byte vector
     assert lib.kv_append(ctypes.byref(a), FAKE, FAKE, FAKE, FAKE, FAKE, None) == 2
+
+
+def _kdims(**kw):
+    from paged_kv_cache_generalized_gb300.pagedkv import KittyDims
+
+    base = dict(dtype=1, num_seqs=4, num_q_heads=8, num_kv_heads=2, head_dim=128, promoted=32,
+                num_pages=20, num_res_pages=5, max_pages_per_seq=9)
+    base.update(kw)
+    return KittyDims(**base)
+
+
+def test_kitty_record_and_workspace_sizes_are_host_only(lib):
+    assert lib.pa_kitty_record_bytes(128, 32) == 11296
+    assert lib.pa_kitty_record_bytes(128, 16) == 10784
+    assert lib.pa_kitty_record_bytes(64, 16) == 0 and lib.pa_kitty_record_bytes(128, 8) == 0
+    ws = lib.pa_kitty_workspace_size(ctypes.byref(_kdims()))
+    # counters, arrival counts, and per row (4 x 8) ceil(9 / 4) + 1 split records of 132 floats
+    assert ws >= 4 * 8 * 4 * 132 * 4
+    for bad in (dict(promoted=24), dict(head_dim=64), dict(num_q_heads=7), dict(dtype=0),
+                dict(num_seqs=0), dict(num_seqs=8193), dict(max_pages_per_seq=0), dict(num_pages=-1)):
+        assert lib.pa_kitty_workspace_size(ctypes.byref(_kdims(**bad))) == 0, bad
+
+
+@pytest.mark.parametrize("kw,code", [(dict(promoted=24), 2), (dict(head_dim=64), 2), (dict(dtype=0), 2),
+                                     (dict(num_q_heads=7), 1), (dict(num_seqs=0), 1)])
+def test_kitty_calls_reject_bad_dims(lib, kw, code):
+    d = _kdims(**kw)
+    assert lib.pa_forward_kitty(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                ctypes.c_float(0.1), FAKE, FAKE, 1 << 30, None) == code
+    assert lib.kv_quantize_pages(ctypes.byref(d), FAKE, FAKE, FAKE, 1, FAKE, None) == code
+
+
+def test_kitty_calls_reject_bad_pointers_and_workspace(lib):
+    d = _kdims()
+    odd = ctypes.c_void_p(0x10008)
+    out = ctypes.c_void_p(0x100000)                 # apart from q
+    args = [FAKE] * 7
+    assert lib.pa_forward_kitty(ctypes.byref(d), *args, ctypes.c_float(0.1), out, FAKE, 16, None) == 3
+    assert lib.pa_forward_kitty(ctypes.byref(d), *args, ctypes.c_float(0.1), FAKE, FAKE, 1 << 30, None) == 1
+    assert lib.pa_forward_kitty(ctypes.byref(d), odd, *args[1:], ctypes.c_float(0.1), out, FAKE,
+                                1 << 30, None) == 1
+    assert lib.pa_forward_kitty(ctypes.byref(d), *args, ctypes.c_float(float("nan")), out, FAKE,
+                                1 << 30, None) == 1
+    assert lib.kv_quantize_pages(ctypes.byref(d), FAKE, FAKE, FAKE, 0, FAKE, None) == 0   # no-op
+    assert lib.kv_quantize_pages(ctypes.byref(d), FAKE, FAKE, FAKE, -1, FAKE, None) == 1
+    assert lib.kv_quantize_pages(ctypes.byref(d), odd, FAKE, FAKE, 1, FAKE, None) == 1
