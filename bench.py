@@ -26,6 +26,10 @@ Workloads (``--workload``):
               into a staging slot + block_copy scatter).  Metric: attention TFLOP/s of all layers
               with the swap-in inside the step; the JSON line also carries the serial schedule,
               each half alone, the gather-kernel variant and swap-out.
+  decode13b_kitty  the decode13b batch over 2-bit K/V pages of 128 tokens with 32 of 128 key
+              channels at 4 bits (Kitty), the last n % 128 tokens of each sequence in a bf16
+              residual page; per step one appended token per sequence and one page quantised.
+              Metric: GB/s (of the page records and residual bytes); the line also gives tokens/s.
   layout      the decode13b batch on one layer of an 8-layer pool kept block-first (all layers of
               a block contiguous) and layer-first; swap-in of 8 sessions in both layouts, by the
               gather kernel and by one copy-engine transfer per contiguous segment.  Metric: decode
@@ -272,6 +276,95 @@ class AttnStep:
         self.out_host.copy_(self.out, non_blocking=True)
 
 
+class KittyStep:
+    """kv_append + kv_quantize_pages + pa_forward_kitty over one KittyBatch (2-bit pages with
+    promoted 4-bit key channels), all inputs resident on the GPU.  The step appends each
+    sequence's new token into its residual page (the token's own values: the append is
+    idempotent) and quantises one residual page into a spare record: with 64 sequences a page
+    fills every 2 steps on average, so one page per step is the amortised quantisation cost."""
+
+    def __init__(self, batch: W.KittyBatch, dev):
+        import torch
+        import paged_kv_cache_generalized_gb300 as pkg
+
+        self.pkg, self.torch, self.b, self.dev = pkg, torch, batch, dev
+        self.kv8 = False
+        tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[batch.dtype]
+        S, Hq, Hkv, d, P = batch.num_seqs, batch.num_q_heads, batch.num_kv_heads, batch.head_dim, batch.promoted
+        T = 128
+        R = pkg.kitty_record_bytes(P)
+
+        def up(x, dt=None):
+            t = torch.from_numpy(np.ascontiguousarray(x))
+            if dt is not None:
+                t = t.view(torch.int16).view(dt)
+            return t
+
+        n = batch.ctx_lens.astype(np.int64) + 1
+        nfull, tail = n // T, n % T
+        slots = np.full(S, -1, np.int64)
+        k_new = np.zeros((S, Hkv, d), np.uint16)
+        v_new = np.zeros((S, Hkv, d), np.uint16)
+        for i in range(S):
+            if tail[i]:
+                rid = int(batch.block_tables[i, nfull[i]])
+                slots[i] = rid * T + tail[i] - 1
+                k_new[i] = batch.res_k[rid, :, tail[i] - 1]
+                v_new[i] = batch.res_v[rid, :, tail[i] - 1]
+        spare = np.setdiff1d(np.arange(batch.num_pages), batch.pairs[:, 1])[0]
+        self.host = {
+            "q": up(batch.q, tdt).pin_memory(),
+            "k_new": up(k_new, tdt).pin_memory(),
+            "v_new": up(v_new, tdt).pin_memory(),
+            "slots": up(slots).pin_memory(),
+            "bt": up(batch.block_tables).pin_memory(),
+            "ctx": up(batch.ctx_lens).pin_memory(),
+            "ql": up(batch.q_lens).pin_memory(),
+            "qpair": up(np.array([[0, spare]], np.int64)).pin_memory(),
+        }
+        self.dev_in = {k2: v.to(dev) for k2, v in self.host.items()}
+        self.pages = torch.zeros((batch.num_pages, Hkv, R), dtype=torch.uint8, device=dev)
+        sk, sv = up(batch.stage_k, tdt).to(dev), up(batch.stage_v, tdt).to(dev)
+        pkg.kv_quantize_pages(sk, sv, up(batch.pairs).to(dev), self.pages, P)
+        # one staging page pair stays for the per-step quantisation
+        self.stage_k, self.stage_v = sk[:1].clone(), sv[:1].clone()
+        del sk, sv
+        self.res_k, self.res_v = up(batch.res_k, tdt).to(dev), up(batch.res_v, tdt).to(dev)
+        self.pool = self.pages
+        self.out = torch.empty_like(self.dev_in["q"])
+        self.out_host = torch.empty_like(self.host["q"]).pin_memory()
+        self.ws = torch.empty(1 << 26, dtype=torch.uint8, device=dev)
+        es = 2
+        self.bytes_attn = float((nfull * Hkv * R).sum() + (tail * Hkv * d * es * 2).sum()
+                                + 2 * S * Hq * d * es + ((n + T - 1) // T).sum() * 4 + S * 8)
+        self.bytes_append = float(2 * int((tail > 0).sum()) * Hkv * d * es * 2 + 8 * S)
+        self.bytes_copy = float(2 * Hkv * T * d * es + Hkv * R + 16)
+        self.flops = attn_flops(batch.ctx_lens, batch.q_lens, Hq, d)
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+        self.launches_per_step = 3          # kv_append, kv_quantize_pages, the decode kernel
+        self.kernel_name = "pa_forward_kitty (persistent decode kernel over 2-bit page records + residual pages)"
+        self.dtype_label = f"bf16 q/out, 2-bit K/V with {P} of 128 key channels at 4 bits, fp32 accumulate"
+        self.pool_bytes = (self.pages.numel() + 2 * self.res_k.numel() * es)
+
+    def step(self, ev=None):
+        inp = self.dev_in
+        self.pkg.kv_append(inp["k_new"], inp["v_new"], inp["slots"], self.res_k, self.res_v)
+        self.pkg.kv_quantize_pages(self.stage_k, self.stage_v, inp["qpair"], self.pages, self.b.promoted)
+        if ev is not None:
+            ev[0].record()
+        self.pkg.pa_forward_kitty(inp["q"], self.pages, self.res_k, self.res_v, inp["bt"], inp["ctx"],
+                                  inp["ql"], self.b.promoted, self.b.scale, out=self.out, workspace=self.ws)
+        if ev is not None:
+            ev[1].record()
+
+    def e2e_step(self):
+        for k2, v in self.host.items():
+            self.dev_in[k2].copy_(v, non_blocking=True)
+        self.step()
+        self.out_host.copy_(self.out, non_blocking=True)
+
+
 class KVMoveStep:
     """KV movement over a multi-layer fp16 pool [L, 2, num_blocks, Hkv, B, d] resident on the GPU:
     block_copy of the copy-on-write pairs (every resident layer, K and V), kv_append of every
@@ -506,6 +599,9 @@ def build_attn_step(name, dev, seqs=None):
     if name in ("decode13b", "decode13b_fp8"):
         b = W.decode13b(seed=2, num_seqs=seqs or 64, poison=False)
         return AttnStep(b, dev, cow_frac=0.1, seed=2, kv8=name.endswith("fp8")), b
+    if name == "decode13b_kitty":
+        b = W.decode13b_kitty(seed=2, num_seqs=seqs or 64)
+        return KittyStep(b, dev), b
     if name == "mixed_gqa":
         half = (seqs or 64) // 2
         b = W.mixed_gqa(seed=3, n_resume=half, n_decode=half, poison=False)
@@ -521,6 +617,10 @@ WORKLOAD_TEXT = {
                  "ctx U{512..4096}, pool +10% free, 6 copy-on-write forks per step",
     "decode13b_fp8": "decode13b_fp8: the decode13b batch with FP8 E4M3 K/V caches (scale 1/32 for K and V), "
                      "bf16 queries and outputs",
+    "decode13b_kitty": "decode13b_kitty: the decode13b batch (64 seqs, 40 MHA heads, head_dim 128, ctx U{512..4096}) "
+                       "over 2-bit K/V pages of 128 tokens with 32 of 128 key channels promoted to 4 bits "
+                       "(Kitty), each sequence's last n % 128 tokens in a bf16 residual page; per step one "
+                       "appended token per sequence and one page quantised",
     "mixed_gqa": "mixed_gqa: 32 resumed turns (ctx U{1024..16384}, q U{16..512}) + 32 decode "
                  "(ctx U{256..8192}), GQA 32/8, head_dim 128, bf16, block 32",
     "longprefill": "longprefill: 8 seqs x (16384 cached + 2048 new), 40 MHA heads, head_dim 128, "
@@ -618,6 +718,49 @@ def oracle_sample(b: W.AttnBatch, budget_s: float, max_rows=None):
     return t_total, kv_bytes, flops, rows, threads
 
 
+def kitty_oracle_sample(b: W.KittyBatch, budget_s: float):
+    """Times the oracle's decode attention over 2-bit pages (it dequantises every page of the
+    sequence, then runs the float64 attention) on whole sequences of the batch, longest first,
+    for about ``budget_s`` seconds; the oracle's own page records are made before the clock starts.
+    Returns (seconds, bytes, flops, rows, threads)."""
+    import oracle
+    from oracle import kitty
+
+    threads = oracle.max_threads()
+    R = kitty.record_bytes(b.promoted)
+    order = np.argsort(-b.ctx_lens, kind="stable")
+    cache = {}
+    t_total, nbytes, flops, rows = 0.0, 0.0, 0.0, []
+    while t_total < budget_s:
+        for i in order:
+            i = int(i)
+            n = int(b.ctx_lens[i]) + 1
+            if i not in cache:
+                recs = np.zeros((max(1, n // 128), b.num_kv_heads, R), np.uint8)
+                bt = np.full((1, b.block_tables.shape[1]), -1, np.int32)
+                for p_, sid in enumerate(b.page_of[i]):
+                    for h in range(b.num_kv_heads):
+                        f = kitty.quantize_page(oracle.widen_f32(b.stage_k[sid, h], b.dtype),
+                                                oracle.widen_f32(b.stage_v[sid, h], b.dtype), b.promoted)
+                        recs[p_, h] = kitty.pack_record(f)
+                    bt[0, p_] = p_
+                if n % 128:
+                    bt[0, n // 128] = b.block_tables[i, n // 128]
+                cache[i] = (recs, bt)
+            recs, bt = cache[i]
+            t0 = time.perf_counter()
+            kitty.paged_attention(b.q[i:i + 1], recs, b.res_k, b.res_v, b.dtype, bt, b.ctx_lens[i:i + 1],
+                                  b.q_lens[i:i + 1], b.num_q_heads, b.num_kv_heads, b.promoted, b.scale,
+                                  threads=threads)
+            t_total += time.perf_counter() - t0
+            nbytes += (n // 128) * b.num_kv_heads * R + (n % 128) * b.num_kv_heads * b.head_dim * 4
+            flops += attn_flops(b.ctx_lens[i:i + 1], b.q_lens[i:i + 1], b.num_q_heads, b.head_dim)
+            rows.append(i)
+            if t_total >= budget_s:
+                break
+    return t_total, nbytes, flops, rows, threads
+
+
 def metric_for(name):
     if name == "kvmove":
         return ("KV movement GB/s (bytes read + written by copy-on-write, append and swap-in per step / step time)", "GB/s", True)
@@ -626,6 +769,9 @@ def metric_for(name):
     if name == "decode13b_fp8":
         return ("paged-attn decode KV GB/s with FP8 E4M3 K/V caches (algorithmic HBM bytes per step / step "
                 "time)", "GB/s", True)
+    if name == "decode13b_kitty":
+        return ("paged-attn decode KV GB/s over 2-bit pages with promoted 4-bit key channels (algorithmic "
+                "HBM bytes per step / step time)", "GB/s", True)
     if name == "layout":
         return ("paged-attn decode KV GB/s on a block-first pool (one layer of L; all layers of a block "
                 "contiguous)", "GB/s", True)
@@ -658,6 +804,28 @@ def run_reference(args):
                 "data": "synthetic", "config": {"workload": workload_text(name, args)},
                 "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                                  "sample": "numpy block copy of 64 copy-on-write pairs and append of 256 tokens per repetition"},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    if name == "decode13b_kitty":
+        kb = W.decode13b_kitty(seed=2)
+        total = args.steps + args.warmup
+        per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
+        secs, moved, nrows, threads = 0.0, 0.0, 0, 1
+        for s_ in range(total):
+            t, nb, _, rows, threads = kitty_oracle_sample(kb, per_step)
+            if s_ >= args.warmup:
+                secs += t
+                moved += nb
+                nrows += len(rows)
+        value = moved / secs / 1e9
+        line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(1, args.steps) * 1e3,
+                "higher_is_better": hib, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": workload_text(name, args)},
+                "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                                 "sample": f"oracle decode attention over 2-bit pages (dequantise + float64 attention) "
+                                           f"on {nrows} whole sequence(s), ~{per_step:.2f}s per step"},
                 "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -762,7 +930,8 @@ def run_native(args):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "traffic_source": tsrc,
                 "algorithmic_bytes": step_obj.bytes_attn,
-                "kernel": "pa_forward (plan + split-KV CUDA-core attention with fused split merge)",
+                "kernel": getattr(step_obj, "kernel_name",
+                                  "pa_forward (plan + split-KV CUDA-core attention with fused split merge)"),
                 "peak_source": f"hbm_gbs of {peak_src}"}
     else:
         achieved = step_obj.flops / (attn_ms * 1e-3) / 1e12
@@ -776,20 +945,26 @@ def run_native(args):
 
     cpu = None
     if world == 1 or rank == 0:
-        t, kvb, fl, rows, threads = oracle_sample(batch, args.cpu_seconds)
+        if isinstance(batch, W.KittyBatch):
+            t, kvb, fl, rows, threads = kitty_oracle_sample(batch, args.cpu_seconds)
+            what = "oracle decode attention over 2-bit pages (dequantise + float64 attention)"
+        else:
+            t, kvb, fl, rows, threads = oracle_sample(batch, args.cpu_seconds)
+            what = "float64 oracle"
         cval = kvb / t / 1e9 if unit == "GB/s" else fl / t / 1e12
         cpu = {"value": cval, "unit": unit, "cores": threads, "kind": "oracle",
-               "sample": f"float64 oracle on {len(rows)} whole sequence(s) of the batch, repeated "
+               "sample": f"{what} on {len(rows)} whole sequence(s) of the batch, repeated "
                          f"passes allowed (all heads, all new tokens), {t:.1f}s; attention only"}
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": hib,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16 q/out, e4m3 K/V, fp32 accumulate" if step_obj.kv8 else batch.dtype,
+            "dtype": getattr(step_obj, "dtype_label",
+                             "bf16 q/out, e4m3 K/V, fp32 accumulate" if step_obj.kv8 else batch.dtype),
             "data": "synthetic",
             "config": {"workload": workload_text(name, args),
                        "l2": "inputs larger than L2 (KV pool %.2f GB resident)" % (
-                           (step_obj.pool.numel() * step_obj.pool.element_size()) / 1e9),
-                       "query_tokens_per_s": batch.total_q * world / (attn_ms * 1e-3),
+                           getattr(step_obj, "pool_bytes", step_obj.pool.numel() * step_obj.pool.element_size()) / 1e9),
+                       "query_tokens_per_s": getattr(batch, "total_q", batch.num_seqs) * world / (attn_ms * 1e-3),
                        "bytes_per_step": step_bytes, "attn_flops_per_step": step_obj.flops,
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "cpu_baseline": cpu,

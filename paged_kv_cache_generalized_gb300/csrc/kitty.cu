@@ -2,12 +2,13 @@
 // Kitty): the page quantiser and decode attention over quantised pages.  The record format and
 // the readings taken where the chapter leaves a step open are in include/pagedkv.h.
 //
-// kitty_quantize_kernel: one CTA of 128 threads per (pair, KV head).  K pass: thread x owns
-// channel x -- float32 magnitude sum over the tokens in order, min, max; the promoted set is the
-// P channels of largest sum (rank by comparison with every other channel, ties to the lower id);
-// codes by float32 subtract, divide and round-half-even; 16 channels' low bits meet in one word
-// through shuffles, high bits through shared-memory ORs.  V pass: one warp per token, a lane per
-// 4 channels, min/max by shuffles.
+// kitty_quantize_kernel: one CTA of 512 threads per (pair, KV head), the page's K and V staged in
+// shared memory.  Thread x < 128 owns channel x for the statistics -- float32 magnitude sum over
+// the tokens in order, min, max; the promoted set is the P channels of largest sum (rank by
+// comparison with every other channel, ties to the lower id).  Codes by float32 subtract, divide
+// and round-half-even, four threads per channel (a quarter of the tokens each); 16 channels' low
+// bits meet in one word through shuffles, high bits through shared-memory ORs.  V: one warp per
+// token, a lane per 4 channels, min/max by shuffles.
 //
 // kitty_decode_kernel: persistent, 8 warps per CTA, one CTA per SM.  Phase 1 streams the
 // quantised pages: a work item is (sequence, query head, up to kChunkPages pages); each warp runs
@@ -22,7 +23,8 @@
 // of every fourth key, and P * s_t (rounded to f16) meets the V codes the same way; the V minimum
 // contributes sum_t p_t min_t.  Phase 2 runs each sequence's residual page (fewer than 128
 // unquantised tokens) as one more item with plain loads.  Items of one row merge by the
-// logsumexp rule: the last split to finish reads the others' (m, l, o) records through L2.
+// logsumexp rule: the last split to finish reads the others' (m, l, o) records through L2.  Odd
+// warps take residual items before pages, so that their loads overlap the others' streaming.
 #include <math.h>
 #include <stdint.h>
 
@@ -36,7 +38,7 @@ constexpr int kPageTokens = 128;
 constexpr int kDim = 128;
 constexpr int kOffKs = 0, kOffKm = 512, kOffVs = 1024, kOffVm = 1536, kOffPid = 2048, kOffKlo = 2080;
 constexpr int kOffKhi = kOffKlo + 32 * kPageTokens;               // 6176
-constexpr int kChunkPages = 4;                                    // pages per decode work item
+constexpr int kChunkPages = 8;                                    // pages per decode work item
 constexpr int kDecWarps = 8;
 constexpr int kStages = 2;
 constexpr int kPartFloats = 132;                                  // m, l, 2 pad, o[128]
@@ -56,75 +58,110 @@ struct QuantParams {
     unsigned *status;
 };
 
+constexpr int kQThreads = 512;
+constexpr int kQSmem = 2 * kPageTokens * kDim * 2;                // the page's K and V (16-bit)
+
 template <typename T, int P>
-__global__ void __launch_bounds__(128) kitty_quantize_kernel(QuantParams p) {
+__global__ void __launch_bounds__(kQThreads) kitty_quantize_kernel(QuantParams p) {
     constexpr int kHiWords = P / 16;                 // 32-bit words of high bits per token
-    __shared__ float s_mag[kDim];
+    extern __shared__ __align__(16) unsigned char qsm[];
+    T *s_k = reinterpret_cast<T *>(qsm);
+    T *s_v = s_k + kPageTokens * kDim;
+    __shared__ float s_mag[kDim], s_min[kDim], s_step[kDim];
+    __shared__ int s_slot[kDim];                     // promoted slot of a channel, or -1
     __shared__ int s_cnt[4];
     __shared__ uint32_t s_hi[kPageTokens * kHiWords];
-    const int x = threadIdx.x, lane = x & 31, warp = x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t pair = blockIdx.x;
     const int h = blockIdx.y;
     const int64_t src = p.pairs[2 * pair], dst = p.pairs[2 * pair + 1];
     if (src < 0 || src >= p.num_res || dst < 0 || dst >= p.num_pages) {
-        if (x == 0) report(p.status, PA_DEV_BAD_PAIR);
+        if (tid == 0) report(p.status, PA_DEV_BAD_PAIR);
         return;
     }
     const size_t plane = (size_t)kPageTokens * kDim;
     const T *rk = reinterpret_cast<const T *>(p.res_k) + ((size_t)src * p.kv_heads + h) * plane;
     const T *rv = reinterpret_cast<const T *>(p.res_v) + ((size_t)src * p.kv_heads + h) * plane;
     uint8_t *rec = p.pages + ((size_t)dst * p.kv_heads + h) * record_bytes(P);
-    for (int i = x; i < kPageTokens * kHiWords; i += 128) s_hi[i] = 0u;
+    for (int i = tid; i < kPageTokens * kHiWords; i += kQThreads) s_hi[i] = 0u;
+    {
+        constexpr int kVecs = kPageTokens * kDim * (int)sizeof(T) / 16;
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(rk), *v4 = reinterpret_cast<const uint4 *>(rv);
+        uint4 *dk = reinterpret_cast<uint4 *>(s_k), *dv = reinterpret_cast<uint4 *>(s_v);
+#pragma unroll
+        for (int i = tid; i < kVecs; i += kQThreads) {
+            dk[i] = __ldg(k4 + i);
+            dv[i] = __ldg(v4 + i);
+        }
+    }
+    __syncthreads();
 
-    // K pass 1: channel x's magnitude sum (tokens in order), minimum and maximum, in float32
+    // K, one thread per channel x: magnitude sum (tokens in order), minimum and maximum in float32
     float mag = 0.f, mn = INFINITY, mx = -INFINITY;
-    for (int t = 0; t < kPageTokens; ++t) {
-        const float v = Elem<T>::to_f(rk[t * kDim + x]);
-        mag = __fadd_rn(mag, fabsf(v));
-        mn = fminf(mn, v);
-        mx = fmaxf(mx, v);
+    if (tid < kDim) {
+        for (int t = 0; t < kPageTokens; ++t) {
+            const float v = Elem<T>::to_f(s_k[t * kDim + tid]);
+            mag = __fadd_rn(mag, fabsf(v));
+            mn = fminf(mn, v);
+            mx = fmaxf(mx, v);
+        }
+        s_mag[tid] = mag;
     }
-    s_mag[x] = mag;
     __syncthreads();
-    int rank = 0;
-    for (int y = 0; y < kDim; ++y) {
-        const float my = s_mag[y];
-        rank += (my > mag) || (my == mag && y < x);
+    if (tid < kDim) {
+        // rank = channels ahead of this one (larger sum, or equal sum and lower id)
+        int rank = 0;
+        for (int y = 0; y < kDim; ++y) {
+            const float my = s_mag[y];
+            rank += (my > mag) || (my == mag && y < tid);
+        }
+        const bool prom = rank < P;
+        const unsigned ball = __ballot_sync(0xffffffffu, prom);
+        if (lane == 0) s_cnt[warp] = __popc(ball);
+        s_slot[tid] = prom ? __popc(ball & ((1u << lane) - 1u)) : -1;
+        const float L = prom ? 15.f : 3.f;
+        const float st = __fdiv_rn(__fsub_rn(mx, mn), L);
+        s_min[tid] = mn;
+        s_step[tid] = st;
+        reinterpret_cast<float *>(rec + kOffKs)[tid] = st;
+        reinterpret_cast<float *>(rec + kOffKm)[tid] = mn;
     }
-    const bool prom = rank < P;
-    const unsigned ball = __ballot_sync(0xffffffffu, prom);
-    if (lane == 0) s_cnt[warp] = __popc(ball);
     __syncthreads();
-    int slot = __popc(ball & ((1u << lane) - 1u));
-    for (int w = 0; w < warp; ++w) slot += s_cnt[w];
-    const float L = prom ? 15.f : 3.f;
-    const float s = __fdiv_rn(__fsub_rn(mx, mn), L);
-    reinterpret_cast<float *>(rec + kOffKs)[x] = s;
-    reinterpret_cast<float *>(rec + kOffKm)[x] = mn;
-    if (prom) rec[kOffPid + slot] = (uint8_t)x;
-    if (x >= P && x < 32) rec[kOffPid + x] = 0;
+    if (tid < kDim) {
+        if (s_slot[tid] >= 0) {
+            int slot = s_slot[tid];
+            for (int w = 0; w < warp; ++w) slot += s_cnt[w];
+            s_slot[tid] = slot;
+            rec[kOffPid + slot] = (uint8_t)tid;
+        }
+        if (tid >= P && tid < 32) rec[kOffPid + tid] = 0;
+    }
+    __syncthreads();
 
-    // K pass 2: codes; 16 channels' low bits form one word of the dense tensor
-    for (int t = 0; t < kPageTokens; ++t) {
-        const float v = Elem<T>::to_f(rk[t * kDim + x]);
-        uint32_t c = 0;
-        if (s != 0.f) c = (uint32_t)fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v, mn), s)), 0.f), L);
-        uint32_t w = (c & 3u) << (2 * (x & 15));
-        w |= __shfl_xor_sync(0xffffffffu, w, 1);
-        w |= __shfl_xor_sync(0xffffffffu, w, 2);
-        w |= __shfl_xor_sync(0xffffffffu, w, 4);
-        w |= __shfl_xor_sync(0xffffffffu, w, 8);
-        if ((x & 15) == 0) reinterpret_cast<uint32_t *>(rec + kOffKlo + t * 32)[x >> 4] = w;
-        if (prom) atomicOr(&s_hi[t * kHiWords + (slot >> 4)], (c >> 2) << (2 * (slot & 15)));
+    // K codes: thread (channel x, token quarter g); 16 channels' low bits form one word
+    {
+        const int x = tid & (kDim - 1), g = tid >> 7;
+        const float mnx = s_min[x], sx = s_step[x];
+        const int slot = s_slot[x];
+        const float L = slot >= 0 ? 15.f : 3.f;
+        for (int t = g * 32; t < g * 32 + 32; ++t) {
+            const float v = Elem<T>::to_f(s_k[t * kDim + x]);
+            uint32_t c = 0;
+            if (sx != 0.f) c = (uint32_t)fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v, mnx), sx)), 0.f), L);
+            uint32_t w = (c & 3u) << (2 * (x & 15));
+            w |= __shfl_xor_sync(0xffffffffu, w, 1);
+            w |= __shfl_xor_sync(0xffffffffu, w, 2);
+            w |= __shfl_xor_sync(0xffffffffu, w, 4);
+            w |= __shfl_xor_sync(0xffffffffu, w, 8);
+            if ((x & 15) == 0) reinterpret_cast<uint32_t *>(rec + kOffKlo + t * 32)[x >> 4] = w;
+            if (slot >= 0) atomicOr(&s_hi[t * kHiWords + (slot >> 4)], (c >> 2) << (2 * (slot & 15)));
+        }
     }
-    __syncthreads();
-    for (int i = x; i < kPageTokens * kHiWords; i += 128)
-        reinterpret_cast<uint32_t *>(rec + kOffKhi)[i] = s_hi[i];
 
     // V: one warp per token, lane l owns channels 4l..4l+3
-    for (int t = warp; t < kPageTokens; t += 4) {
+    for (int t = warp; t < kPageTokens; t += kQThreads / 32) {
         float v[4];
-        load_f<T, 4>(rv + t * kDim + 4 * lane, v);
+        load_f<T, 4>(s_v + t * kDim + 4 * lane, v);
         float lo = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
         float hi = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
 #pragma unroll
@@ -149,6 +186,9 @@ __global__ void __launch_bounds__(128) kitty_quantize_kernel(QuantParams p) {
             reinterpret_cast<float *>(rec + kOffVm)[t] = lo;
         }
     }
+    __syncthreads();
+    for (int i = tid; i < kPageTokens * kHiWords; i += kQThreads)
+        reinterpret_cast<uint32_t *>(rec + kOffKhi)[i] = s_hi[i];
 }
 
 // ---- decode attention ----------------------------------------------------------------------
@@ -268,6 +308,108 @@ template <> __device__ __forceinline__ void fma_pair<__half>(uint32_t a, uint32_
     fma_h2(a, b, d0, d1);
 }
 
+// Residual-page items, one per (sequence, query head) whose length is not a multiple of 128: the
+// last n % 128 tokens, unquantised, with plain loads (one lane per key for QK^T, one lane per 4
+// channels for PV, 8 keys' V rows in flight).
+template <typename T>
+__device__ void tail_items(const DecParams &p, int lane) {
+    const uint32_t rows = (uint32_t)p.num_seqs * p.q_heads;
+    while (true) {
+        uint32_t j = 0;
+        if (lane == 0) j = atomicAdd(p.counters + 1, 1u);
+        j = __shfl_sync(0xffffffffu, j, 0);
+        if (j >= rows) break;
+        const int seq = j / p.q_heads, h = j - seq * p.q_heads;
+        const int n = seq_tokens(p, seq);
+        if (n < 0 || n % kPageTokens == 0) continue;
+        const int nt = n % kPageTokens, nfull = n / kPageTokens;
+        const int nch = quant_chunks(n) + 1;
+        const int32_t rid = __ldg(p.bt + (int64_t)seq * p.max_pages + nfull);
+        float m_run = -INFINITY, l_l = 0.f;
+        uint64_t o2[2] = {0ull, 0ull};               // channels 4 lane .. 4 lane + 3
+        if (rid < 0 || rid >= p.num_res) {
+            if (lane == 0) report(p.status, PA_DEV_BAD_BLOCK_ID);
+        } else {
+            const size_t plane = (size_t)kPageTokens * kDim;
+            const T *rk = reinterpret_cast<const T *>(p.res_k) + ((size_t)rid * p.kv_heads + h / p.group) * plane;
+            const T *rv = reinterpret_cast<const T *>(p.res_v) + ((size_t)rid * p.kv_heads + h / p.group) * plane;
+            uint32_t qp[64];
+            const uint4 *qsrc = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + (size_t)j * kDim);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint4 w = __ldg(qsrc + i);
+                qp[4 * i] = w.x, qp[4 * i + 1] = w.y, qp[4 * i + 2] = w.z, qp[4 * i + 3] = w.w;
+            }
+            for (int t0 = 0; t0 < nt; t0 += 32) {
+                const int t = t0 + lane;
+                float z = -INFINITY;
+                if (t < nt) {
+                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    const uint4 *kr = reinterpret_cast<const uint4 *>(rk + (size_t)t * kDim);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint4 w = __ldg(kr + i);
+                        fma_pair<T>(qp[4 * i], w.x, acc[0], acc[1]);
+                        fma_pair<T>(qp[4 * i + 1], w.y, acc[2], acc[3]);
+                        fma_pair<T>(qp[4 * i + 2], w.z, acc[4], acc[5]);
+                        fma_pair<T>(qp[4 * i + 3], w.w, acc[6], acc[7]);
+                    }
+                    z = (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]))) * p.scale_log2;
+                }
+                const float mloc = warp_max(z);
+                if (mloc > m_run) {
+                    const float al = fast_exp2(m_run - mloc);
+                    l_l *= al;
+                    const uint64_t al2 = f2pack(al, al);
+                    o2[0] = mul2(o2[0], al2);
+                    o2[1] = mul2(o2[1], al2);
+                    m_run = mloc;
+                }
+                const float pz = t < nt ? fast_exp2(z - m_run) : 0.f;
+                l_l += pz;
+                const int cnt = min(32, nt - t0);
+                const T *vb = rv + (size_t)t0 * kDim + 4 * lane;
+                // 8 keys' V rows in flight at once; rows past the tail (never read) may hold NaN
+                for (int k0 = 0; k0 < cnt; k0 += 8) {
+                    uint2 w[8];
+                    float pk[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        pk[u] = __shfl_sync(0xffffffffu, pz, k0 + u);
+                        w[u] = k0 + u < cnt ? __ldg(reinterpret_cast<const uint2 *>(vb + (size_t)(k0 + u) * kDim))
+                                            : make_uint2(0u, 0u);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint64_t pk2 = f2pack(pk[u], pk[u]);
+                        o2[0] = fma2(widen2<T>(w[u].x), pk2, o2[0]);
+                        o2[1] = fma2(widen2<T>(w[u].y), pk2, o2[1]);
+                    }
+                }
+            }
+        }
+        const float l = wsum(l_l);
+        float res[4];
+        f2unpack(o2[0], res[0], res[1]);
+        f2unpack(o2[1], res[2], res[3]);
+        if (nch == 1) {
+            if (rid >= 0 && rid < p.num_res) {
+                const float inv = 1.f / l;
+                float v[4] = {res[0] * inv, res[1] * inv, res[2] * inv, res[3] * inv};
+                store_f<T, 4>(reinterpret_cast<T *>(p.out) + (size_t)j * kDim + 4 * lane, v);
+            }
+        } else {
+            float *rec = p.parts + ((size_t)j * p.max_chunks + (nch - 1)) * kPartFloats;
+            reinterpret_cast<float4 *>(rec + 4)[lane] = make_float4(res[0], res[1], res[2], res[3]);
+            if (lane == 0) {
+                rec[0] = m_run;
+                rec[1] = l;
+            }
+            merge_row<T>(p, (int)j, nch, lane);
+        }
+    }
+}
+
 // Shared memory of the decode kernel: per warp kStages records and a scratch area, the ring's
 // mbarriers, then the per-sequence item prefix.
 __host__ __device__ constexpr size_t dec_smem_bytes(int P, int num_seqs) {
@@ -339,6 +481,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
         }
         __syncthreads();
     }
+
+    // odd warps take residual-page items first, so that their latency-bound loads overlap the
+    // page streaming of the even warps; every warp then streams pages, then takes what is left
+    if (warp & 1) tail_items<T>(p, lane);
 
     // ---- phase 1: quantised pages ----
     Item cur = claim_quant(p, s_cu, lane), nxt;
@@ -586,93 +732,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
         return;
     }
 
-    // ---- phase 2: residual pages (the last n % 128 tokens of each sequence, unquantised) ----
-    const uint32_t rows = (uint32_t)p.num_seqs * p.q_heads;
-    while (true) {
-        uint32_t j = 0;
-        if (lane == 0) j = atomicAdd(p.counters + 1, 1u);
-        j = __shfl_sync(0xffffffffu, j, 0);
-        if (j >= rows) break;
-        const int seq = j / p.q_heads, h = j - seq * p.q_heads;
-        const int n = seq_tokens(p, seq);
-        if (n < 0 || n % kPageTokens == 0) continue;
-        const int nt = n % kPageTokens, nfull = n / kPageTokens;
-        const int nch = quant_chunks(n) + 1;
-        const int32_t rid = __ldg(p.bt + (int64_t)seq * p.max_pages + nfull);
-        float m_run = -INFINITY, l_l = 0.f;
-        uint64_t o2[2] = {0ull, 0ull};               // channels 4 lane .. 4 lane + 3
-        if (rid < 0 || rid >= p.num_res) {
-            if (lane == 0) report(p.status, PA_DEV_BAD_BLOCK_ID);
-        } else {
-            const size_t plane = (size_t)kPageTokens * kDim;
-            const T *rk = reinterpret_cast<const T *>(p.res_k) + ((size_t)rid * p.kv_heads + h / p.group) * plane;
-            const T *rv = reinterpret_cast<const T *>(p.res_v) + ((size_t)rid * p.kv_heads + h / p.group) * plane;
-            uint32_t qp[64];
-            const uint4 *qsrc = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + (size_t)j * kDim);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint4 w = __ldg(qsrc + i);
-                qp[4 * i] = w.x, qp[4 * i + 1] = w.y, qp[4 * i + 2] = w.z, qp[4 * i + 3] = w.w;
-            }
-            for (int t0 = 0; t0 < nt; t0 += 32) {
-                const int t = t0 + lane;
-                float z = -INFINITY;
-                if (t < nt) {
-                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    const uint4 *kr = reinterpret_cast<const uint4 *>(rk + (size_t)t * kDim);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint4 w = __ldg(kr + i);
-                        fma_pair<T>(qp[4 * i], w.x, acc[0], acc[1]);
-                        fma_pair<T>(qp[4 * i + 1], w.y, acc[2], acc[3]);
-                        fma_pair<T>(qp[4 * i + 2], w.z, acc[4], acc[5]);
-                        fma_pair<T>(qp[4 * i + 3], w.w, acc[6], acc[7]);
-                    }
-                    z = (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]))) * p.scale_log2;
-                }
-                const float mloc = warp_max(z);
-                if (mloc > m_run) {
-                    const float al = fast_exp2(m_run - mloc);
-                    l_l *= al;
-                    const uint64_t al2 = f2pack(al, al);
-                    o2[0] = mul2(o2[0], al2);
-                    o2[1] = mul2(o2[1], al2);
-                    m_run = mloc;
-                }
-                const float pz = t < nt ? fast_exp2(z - m_run) : 0.f;
-                l_l += pz;
-                const int cnt = min(32, nt - t0);
-                const T *vb = rv + (size_t)t0 * kDim + 4 * lane;
-#pragma unroll 4
-                for (int k = 0; k < cnt; ++k) {
-                    const float pk = __shfl_sync(0xffffffffu, pz, k);
-                    const uint2 w = __ldg(reinterpret_cast<const uint2 *>(vb + (size_t)k * kDim));
-                    const uint64_t pk2 = f2pack(pk, pk);
-                    o2[0] = fma2(widen2<T>(w.x), pk2, o2[0]);
-                    o2[1] = fma2(widen2<T>(w.y), pk2, o2[1]);
-                }
-            }
-        }
-        const float l = wsum(l_l);
-        float res[4];
-        f2unpack(o2[0], res[0], res[1]);
-        f2unpack(o2[1], res[2], res[3]);
-        if (nch == 1) {
-            if (rid >= 0 && rid < p.num_res) {
-                const float inv = 1.f / l;
-                float v[4] = {res[0] * inv, res[1] * inv, res[2] * inv, res[3] * inv};
-                store_f<T, 4>(reinterpret_cast<T *>(p.out) + (size_t)j * kDim + 4 * lane, v);
-            }
-        } else {
-            float *rec = p.parts + ((size_t)j * p.max_chunks + (nch - 1)) * kPartFloats;
-            reinterpret_cast<float4 *>(rec + 4)[lane] = make_float4(res[0], res[1], res[2], res[3]);
-            if (lane == 0) {
-                rec[0] = m_run;
-                rec[1] = l;
-            }
-            merge_row<T>(p, (int)j, nch, lane);
-        }
-    }
+    tail_items<T>(p, lane);
 }
 
 // ---- launchers ---------------------------------------------------------------------------------
@@ -700,12 +760,26 @@ cudaError_t launch_decode(const DecParams &d, int P, int num_sms, cudaStream_t s
     return P == 16 ? launch_decode_t<T, 16>(d, num_sms, s) : launch_decode_t<T, 32>(d, num_sms, s);
 }
 
+template <typename T, int P>
+cudaError_t launch_quantize_t(const QuantParams &q, cudaStream_t s) {
+    static bool configured[kMaxDevs];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevs) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(kitty_quantize_kernel<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const dim3 grid((unsigned)q.num_pairs, (unsigned)q.kv_heads);
+    kitty_quantize_kernel<T, P><<<grid, kQThreads, kQSmem, s>>>(q);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_quantize(const QuantParams &q, int P, cudaStream_t s) {
-    const dim3 grid((unsigned)q.num_pairs, (unsigned)q.kv_heads);
-    if (P == 16) kitty_quantize_kernel<T, 16><<<grid, 128, 0, s>>>(q);
-    else kitty_quantize_kernel<T, 32><<<grid, 128, 0, s>>>(q);
-    return cudaGetLastError();
+    return P == 16 ? launch_quantize_t<T, 16>(q, s) : launch_quantize_t<T, 32>(q, s);
 }
 
 bool is_aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -173,8 +173,9 @@ def test_kitty_record_and_workspace_sizes_are_host_only(lib):
     assert lib.pa_kitty_record_bytes(128, 16) == 10784
     assert lib.pa_kitty_record_bytes(64, 16) == 0 and lib.pa_kitty_record_bytes(128, 8) == 0
     ws = lib.pa_kitty_workspace_size(ctypes.byref(_kdims()))
-    # counters, arrival counts, and per row (4 x 8) ceil(9 / 4) + 1 split records of 132 floats
-    assert ws >= 4 * 8 * 4 * 132 * 4
+    # counters, arrival counts, and per row (4 x 8) at least two split records of 132 floats (the
+    # quantised pages' and the residual page's)
+    assert ws >= 4 * 8 * 2 * 132 * 4
     for bad in (dict(promoted=24), dict(head_dim=64), dict(num_q_heads=7), dict(dtype=0),
                 dict(num_seqs=0), dict(num_seqs=8193), dict(max_pages_per_seq=0), dict(num_pages=-1)):
         assert lib.pa_kitty_workspace_size(ctypes.byref(_kdims(**bad))) == 0, bad
