@@ -23,6 +23,8 @@
 // FMAs with fp32 accumulators: no f16 -> fp32 widening per element.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -1047,6 +1049,322 @@ __global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
                               lane);
 }
 
+// ----------------------------------------------------------------------------------------------
+// GQA decode on tensor cores (16-bit caches, head_dim 128; mma.m16n8k16, fp32 accumulators).  The
+// item structure, the ring and the split merge are those of simt_gqa_kernel; the arithmetic runs
+// as FlashAttention-2 style fragments: the item's R query rows are rows 0..R-1 of a 16-row A
+// operand (the other rows zero), S = Q K^T takes K as B fragments straight from the swizzled TMA
+// panels (ldmatrix), P stays in registers as the A operand of O += P V, and V arrives through TMA
+// with the same swizzle and is read transposed (ldmatrix.trans).  Lane (g, c) owns row g: scores
+// of keys 2c, 2c+1 (+8) of each 16-key stage, and output columns 8 n + 2c, +1.  P is rounded to the
+// query's 16-bit type before PV, as in the tensor-core prefill kernel.
+// ----------------------------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// D += A B, m16n8k16 with A rows 8..15 zero (a1 = a3 = 0): a0 = A[g][2c..2c+1], a2 = A[g][2c+8..2c+9].
+template <typename T>
+__device__ __forceinline__ void mma_rows8(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    if constexpr (sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+// Two fp32 values -> one pair of the 16-bit type (a in the low half), rounded to nearest even.
+template <typename T> __device__ __forceinline__ uint32_t pack16(float a, float b);
+template <> __device__ __forceinline__ uint32_t pack16<__nv_bfloat16>(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+template <> __device__ __forceinline__ uint32_t pack16<__half>(float a, float b) { return h2_from_f32(a, b); }
+
+template <typename T, int R>
+__global__ void __launch_bounds__(kSimtMaxWarps * 32, 1)
+    gqa_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, SimtParams p) {
+    constexpr int D = 128;
+    static_assert(R == 2 || R == 4, "two or four rows per item");
+    using S = GqaStage<T, D>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c4 = lane & 3;
+    const int NST = p.nst;
+    const int nwarps = blockDim.x >> 5;
+    unsigned char *ring = smem + (size_t)warp * NST * S::kBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)nwarps * NST * S::kBytes) + warp * NST;
+    // ldmatrix row addresses within a stage.  S: matrix i = lane / 8 covers keys 8 (i / 2) .. +7 and
+    // channels 8 (i % 2) .. +7 of the 16-channel step; PV: keys 8 (i % 2) .. +7, channels 8 (i / 2)
+    // .. +7 of the 16-channel pair of n-blocks.  Row t of a 128-byte panel holds 16-byte chunk q
+    // at chunk q ^ (t mod 8).
+    const int mi = lane >> 3, mr = lane & 7;
+    const int kkey = (mi >> 1) * 8 + mr, kch = mi & 1;
+    const int vkey = (mi & 1) * 8 + mr, vch = mi >> 1;
+    if (lane == 0) {
+        for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+
+    const int B = p.block_size;
+    const int spb = B / kStageTokens;
+    int slot_i = 0, slot_c = 0, inflight = 0;
+    uint32_t phase_c = 0;
+    const uint32_t total_items = p.counters[kSimtTotal];
+    PendingSplit pend;
+    pend.on = false;
+
+    while (true) {
+        int item = 0;
+        if (lane == 0) item = (int)atomicAdd(&p.counters[kSimtNext], 1u);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if ((uint32_t)item >= total_items) break;
+
+        const int seq = find_owner(p.simt_cu, p.num_seqs, item);
+        const int local = item - __ldg(p.simt_cu + seq);
+        const int K = __ldg(p.nchunk + seq);
+        const int G = __ldg(p.groups + seq);
+        const int chunk = local % K;
+        const int rest = local / K;
+        const int grp = rest % G;
+        const int kvh = rest / G;
+        const int c = __ldg(p.ctx + seq), qn = __ldg(p.qlen + seq);
+        const int64_t tok0 = __ldg(p.cu_q + seq);
+        const int rows_total = qn * p.group;
+        const int r0 = grp * R;
+        const int nrows = min(R, rows_total - r0);
+        const int n = c + qn;
+        const int nb = (n + B - 1) / B;
+        const int cblocks = (nb + K - 1) / K;
+        // causal limit of this lane's row g (-1: a padding row, every key masked)
+        const int Pmine = g < nrows ? c + (r0 + g) / p.group : -1;
+        const int Pmax = c + (r0 + nrows - 1) / p.group;
+        const int st_lo = chunk * cblocks * spb;
+        const int st_hi = min((chunk + 1) * cblocks * spb, (Pmax + kStageTokens) / kStageTokens);
+        const int nb_lim = (Pmax + B) / B;
+
+        float m = -INFINITY, lsum = 0.f;
+        float o[16][4];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+        const int32_t *bt_row = p.bt + (int64_t)seq * p.max_blocks;
+        int wbase = -1000000;
+        int32_t win = 0;
+        bool timed_out = false;
+        int st_issue = st_lo, ib = st_lo / spb, isub = st_lo - (st_lo / spb) * spb;
+
+        auto issue = [&]() {
+            if (ib >= wbase + 32 || ib < wbase) {
+                wbase = ib;
+                win = (wbase + lane < nb_lim) ? __ldg(bt_row + wbase + lane) : 0;
+            }
+            int32_t phys = __shfl_sync(0xffffffffu, win, ib - wbase);
+            if (phys < 0 || (int64_t)phys >= p.num_blocks) {
+                if (lane == 0) report(p.status, PA_DEV_BAD_BLOCK_ID);
+                phys = 0;
+            }
+            if (lane == 0) {
+                unsigned char *dst = ring + (size_t)slot_i * S::kBytes;
+                const int row = kvh * B + isub * kStageTokens;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&bars[slot_i], S::kK + S::kV);
+#pragma unroll
+                for (int pn = 0; pn < S::kPanels; ++pn) {
+                    tma_load_3d(dst + pn * S::kPanelBytes, &kmap, pn * (128 / (int)sizeof(T)), row, phys, &bars[slot_i]);
+                    tma_load_3d(dst + S::kK + pn * S::kPanelBytes, &vmap, pn * (128 / (int)sizeof(T)), row, phys,
+                                &bars[slot_i]);
+                }
+            }
+            slot_i = slot_i + 1 == NST ? 0 : slot_i + 1;
+            ++inflight;
+            ++st_issue;
+            if (++isub == spb) {
+                isub = 0;
+                ++ib;
+            }
+        };
+
+        while (st_issue < st_hi && inflight < NST) issue();
+        if (pend.on) {
+            finish_split<T, D, R>(p, pend.seq, pend.kvh, pend.grp, pend.G, pend.K, pend.r0, pend.nrows,
+                                  pend.tok0, lane);
+            pend.on = false;
+        }
+        // A fragments of the query rows (rows >= nrows and 8..15 zero): channels 16 ks + 2c, +1 and
+        // 16 ks + 8 + 2c, +1 of row g
+        uint32_t qa[8][2];
+        {
+            const T *qp = nullptr;
+            if (g < nrows) {
+                const int row = r0 + g;
+                const int j = row / p.group, hh = row - j * p.group;
+                qp = reinterpret_cast<const T *>(p.q) + ((tok0 + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D;
+            }
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qa[ks][0] = qp ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * ks + 2 * c4)) : 0u;
+                qa[ks][1] = qp ? __ldg(reinterpret_cast<const uint32_t *>(qp + 16 * ks + 8 + 2 * c4)) : 0u;
+            }
+        }
+
+        for (int st = st_lo; st < st_hi; ++st) {
+            if (!mbar_wait(&bars[slot_c], phase_c)) {
+                timed_out = true;
+                break;
+            }
+            unsigned char *sk = ring + (size_t)slot_c * S::kBytes;
+            unsigned char *sv = sk + S::kK;
+            const int p0 = st * kStageTokens;
+            // V rows past the last key any row sees hold stale or unread data (possibly NaN): zero
+            // them, so that P = 0 times them stays 0 in the MMA
+            if (p0 + kStageTokens - 1 > Pmax) {
+                const int first = Pmax - p0 + 1;           // >= 1
+                for (int i = lane; i < (kStageTokens - first) * (S::kRow / 16); i += 32) {
+                    const int key = first + i / (S::kRow / 16), ch = i % (S::kRow / 16);
+                    *reinterpret_cast<uint4 *>(sv + (ch >> 3) * S::kPanelBytes + key * 128 + ((ch & 7) << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            // S = Q K^T: n-block 0 = keys 0..7, n-block 1 = keys 8..15 of the stage
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const uint32_t kbase = smem_addr(sk);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int q = 2 * ks + kch;                    // 16-byte chunk of the key row
+                const uint32_t addr = kbase + (q >> 3) * S::kPanelBytes + kkey * 128 + (((q & 7) ^ (kkey & 7)) << 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(addr, b0, b1, b2, b3);
+                mma_rows8<T>(sc[0], qa[ks][0], qa[ks][1], b0, b1);
+                mma_rows8<T>(sc[1], qa[ks][0], qa[ks][1], b2, b3);
+            }
+            // scores of keys 8 nb + 2c + e of row g, in log2 units, causally masked
+            float z[2][2];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nb2 = 0; nb2 < 2; ++nb2)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = 8 * nb2 + 2 * c4 + e;
+                    z[nb2][e] = (p0 + key <= Pmine) ? sc[nb2][e] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, z[nb2][e]);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mnew = fmaxf(m, mx);
+            const float mref = (mnew == -INFINITY) ? 0.f : mnew;
+            const float alpha = fast_exp2(m - mref);
+            float pe[2][2];
+#pragma unroll
+            for (int nb2 = 0; nb2 < 2; ++nb2)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) pe[nb2][e] = fast_exp2(z[nb2][e] - mref);
+            lsum = lsum * alpha + ((pe[0][0] + pe[0][1]) + (pe[1][0] + pe[1][1]));
+            m = mnew;
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    o[i][0] *= alpha;
+                    o[i][1] *= alpha;
+                }
+            }
+            // O += P V: P as the A operand (keys 2c, 2c+1 and 8 + 2c, +1 of row g), V by ldmatrix.trans
+            const uint32_t pa0 = pack16<T>(pe[0][0], pe[0][1]), pa2 = pack16<T>(pe[1][0], pe[1][1]);
+            const uint32_t vbase = smem_addr(sv);
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                const int q = 2 * np + vch;
+                const uint32_t addr = vbase + (q >> 3) * S::kPanelBytes + vkey * 128 + (((q & 7) ^ (vkey & 7)) << 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(addr, b0, b1, b2, b3);
+                mma_rows8<T>(o[2 * np], pa0, pa2, b0, b1);
+                mma_rows8<T>(o[2 * np + 1], pa0, pa2, b2, b3);
+            }
+            __syncwarp();
+            slot_c = slot_c + 1 == NST ? 0 : slot_c + 1;
+            phase_c ^= slot_c == 0 ? 1u : 0u;
+            --inflight;
+            if (st_issue < st_hi) issue();
+        }
+
+        if (timed_out) {
+            if (lane == 0) report(p.status, PA_DEV_TIMEOUT);
+            while (inflight > 0) {
+                mbar_wait(&bars[slot_c], phase_c);
+                slot_c = slot_c + 1 == NST ? 0 : slot_c + 1;
+                phase_c ^= slot_c == 0 ? 1u : 0u;
+                --inflight;
+            }
+            return;
+        }
+
+        // row g's sum over the four lanes of the row; lane (g, c) holds columns 8 i + 2c, +1
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+        if (g < nrows) {
+            const int row = r0 + g;
+            if (K == 1) {
+                const int j = row / p.group, hh = row - j * p.group;
+                const float inv = 1.f / lsum;
+                T *op = reinterpret_cast<T *>(p.out) + ((tok0 + j) * p.q_heads + (int64_t)kvh * p.group + hh) * D;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    *reinterpret_cast<uint32_t *>(op + 8 * i + 2 * c4) = pack16<T>(o[i][0] * inv, o[i][1] * inv);
+            } else {
+                const int64_t part = (int64_t)__ldg(p.parts_cu + seq) + local;
+                float *po = p.parts_o + (part * R + g) * D;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    *reinterpret_cast<float2 *>(po + 8 * i + 2 * c4) = make_float2(o[i][0], o[i][1]);
+                if (c4 == 0) p.parts_ml[part * R + g] = make_float2(m, lsum);
+            }
+        }
+        if (K > 1) pend = PendingSplit{seq, kvh, grp, G, K, r0, nrows, tok0, true};
+    }
+    if (pend.on)
+        finish_split<T, D, R>(p, pend.seq, pend.kvh, pend.grp, pend.G, pend.K, pend.r0, pend.nrows, pend.tok0,
+                              lane);
+}
+
+template <typename T, int R>
+cudaError_t launch_gqa_mma_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s) {
+    constexpr int D = 128;
+    SimtParams p = p0;
+    using S = GqaStage<T, D>;
+    // K and V as [num_blocks][Hkv * B rows][D]; one TMA box = one 128-byte panel of 16 rows
+    CUtensorMap kmap, vmap;
+    const uint64_t es = sizeof(T);
+    if (!make_map_3d(&kmap, a.dims.dtype, a.k, D, (uint64_t)a.dims.num_kv_heads * a.dims.block_size,
+                     a.dims.num_blocks, D * es, (uint64_t)p.block_stride * es, (uint32_t)(128 / es), kStageTokens, 1) ||
+        !make_map_3d(&vmap, a.dims.dtype, a.v, D, (uint64_t)a.dims.num_kv_heads * a.dims.block_size,
+                     a.dims.num_blocks, D * es, (uint64_t)p.block_stride * es, (uint32_t)(128 / es), kStageTokens, 1))
+        return cudaErrorInvalidValue;
+    const int nst = 3, warps = kSimtMaxWarps;
+    p.nst = nst;
+    p.bar_bytes = 0;
+    const size_t smem = 1024 + (size_t)warps * nst * (S::kBytes + sizeof(uint64_t));
+    auto kern = gqa_mma_kernel<T, R>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<a.num_sms, warps * 32, smem, s>>>(kmap, vmap, p);
+    return cudaGetLastError();
+}
+
 template <typename T, typename TK, int D, int R>
 cudaError_t launch_simt_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s) {
     SimtParams p = p0;
@@ -1108,10 +1426,16 @@ cudaError_t launch_gqa_t(const FwdArgs &a, const SimtParams &p0, cudaStream_t s)
 
 template <typename T, typename TK, int D>
 cudaError_t launch_simt_rows(const FwdArgs &a, const SimtParams &p, cudaStream_t s) {
+    // GQA rows of 16-bit caches with head_dim 128 run on tensor cores
+    constexpr bool kMma = std::is_same<T, TK>::value && sizeof(T) == 2 && D == 128;
     switch (a.lay.rows_per_item) {
     case 1: return launch_simt_t<T, TK, D, 1>(a, p, s);
-    case 2: return launch_gqa_t<T, TK, D, 2>(a, p, s);
-    default: return launch_gqa_t<T, TK, D, 4>(a, p, s);
+    case 2:
+        if constexpr (kMma) return launch_gqa_mma_t<T, 2>(a, p, s);
+        else return launch_gqa_t<T, TK, D, 2>(a, p, s);
+    default:
+        if constexpr (kMma) return launch_gqa_mma_t<T, 4>(a, p, s);
+        else return launch_gqa_t<T, TK, D, 4>(a, p, s);
     }
 }
 
