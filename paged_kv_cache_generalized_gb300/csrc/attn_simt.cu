@@ -14,11 +14,12 @@
 // share it, and a range of KV blocks).  The warp streams its K/V through a private ring of
 // shared-memory stages filled by asynchronous copies with mbarrier completion, so each SM keeps
 // ~200 KB of HBM reads in flight.  Work items are taken from a global counter (persistent grid).
-// Two kernels: simt_attention_kernel for one query row per KV head (MHA decode; half-warps take
-// alternate keys, each lane holds d/16 dimensions, reductions are warp shuffles, one bulk copy per
-// 16-token run of a (block, head)), and simt_gqa_kernel for 2 or 4 rows (below).  Both read K/V
-// caches of the query's dtype or of one-byte E4M3 codes (the scales fold into the query scale
-// and into o).  On E4M3 caches the one-row kernel converts the codes to f16 pairs in hardware and
+// Three kernels: simt_attention_kernel for one query row per KV head (MHA decode; half-warps
+// take alternate keys, each lane holds d/16 dimensions, reductions are warp shuffles, one bulk
+// copy per 16-token run of a (block, head)), simt_gqa_kernel for 2 or 4 rows (below), and
+// gqa_mma_kernel, which takes those GQA rows instead for 16-bit caches with head_dim 128
+// (tensor-core fragments).  The CUDA-core kernels read K/V caches of the query's dtype or of
+// one-byte E4M3 codes (the scales fold into the query scale and into o).  On E4M3 caches the one-row kernel converts the codes to f16 pairs in hardware and
 // feeds them, with an f16 copy of the query (scaled by a power of two) or of P, to mixed-precision
 // FMAs with fp32 accumulators: no f16 -> fp32 widening per element.
 #include <math.h>
