@@ -311,7 +311,7 @@ size_t pa_kitty_workspace_size(const pa_kitty_dims *dims);
  * Workspace: pa_kitty_workspace_size(dims) bytes, 256-byte aligned, contents clobbered.
  * q_lens[i] != 1, ctx_lens[i] < 0 or n_i > max_pages_per_seq * 128 -> that sequence's rows are
  * not written, PA_DEV_BAD_LENGTHS; a page or residual id outside its pool -> that page is
- * skipped, PA_DEV_BAD_BLOCK_ID.  num_seqs <= 8192. */
+ * skipped, PA_DEV_BAD_BLOCK_ID.  num_seqs <= 4096. */
 pa_status pa_forward_kitty(const pa_kitty_dims *dims, const void *q, const void *pages,
                            const void *res_k, const void *res_v, const int32_t *block_tables,
                            const int32_t *ctx_lens, const int32_t *q_lens, float scale, void *out,

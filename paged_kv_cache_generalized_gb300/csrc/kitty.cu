@@ -10,10 +10,12 @@
 // bits meet in one word through shuffles, high bits through shared-memory ORs.  V: one warp per
 // token, a lane per 4 channels, min/max by shuffles.
 //
-// kitty_decode_kernel: persistent, 8 warps per CTA, one CTA per SM.  Phase 1 streams the
-// quantised pages: a work item is (sequence, query head, up to kChunkPages pages); each warp runs
-// a 2-stage ring of whole (page, KV head) records filled by bulk copies with mbarrier completion,
-// and claims its next item while the current one computes, so the ring runs across items.  Per
+// kitty_decode_kernel: persistent, 16 warps per CTA (128 registers each), one CTA per SM.  Phase 1
+// streams the quantised pages: a work item is (sequence, query head, up to kChunkPages pages);
+// each warp runs a 2-stage ring of half pages (64 keys of one (page, KV head) record: the half's
+// codes, V scales and minimums, and on the first half the K scales, minimums and promoted ids),
+// filled by bulk copies with mbarrier completion, and claims its next item while the current one
+// computes, so the ring runs across items.  The a_x pairs sit in the warp's shared scratch.  Per
 // page the warp folds each channel's scale into the query (a_x = scale * q_x * s_x, and
 // b = scale * sum_x q_x min_x), so a key's score is b + sum_x a_x code_x.  The codes are never
 // unpacked: masking a 2-bit field of a 32-bit word in place leaves, in each 16-bit half, an f16
@@ -39,14 +41,20 @@ constexpr int kDim = 128;
 constexpr int kOffKs = 0, kOffKm = 512, kOffVs = 1024, kOffVm = 1536, kOffPid = 2048, kOffKlo = 2080;
 constexpr int kOffKhi = kOffKlo + 32 * kPageTokens;               // 6176
 constexpr int kChunkPages = 8;                                    // pages per decode work item
-constexpr int kDecWarps = 8;
+constexpr int kDecWarps = 16;
 constexpr int kStages = 2;
 constexpr int kPartFloats = 132;                                  // m, l, 2 pad, o[128]
-constexpr int kMaxSeqs = 8192;
+constexpr int kMaxSeqs = 4096;
 constexpr int kScratchBytes = 512 + 64 * 4 + 16 * 4;              // a_x fp32, f16 pairs lo, hi
 
 __host__ __device__ constexpr int record_bytes(int P) { return 10272 + 32 * P; }
 __host__ __device__ constexpr int off_vc(int P) { return kOffKhi + 32 * P; }
+// A decode ring stage holds half a page (64 keys) of one record: K scales and minimums and the
+// promoted ids (first half only), then the half's V scales, V minimums, K low bits, K high bits
+// and V codes.
+constexpr int kHsKs = 0, kHsKm = 512, kHsVs = 1024, kHsVm = 1280, kHsPid = 1536, kHsKlo = 1568, kHsKhi = 3616;
+__host__ __device__ constexpr int hs_vc(int P) { return kHsKhi + 16 * P; }
+__host__ __device__ constexpr int half_stage_bytes(int P) { return hs_vc(P) + 2048; }
 
 // ---- quantiser ---------------------------------------------------------------------------------
 struct QuantParams {
@@ -410,25 +418,31 @@ __device__ void tail_items(const DecParams &p, int lane) {
     }
 }
 
+// 16-byte shared-memory load kept in place (volatile), so that the compiler does not hoist the
+// a_x pairs of every word into registers across the passes.
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
+}
+
 // Shared memory of the decode kernel: per warp kStages records and a scratch area, the ring's
 // mbarriers, then the per-sequence item prefix.
 __host__ __device__ constexpr size_t dec_smem_bytes(int P, int num_seqs) {
-    return (size_t)kDecWarps * (kStages * record_bytes(P) + kScratchBytes) + kDecWarps * kStages * 8 +
+    return (size_t)kDecWarps * (kStages * half_stage_bytes(P) + kScratchBytes) + kDecWarps * kStages * 8 +
            (size_t)(num_seqs + 1) * 4;
 }
 
 template <typename T, int P>
 __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecParams p) {
     constexpr int REC = record_bytes(P);
-    constexpr int kHiPairs = P / 2;                   // f16 pairs of promoted slots
+    constexpr int HS = half_stage_bytes(P);
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_part[kDecWarps * 32];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    unsigned char *ring = smem + (size_t)warp * kStages * REC;
-    unsigned char *scratch = smem + (size_t)kDecWarps * kStages * REC + warp * kScratchBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kDecWarps * (kStages * REC + kScratchBytes)) +
+    unsigned char *ring = smem + (size_t)warp * kStages * HS;
+    unsigned char *scratch = smem + (size_t)kDecWarps * kStages * HS + warp * kScratchBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kDecWarps * (kStages * HS + kScratchBytes)) +
                      warp * kStages;
-    int *s_cu = reinterpret_cast<int *>(smem + (size_t)kDecWarps * (kStages * REC + kScratchBytes) +
+    int *s_cu = reinterpret_cast<int *>(smem + (size_t)kDecWarps * (kStages * HS + kScratchBytes) +
                                         kDecWarps * kStages * 8);
     float *s_a = reinterpret_cast<float *>(scratch);                       // a_x, fp32
     uint16_t *s_lo = reinterpret_cast<uint16_t *>(scratch + 512);          // 64 f16 pairs
@@ -486,19 +500,19 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
     // page streaming of the even warps; every warp then streams pages, then takes what is left
     if (warp & 1) tail_items<T>(p, lane);
 
-    // ---- phase 1: quantised pages ----
+    // ---- phase 1: quantised pages, streamed as half pages ----
     Item cur = claim_quant(p, s_cu, lane), nxt;
     nxt.valid = false;
     bool have_nxt = false, iss_nxt = false, dead = false;
-    int iss_pg = cur.p0;
+    int iss_pg = cur.p0, iss_h = 0;
     uint32_t issued = 0, done = 0;
 
     auto page_id = [&](const Item &it, int pg) -> int64_t {
         const int32_t id = __ldg(p.bt + (int64_t)it.seq * p.max_pages + pg);
         return (id < 0 || id >= p.num_pages) ? -1 : id;
     };
-    // Issues the copy of the next page (of the current item, else of the next one, which it
-    // claims when needed); false when there is nothing to issue.
+    // Issues the copies of the next half page (of the current item, else of the next one, which
+    // it claims when needed); false when there is nothing to issue.
     auto issue = [&]() -> bool {
         if (!cur.valid) return false;
         if (iss_pg >= (iss_nxt ? nxt.p1 : cur.p1)) {
@@ -510,18 +524,33 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
             if (!nxt.valid) return false;
             iss_nxt = true;
             iss_pg = nxt.p0;
+            iss_h = 0;
         }
         const Item &it = iss_nxt ? nxt : cur;
         int64_t id = page_id(it, iss_pg);
         if (id < 0) id = 0;      // a bad id still fills the stage (the ring stays in step); compute skips it
         const int slot = issued % kStages;
         if (lane == 0) {
+            const uint8_t *rec = p.pages + ((size_t)id * p.kv_heads + it.kvh) * REC;
+            unsigned char *dst = ring + slot * HS;
+            const uint32_t bytes = (iss_h == 0 ? 1056u : 0u) + 512u + 2048u + 16u * P + 2048u;
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&bars[slot], REC);
-            bulk_g2s(ring + slot * REC, p.pages + ((size_t)id * p.kv_heads + it.kvh) * REC, REC, &bars[slot]);
+            mbar_arrive_expect_tx(&bars[slot], bytes);
+            if (iss_h == 0) {
+                bulk_g2s(dst + kHsKs, rec + kOffKs, 1024, &bars[slot]);          // K scales, minimums
+                bulk_g2s(dst + kHsPid, rec + kOffPid, 32, &bars[slot]);
+            }
+            bulk_g2s(dst + kHsVs, rec + kOffVs + 256 * iss_h, 256, &bars[slot]);
+            bulk_g2s(dst + kHsVm, rec + kOffVm + 256 * iss_h, 256, &bars[slot]);
+            bulk_g2s(dst + kHsKlo, rec + kOffKlo + 2048 * iss_h, 2048, &bars[slot]);
+            bulk_g2s(dst + kHsKhi, rec + kOffKhi + 16 * P * iss_h, 16 * P, &bars[slot]);
+            bulk_g2s(dst + hs_vc(P), rec + off_vc(P) + 2048 * iss_h, 2048, &bars[slot]);
         }
         ++issued;
-        ++iss_pg;
+        if (++iss_h == 2) {
+            iss_h = 0;
+            ++iss_pg;
+        }
         return true;
     };
 
@@ -539,140 +568,145 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
         for (int i = 0; i < 16; ++i) o[i] = 0.f;
         int F_cur = 0;
         bool have_F = false;
+        float b = 0.f, zmul = 0.f;                  // of the current page, set by its first half
 
-        for (int pg = cur.p0; pg < cur.p1; ++pg) {
-            const int slot = done % kStages;
-            if (!mbar_wait(&bars[slot], (done / kStages) & 1u)) {
-                report(p.status, PA_DEV_TIMEOUT);
-                dead = true;
-                break;
-            }
-            const unsigned char *st = ring + slot * REC;
-            if (page_id(cur, pg) < 0) {
-                if (lane == 0) report(p.status, PA_DEV_BAD_BLOCK_ID);
-            } else {
-                // page prologue: a_x = scale q_x s_x, b = scale sum_x q_x min_x; f16 pairs of a_x
-                // scaled by 2^(E - 2 (x % 4)), E putting max |a| in [2^12, 2^13)
-                const float4 ks = reinterpret_cast<const float4 *>(st + kOffKs)[lane];
-                const float4 km = reinterpret_cast<const float4 *>(st + kOffKm)[lane];
-                const float a[4] = {qs[0] * ks.x, qs[1] * ks.y, qs[2] * ks.z, qs[3] * ks.w};
-                const float b = wsum(qs[0] * km.x + qs[1] * km.y + qs[2] * km.z + qs[3] * km.w);
-                const float amax = warp_max(fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3]))));
-                const int E = amax > 0.f ? max(-100, min(100, 12 - exponent_of(amax))) : 0;
+        for (int pg = cur.p0; pg < cur.p1 && !dead; ++pg) {
+            const bool page_ok = page_id(cur, pg) >= 0;
+            if (!page_ok && lane == 0) report(p.status, PA_DEV_BAD_BLOCK_ID);
+            for (int hh = 0; hh < 2; ++hh) {
+                const int slot = done % kStages;
+                if (!mbar_wait(&bars[slot], (done / kStages) & 1u)) {
+                    report(p.status, PA_DEV_TIMEOUT);
+                    dead = true;
+                    break;
+                }
+                const unsigned char *st = ring + slot * HS;
+                if (page_ok) {
+                    if (hh == 0) {
+                        // page prologue: a_x = scale q_x s_x, b = scale sum_x q_x min_x; f16 pairs
+                        // of a_x scaled by 2^(E - 2 (x % 4)), E putting max |a| in [2^12, 2^13)
+                        const float4 ks = reinterpret_cast<const float4 *>(st + kHsKs)[lane];
+                        const float4 km = reinterpret_cast<const float4 *>(st + kHsKm)[lane];
+                        const float a[4] = {qs[0] * ks.x, qs[1] * ks.y, qs[2] * ks.z, qs[3] * ks.w};
+                        b = wsum(qs[0] * km.x + qs[1] * km.y + qs[2] * km.z + qs[3] * km.w);
+                        const float amax =
+                            warp_max(fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3]))));
+                        const int E = amax > 0.f ? max(-100, min(100, 12 - exponent_of(amax))) : 0;
+                        __syncwarp();                     // the previous page's pairs are read
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int x = 4 * lane + e;
-                    s_a[x] = a[e];
-                    s_lo[((x >> 4) * 8 + (x & 7)) * 2 + ((x >> 3) & 1)] = f16_from_f32(a[e] * pow2f(E - 2 * e));
-                }
-                __syncwarp();
-                if (lane < P) {
-                    const int x = st[kOffPid + lane];
-                    s_hi[((lane >> 4) * 8 + (lane & 7)) * 2 + ((lane >> 3) & 1)] =
-                        f16_from_f32(4.f * s_a[x] * pow2f(E - 2 * (lane & 3)));
-                }
-                __syncwarp();
-                uint32_t alo[64], ahi[kHiPairs];
+                        for (int e = 0; e < 4; ++e) {
+                            const int x = 4 * lane + e;
+                            s_a[x] = a[e];
+                            s_lo[((x >> 4) * 8 + (x & 7)) * 2 + ((x >> 3) & 1)] = f16_from_f32(a[e] * pow2f(E - 2 * e));
+                        }
+                        __syncwarp();
+                        if (lane < P) {
+                            const int x = st[kHsPid + lane];
+                            s_hi[((lane >> 4) * 8 + (lane & 7)) * 2 + ((lane >> 3) & 1)] =
+                                f16_from_f32(4.f * s_a[x] * pow2f(E - 2 * (lane & 3)));
+                        }
+                        __syncwarp();
+                        zmul = pow2f(24 - E);
+                    }
+                    // V: F puts this half's largest token scale in [2^14, 2^15); o is kept in units of 2^F
+                    const float *vsc = reinterpret_cast<const float *>(st + kHsVs);
+                    const float *vmn = reinterpret_cast<const float *>(st + kHsVm);
+                    const float vmax = warp_max(fmaxf(vsc[lane], vsc[lane + 32]));
+                    const int F = vmax > 0.f ? max(-60, min(60, 14 - exponent_of(vmax))) : 0;
+                    if (!have_F) {
+                        F_cur = F;
+                        have_F = true;
+                    } else if (F != F_cur) {
+                        const float r = pow2f(F - F_cur);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const uint4 w = reinterpret_cast<const uint4 *>(s_lo)[i];
-                    alo[4 * i] = w.x, alo[4 * i + 1] = w.y, alo[4 * i + 2] = w.z, alo[4 * i + 3] = w.w;
-                }
-#pragma unroll
-                for (int i = 0; i < kHiPairs / 4; ++i) {
-                    const uint4 w = reinterpret_cast<const uint4 *>(s_hi)[i];
-                    ahi[4 * i] = w.x, ahi[4 * i + 1] = w.y, ahi[4 * i + 2] = w.z, ahi[4 * i + 3] = w.w;
-                }
-                const float zmul = pow2f(24 - E);
-                // V: F puts the largest token scale in [2^14, 2^15); o is kept in units of 2^F
-                const float4 vs4 = reinterpret_cast<const float4 *>(st + kOffVs)[lane];
-                const float vmax = warp_max(fmaxf(fmaxf(vs4.x, vs4.y), fmaxf(vs4.z, vs4.w)));
-                const int F = vmax > 0.f ? max(-60, min(60, 14 - exponent_of(vmax))) : 0;
-                if (!have_F) {
-                    F_cur = F;
-                    have_F = true;
-                } else if (F != F_cur) {
-                    const float r = pow2f(F - F_cur);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] *= r;
-                    F_cur = F;
-                }
-                const float psc = pow2f(F_cur);
-                const int u = lane >> 3, wv = lane & 7;
+                        for (int i = 0; i < 16; ++i) o[i] *= r;
+                        F_cur = F;
+                    }
+                    const float psc = pow2f(F_cur);
+                    const int u = lane >> 3, wv = lane & 7;
+                    const uint32_t s_lo_a = smem_addr(s_lo), s_hi_a = smem_addr(s_hi);
 
 #pragma unroll 1
-                for (int pass = 0; pass < kPageTokens / 32; ++pass) {
-                    const int t = pass * 32 + lane;
-                    // QK^T, one key per lane
-                    const uint4 *kl = reinterpret_cast<const uint4 *>(st + kOffKlo + t * 32);
-                    const uint4 w0 = kl[0], w1 = kl[1];
-                    const uint32_t kw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                    uint32_t hw[P / 16];
-                    if constexpr (P == 32) {
-                        const uint2 h2 = *reinterpret_cast<const uint2 *>(st + kOffKhi + t * 8);
-                        hw[0] = h2.x;
-                        hw[1] = h2.y;
-                    } else {
-                        hw[0] = *reinterpret_cast<const uint32_t *>(st + kOffKhi + t * 4);
-                    }
-                    float acc[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-#pragma unroll
-                    for (int wd = 0; wd < 8; ++wd) {
-                        const uint32_t x = kw[wd], y = x >> 8;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            fma_h2(alo[wd * 8 + j], x & (0x00030003u << (2 * j)), acc[2 * j], acc[2 * j + 1]);
-                            fma_h2(alo[wd * 8 + 4 + j], y & (0x00030003u << (2 * j)), acc[8 + 2 * j], acc[9 + 2 * j]);
+                    for (int pass = 0; pass < 2; ++pass) {
+                        const int t = pass * 32 + lane;
+                        // QK^T, one key per lane; the a_x pairs come from shared memory (broadcast)
+                        const uint4 *kl = reinterpret_cast<const uint4 *>(st + kHsKlo + t * 32);
+                        const uint4 w0 = kl[0], w1 = kl[1];
+                        const uint32_t kw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        uint32_t hw[P / 16];
+                        if constexpr (P == 32) {
+                            const uint2 h2 = *reinterpret_cast<const uint2 *>(st + kHsKhi + t * 8);
+                            hw[0] = h2.x;
+                            hw[1] = h2.y;
+                        } else {
+                            hw[0] = *reinterpret_cast<const uint32_t *>(st + kHsKhi + t * 4);
                         }
-                    }
+                        float acc[16];
 #pragma unroll
-                    for (int wd = 0; wd < P / 16; ++wd) {
-                        const uint32_t x = hw[wd], y = x >> 8;
+                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            fma_h2(ahi[wd * 8 + j], x & (0x00030003u << (2 * j)), acc[2 * j], acc[2 * j + 1]);
-                            fma_h2(ahi[wd * 8 + 4 + j], y & (0x00030003u << (2 * j)), acc[8 + 2 * j], acc[9 + 2 * j]);
+                        for (int wd = 0; wd < 8; ++wd) {
+                            uint32_t ap[8];
+                            lds128(s_lo_a + wd * 32, ap[0], ap[1], ap[2], ap[3]);
+                            lds128(s_lo_a + wd * 32 + 16, ap[4], ap[5], ap[6], ap[7]);
+                            const uint32_t x = kw[wd], y = x >> 8;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                fma_h2(ap[j], x & (0x00030003u << (2 * j)), acc[2 * j], acc[2 * j + 1]);
+                                fma_h2(ap[4 + j], y & (0x00030003u << (2 * j)), acc[8 + 2 * j], acc[9 + 2 * j]);
+                            }
                         }
-                    }
 #pragma unroll
-                    for (int i = 8; i > 0; i >>= 1)
+                        for (int wd = 0; wd < P / 16; ++wd) {
+                            uint32_t ap[8];
+                            lds128(s_hi_a + wd * 32, ap[0], ap[1], ap[2], ap[3]);
+                            lds128(s_hi_a + wd * 32 + 16, ap[4], ap[5], ap[6], ap[7]);
+                            const uint32_t x = hw[wd], y = x >> 8;
 #pragma unroll
-                        for (int k = 0; k < i; ++k) acc[k] += acc[k + i];
-                    const float z = fmaf(acc[0], zmul, b);
-                    // online softmax
-                    const float mloc = warp_max(z);
-                    if (mloc > m_run) {
-                        const float al = fast_exp2(m_run - mloc);
-                        l_l *= al;
-                        bv_l *= al;
+                            for (int j = 0; j < 4; ++j) {
+                                fma_h2(ap[j], x & (0x00030003u << (2 * j)), acc[2 * j], acc[2 * j + 1]);
+                                fma_h2(ap[4 + j], y & (0x00030003u << (2 * j)), acc[8 + 2 * j], acc[9 + 2 * j]);
+                            }
+                        }
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] *= al;
-                        m_run = mloc;
-                    }
-                    const float pz = fast_exp2(z - m_run);
-                    l_l += pz;
-                    bv_l = fmaf(pz, reinterpret_cast<const float *>(st + kOffVm)[t], bv_l);
-                    const uint32_t ph = f16_from_f32(pz * reinterpret_cast<const float *>(st + kOffVs)[t] * psc);
-                    // PV: lane (u, wv) takes word wv (channels 16 wv .. 16 wv + 15) of keys 4 i + u
+                        for (int i = 8; i > 0; i >>= 1)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int tok = 4 * i + u;
-                        const uint16_t pt = (uint16_t)__shfl_sync(0xffffffffu, ph, tok);
-                        const uint32_t x = *reinterpret_cast<const uint32_t *>(st + off_vc(P) + (pass * 32 + tok) * 32 + wv * 4);
-                        const uint32_t y = x >> 8;
+                            for (int k = 0; k < i; ++k) acc[k] += acc[k + i];
+                        const float z = fmaf(acc[0], zmul, b);
+                        // online softmax
+                        const float mloc = warp_max(z);
+                        if (mloc > m_run) {
+                            const float al = fast_exp2(m_run - mloc);
+                            l_l *= al;
+                            bv_l *= al;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            fma_h2s(x & (0x00030003u << (2 * j)), pt, o[2 * j], o[2 * j + 1]);
-                            fma_h2s(y & (0x00030003u << (2 * j)), pt, o[8 + 2 * j], o[9 + 2 * j]);
+                            for (int i = 0; i < 16; ++i) o[i] *= al;
+                            m_run = mloc;
+                        }
+                        const float pz = fast_exp2(z - m_run);
+                        l_l += pz;
+                        bv_l = fmaf(pz, vmn[t], bv_l);
+                        const uint32_t ph = f16_from_f32(pz * vsc[t] * psc);
+                        // PV: lane (u, wv) takes word wv (channels 16 wv .. 16 wv + 15) of keys 4 i + u
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int tok = 4 * i + u;
+                            const uint16_t pt = (uint16_t)__shfl_sync(0xffffffffu, ph, tok);
+                            const uint32_t x =
+                                *reinterpret_cast<const uint32_t *>(st + hs_vc(P) + (pass * 32 + tok) * 32 + wv * 4);
+                            const uint32_t y = x >> 8;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                fma_h2s(x & (0x00030003u << (2 * j)), pt, o[2 * j], o[2 * j + 1]);
+                                fma_h2s(y & (0x00030003u << (2 * j)), pt, o[8 + 2 * j], o[9 + 2 * j]);
+                            }
                         }
                     }
                 }
+                __syncwarp();
+                ++done;
+                issue();
             }
-            __syncwarp();
-            ++done;
-            issue();
         }
         if (dead) break;
 
@@ -721,8 +755,12 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
         }
         cur = nxt;
         have_nxt = false;
-        if (iss_nxt) iss_nxt = false;
-        else iss_pg = cur.p0;
+        if (iss_nxt) {
+            iss_nxt = false;
+        } else {
+            iss_pg = cur.p0;
+            iss_h = 0;
+        }
         while (issued - done < kStages && issue()) {
         }
     }

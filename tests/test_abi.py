@@ -177,7 +177,7 @@ def test_kitty_record_and_workspace_sizes_are_host_only(lib):
     # quantised pages' and the residual page's)
     assert ws >= 4 * 8 * 2 * 132 * 4
     for bad in (dict(promoted=24), dict(head_dim=64), dict(num_q_heads=7), dict(dtype=0),
-                dict(num_seqs=0), dict(num_seqs=8193), dict(max_pages_per_seq=0), dict(num_pages=-1)):
+                dict(num_seqs=0), dict(num_seqs=4097), dict(max_pages_per_seq=0), dict(num_pages=-1)):
         assert lib.pa_kitty_workspace_size(ctypes.byref(_kdims(**bad))) == 0, bad
 
 
