@@ -424,8 +424,8 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t &a, uint32_t &b, 
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
 }
 
-// Shared memory of the decode kernel: per warp kStages records and a scratch area, the ring's
-// mbarriers, then the per-sequence item prefix.
+// Shared memory of the decode kernel: per warp kStages half-page stages and a scratch area, the
+// ring's mbarriers, then the per-sequence item prefix.
 __host__ __device__ constexpr size_t dec_smem_bytes(int P, int num_seqs) {
     return (size_t)kDecWarps * (kStages * half_stage_bytes(P) + kScratchBytes) + kDecWarps * kStages * 8 +
            (size_t)(num_seqs + 1) * 4;
