@@ -25,8 +25,8 @@
 // of every fourth key, and P * s_t (rounded to f16) meets the V codes the same way; the V minimum
 // contributes sum_t p_t min_t.  Phase 2 runs each sequence's residual page (fewer than 128
 // unquantised tokens) as one more item with plain loads.  Items of one row merge by the
-// logsumexp rule: the last split to finish reads the others' (m, l, o) records through L2.  Odd
-// warps take residual items before pages, so that their loads overlap the others' streaming.
+// logsumexp rule: the last split to finish reads the others' (m, l, o) records through L2.  Every
+// warp streams pages first and takes residual items when no page item is left.
 #include <math.h>
 #include <stdint.h>
 
@@ -496,9 +496,6 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
         __syncthreads();
     }
 
-    // odd warps take residual-page items first, so that their latency-bound loads overlap the
-    // page streaming of the even warps; every warp then streams pages, then takes what is left
-    if (warp & 1) tail_items<T>(p, lane);
 
     // ---- phase 1: quantised pages, streamed as half pages ----
     Item cur = claim_quant(p, s_cu, lane), nxt;
