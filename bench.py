@@ -333,7 +333,8 @@ class KittyStep:
         self.pool = self.pages
         self.out = torch.empty_like(self.dev_in["q"])
         self.out_host = torch.empty_like(self.host["q"]).pin_memory()
-        self.ws = torch.empty(1 << 26, dtype=torch.uint8, device=dev)
+        need = pkg.kitty_workspace_size(self.dev_in["q"], self.pages, self.res_k, self.dev_in["bt"], P)
+        self.ws = torch.empty(max(256, need), dtype=torch.uint8, device=dev)
         es = 2
         self.bytes_attn = float((nfull * Hkv * R).sum() + (tail * Hkv * d * es * 2).sum()
                                 + 2 * S * Hq * d * es + ((n + T - 1) // T).sum() * 4 + S * 8)

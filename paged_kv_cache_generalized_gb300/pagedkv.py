@@ -262,6 +262,13 @@ def kv_quantize_pages(res_k, res_v, pairs, pages, promoted, stream=None):
     return pages
 
 
+def kitty_workspace_size(q, pages, res_k, block_tables, promoted) -> int:
+    """Workspace bytes pa_forward_kitty needs for these shapes (0 if unsupported)."""
+    dims = kitty_dims(q, pages, promoted, num_q_heads=q.shape[1], num_seqs=q.shape[0], res_pages=res_k,
+                      max_pages_per_seq=block_tables.shape[1])
+    return int(load_library().pa_kitty_workspace_size(ctypes.byref(dims)))
+
+
 def pa_forward_kitty(q, pages, res_k, res_v, block_tables, ctx_lens, q_lens, promoted, scale=None,
                      out=None, workspace=None, stream=None):
     """Decode attention over 2-bit pages with promoted 4-bit key channels plus each sequence's
