@@ -95,7 +95,9 @@ typedef enum { PA_KV_SAME = 0, PA_KV_E4M3 = 1 } pa_kv_dtype;
  * tensor-core kernel needs both MMA operands of one type).
  * Sequences with q_len * g >= 16 query rows per KV head run on the tcgen05 tensor-core kernel when
  * the dtype is bf16/f16, d = 128, g divides 128 and scale > 0; decode steps, short turns and
- * everything else run on the CUDA-core split-KV kernel.
+ * everything else run on the split-KV decode kernels: 2-4 query rows per KV head of bf16/f16
+ * caches with d = 128 as mma.m16n8k16 tensor-core fragments (P rounded to the 16-bit type before
+ * P V), one row per KV head, E4M3 caches, fp32 and d = 64 on CUDA cores.
  * Streams: when some sequence takes the tensor-core kernel, that kernel runs on a library-owned
  * high-priority stream of the current device, forked from `stream` after the planner and joined
  * back before the call's last kernel, so that the CUDA-core work fills the SMs it leaves.  To the
