@@ -294,7 +294,8 @@ size_t pa_kitty_record_bytes(int32_t head_dim, int32_t promoted);
  * quantise the 128 tokens of residual page s (res_k / res_v [s][h]) into record t of `pages`, by
  * the rules above (bit-exact: same bytes on every run).  pairs is int64 device memory; ids
  * outside [0, num_res_pages) / [0, num_pages) are skipped and flagged PA_DEV_BAD_PAIR.
- * Destinations must be distinct.  Non-finite inputs give unspecified records. */
+ * Destinations must be distinct.  Non-finite inputs give unspecified records.  Of `dims` only
+ * dtype, num_kv_heads, head_dim, promoted, num_pages and num_res_pages are read. */
 pa_status kv_quantize_pages(const pa_kitty_dims *dims, const void *res_k, const void *res_v,
                             const int64_t *pairs, int64_t num_pairs, void *pages,
                             pa_stream_t stream);

@@ -869,8 +869,12 @@ size_t pa_kitty_workspace_size(const pa_kitty_dims *dims) {
 
 pa_status kv_quantize_pages(const pa_kitty_dims *dims, const void *res_k, const void *res_v,
                             const int64_t *pairs, int64_t num_pairs, void *pages, pa_stream_t stream) {
-    const pa_status st = check_kitty_dims(dims);
-    if (st != PA_OK) return st;
+    // only the page geometry matters here (the decode fields may hold anything)
+    if (!dims) return PA_ERR_INVALID_ARG;
+    if (dims->dtype != PA_BF16 && dims->dtype != PA_F16)
+        return dims->dtype == PA_F32 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
+    if (dims->num_kv_heads < 1 || dims->num_pages < 0 || dims->num_res_pages < 0) return PA_ERR_INVALID_ARG;
+    if (dims->head_dim != kDim || (dims->promoted != 16 && dims->promoted != 32)) return PA_ERR_UNSUPPORTED;
     if (num_pairs < 0 || num_pairs > 0x7fffffff) return PA_ERR_INVALID_ARG;
     if (num_pairs == 0) return PA_OK;
     if (!res_k || !res_v || !pairs || !pages) return PA_ERR_INVALID_ARG;

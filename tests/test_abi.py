@@ -187,7 +187,16 @@ def test_kitty_calls_reject_bad_dims(lib, kw, code):
     d = _kdims(**kw)
     assert lib.pa_forward_kitty(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                 ctypes.c_float(0.1), FAKE, FAKE, 1 << 30, None) == code
-    assert lib.kv_quantize_pages(ctypes.byref(d), FAKE, FAKE, FAKE, 1, FAKE, None) == code
+    # the quantiser reads only the page geometry
+    qcode = code if ("num_q_heads" not in kw and "num_seqs" not in kw) else None
+    if qcode is not None:
+        assert lib.kv_quantize_pages(ctypes.byref(d), FAKE, FAKE, FAKE, 1, FAKE, None) == qcode
+
+
+def test_kitty_quantiser_ignores_decode_fields(lib):
+    d = _kdims(num_seqs=0, num_q_heads=7, max_pages_per_seq=0)
+    assert lib.kv_quantize_pages(ctypes.byref(d), FAKE, FAKE, FAKE, 0, FAKE, None) == 0   # no-op
+    assert lib.kv_quantize_pages(ctypes.byref(_kdims(num_kv_heads=0)), FAKE, FAKE, FAKE, 0, FAKE, None) == 1
 
 
 def test_kitty_calls_reject_bad_pointers_and_workspace(lib):
