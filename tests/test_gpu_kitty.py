@@ -84,7 +84,7 @@ def test_quantised_records_are_bit_exact(dtype, P):
                                             (4, 4, "f16", 16), (8, 1, "f16", 32)])
 def test_decode_matches_oracle_every_row(hq, hkv, dtype, P):
     # tail only (c = 0), one token short of a page, exactly one and two pages (no residual page),
-    # one past a page, several chunks of four pages with a tail, a long sequence
+    # one past a page, several items of eight pages with a tail, a long sequence
     lens = [0, 126, 127, 128, 255, 511, 700, 1800, 4100]
     b = W.make_kitty_batch("every_row", lens, hq, hkv, P, dtype=dtype, seed=hq + hkv + P)
     d = gpu_state(b)
@@ -156,3 +156,14 @@ def test_full_decode_batch_sampled_sequences():
             f = kitty.quantize_page(oracle.widen_f32(b.stage_k[sid, h], "bf16"),
                                     oracle.widen_f32(b.stage_v[sid, h], "bf16"), b.promoted)
             assert np.array_equal(pages[t, h].cpu().numpy(), kitty.pack_record(f))
+
+
+def test_long_sequence_merges_many_splits():
+    # 60,001 tokens: 468 quantised pages in 59 items of 8 pages plus the residual page, so the
+    # row's merge combines 60 split records (more than one warp-width of records)
+    b = W.make_kitty_batch("long", [60000, 300], 4, 2, 32, seed=31)
+    d = gpu_state(b)
+    out = gpu_forward(b, d)
+    assert pkg.device_status() == 0
+    ref = oracle_rows(b, [0, 1])
+    assert_close(as_f64(out), ref, "bf16", "kitty long sequence")
