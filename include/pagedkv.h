@@ -38,7 +38,7 @@ typedef struct CUstream_st *pa_stream_t; /* same type as cudaStream_t */
 typedef enum {
     PA_OK = 0,
     PA_ERR_INVALID_ARG = 1,  /* a NULL pointer, a bad shape, stride or alignment */
-    PA_ERR_UNSUPPORTED = 2,  /* a valid request this build does not implement (e.g. head_dim) */
+    PA_ERR_UNSUPPORTED = 2,  /* a valid request the library does not implement (e.g. head_dim) */
     PA_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned */
     PA_ERR_CUDA = 4,         /* a CUDA runtime call (launch, attribute query) failed */
     PA_ERR_DEVICE = 5        /* pa_get_device_status found device-side error bits */
