@@ -215,7 +215,10 @@ pa_status kv_append(const kv_append_dims *dims, const void *k_new, const void *v
  * precondition gives unspecified bytes in the affected blocks, nothing else.  Ids outside
  * [0, src_num_blocks) / [0, dst_num_blocks) are skipped and flagged PA_DEV_BAD_PAIR.
  * src and dst may be device memory or page-locked host memory.  block_bytes, strides and both
- * base pointers must be multiples of 16 bytes.
+ * base pointers must be multiples of 16 bytes.  With num_planes > 1 the planes of each pool must
+ * not overlap: either plane_stride >= num_blocks * block stride (planes one after another), or
+ * block_bytes <= plane_stride and num_planes * plane_stride <= block stride (planes side by side
+ * inside every block); any other plane stride (0 included) is refused with PA_ERR_INVALID_ARG.
  *
  * max_ctas bounds the copy's grid (256-thread CTAs, no shared memory).  0 takes the default, a
  * persistent grid of 8 CTAs per SM, for a copy that has the GPU to itself.  A small value (a few

@@ -93,6 +93,19 @@ bool overlap(const void *a, size_t an, const void *b, size_t bn) {
     return x < y + bn && y < x + an;
 }
 
+// Whether the blocks of a pool's planes occupy disjoint bytes: either every plane lies past the
+// previous plane's last block (planes outside one another, e.g. layer-first), or the planes sit
+// side by side inside each block's stride (e.g. block-first, all layers of a block together).
+// Anything else (a zero or short plane stride) lets one plane's copy overwrite another plane.
+bool planes_disjoint(int32_t planes, int64_t plane_stride, int64_t block_stride, int64_t blocks,
+                     int64_t block_bytes) {
+    if (planes <= 1) return true;
+    const int64_t bs = block_stride ? block_stride : block_bytes;
+    if (plane_stride <= 0) return false;
+    if (plane_stride >= blocks * bs) return true;
+    return plane_stride >= block_bytes && bs >= (int64_t)planes * plane_stride;
+}
+
 pa_status check_dims(const pa_dims *d) {
     if (!d) return PA_ERR_INVALID_ARG;
     if (!valid_dtype(d->dtype)) return PA_ERR_INVALID_ARG;
@@ -292,6 +305,9 @@ pa_status block_copy(const block_copy_dims *dims, const void *src, void *dst, co
         return PA_ERR_INVALID_ARG;
     if (d.src_block_stride && d.src_block_stride < d.block_bytes) return PA_ERR_INVALID_ARG;
     if (d.dst_block_stride && d.dst_block_stride < d.block_bytes) return PA_ERR_INVALID_ARG;
+    if (!planes_disjoint(d.num_planes, d.src_plane_stride, d.src_block_stride, d.src_num_blocks, d.block_bytes) ||
+        !planes_disjoint(d.num_planes, d.dst_plane_stride, d.dst_block_stride, d.dst_num_blocks, d.block_bytes))
+        return PA_ERR_INVALID_ARG;
     if (!aligned(src, 16) || !aligned(dst, 16) || !aligned(pairs, 8)) return PA_ERR_INVALID_ARG;
     unsigned *status = status_ptr();
     const int sms = sm_count();

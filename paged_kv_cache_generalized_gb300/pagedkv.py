@@ -168,6 +168,26 @@ def forward_dims(q, k_cache, block_tables, ctx_lens, k_scale=None, v_scale=None)
                   block_tables.shape[1], bstride, kind, ks, vs)
 
 
+def _forward_args(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, k_scale, v_scale) -> PaDims:
+    """Checks the arguments of pa_forward and pa_forward_no_alloc (one set of rules for both:
+    the library reads V with K's geometry and element size, and the index arrays as int32) and
+    returns their dims.  Raises ValueError before anything reaches the device."""
+    if q.dim() != 3 or not q.is_contiguous():
+        raise ValueError("q must be contiguous [T, Hq, d]")
+    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
+        raise ValueError("k_cache and v_cache must have the same shape and strides")
+    if v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must share a dtype")
+    for t in (block_tables, ctx_lens, q_lens):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError("block_tables, ctx_lens and q_lens must be contiguous int32")
+    if block_tables.dim() != 2 or ctx_lens.dim() != 1 or q_lens.shape != ctx_lens.shape:
+        raise ValueError("block_tables must be [S, max_blocks], ctx_lens and q_lens [S]")
+    if block_tables.shape[0] != ctx_lens.shape[0]:
+        raise ValueError("block_tables and ctx_lens disagree on the number of sequences")
+    return forward_dims(q, k_cache, block_tables, ctx_lens, k_scale, v_scale)
+
+
 def forward_workspace_size(q, k_cache, block_tables, ctx_lens) -> int:
     dims = forward_dims(q, k_cache, block_tables, ctx_lens, 1.0, 1.0)
     return int(load_library().pa_forward_workspace_size(ctypes.byref(dims)))
@@ -180,17 +200,8 @@ def pa_forward(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale=None, 
     q: [T, Hq, d]; k_cache/v_cache: [num_blocks, Hkv, B, d] in q's dtype, or E4M3 codes (uint8 or
     float8_e4m3fn) with ``k_scale`` / ``v_scale``; block_tables: int32 [S, max_blocks];
     ctx_lens/q_lens: int32 [S].  Returns ``out`` ([T, Hq, d])."""
+    dims = _forward_args(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, k_scale, v_scale)
     lib = load_library()
-    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
-        raise ValueError("k_cache and v_cache must have the same shape and strides")
-    if v_cache.dtype != k_cache.dtype:
-        raise ValueError("k_cache and v_cache must share a dtype")
-    for t in (block_tables, ctx_lens, q_lens):
-        if t.dtype != torch.int32 or not t.is_contiguous():
-            raise ValueError("block_tables, ctx_lens and q_lens must be contiguous int32")
-    if not q.is_contiguous():
-        raise ValueError("q must be contiguous [T, Hq, d]")
-    dims = forward_dims(q, k_cache, block_tables, ctx_lens, k_scale, v_scale)
     if scale is None:
         scale = 1.0 / float(dims.head_dim) ** 0.5
     if out is None:
@@ -211,10 +222,8 @@ def pa_forward_no_alloc(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, sca
     """pa_forward with the library's own fixed-size scratch (see ``pa_forward_no_alloc`` in
     include/pagedkv.h): for callers that cannot allocate device memory.  Raises if the batch
     needs more scratch than the library holds."""
+    dims = _forward_args(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, k_scale, v_scale)
     lib = load_library()
-    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
-        raise ValueError("k_cache and v_cache must have the same shape and strides")
-    dims = forward_dims(q, k_cache, block_tables, ctx_lens, k_scale, v_scale)
     if scale is None:
         scale = 1.0 / float(dims.head_dim) ** 0.5
     if out is None:

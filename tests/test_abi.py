@@ -134,6 +134,32 @@ def test_append_and_copy_reject_bad_arguments(lib):
     assert lib.block_copy(ctypes.byref(c), FAKE, FAKE, FAKE, None) == 1
 
 
+@pytest.mark.parametrize("src_ps,dst_ps,src_bs,dst_bs,ok", [
+    (0, 4 * 4096, 0, 0, False),             # two source planes on the same bytes
+    (4 * 4096, 0, 0, 0, False),             # two destination planes on the same bytes
+    (4096, 4 * 4096, 0, 0, False),          # plane 1 starts at plane 0's block 1
+    (2048, 2048, 2 * 4096, 2 * 4096, False),  # side by side but narrower than a block
+    (4 * 4096, 8 * 4096, 0, 0, True),       # layer-first: planes one after another
+    (4096, 4096, 2 * 4096, 2 * 4096, True),  # block-first: planes side by side in each block
+])
+def test_block_copy_refuses_overlapping_planes(lib, src_ps, dst_ps, src_bs, dst_bs, ok):
+    """With several planes, a plane stride that makes two planes share bytes would let one plane's
+    copy overwrite another's blocks; the call refuses it on the host.  Without a GPU an accepted
+    layout passes every host check and stops at the device lookup (PA_ERR_CUDA), so the two
+    outcomes differ.  The fake pointers must never reach a launch, so the test does not run where
+    a GPU is visible."""
+    import torch
+
+    from paged_kv_cache_generalized_gb300.pagedkv import BlockCopyDims
+
+    if torch.cuda.is_available():
+        pytest.skip("checks host-side refusals with fake pointers: only where no GPU is visible")
+    c = BlockCopyDims(block_bytes=4096, num_planes=2, src_plane_stride=src_ps, dst_plane_stride=dst_ps,
+                      src_block_stride=src_bs, dst_block_stride=dst_bs, src_num_blocks=4,
+                      dst_num_blocks=4, num_pairs=1, max_ctas=0)
+    rc = lib.block_copy(ctypes.byref(c), FAKE, FAKE, FAKE, None)
+    assert rc == (4 if ok else 1)
+
 def test_e4m3_caches_reject_bad_scales_and_unsupported_shapes(lib):
     from paged_kv_cache_generalized_gb300.pagedkv import KvAppendDims, PaDims
 
