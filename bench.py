@@ -10,7 +10,11 @@ Workloads (``--workload``):
   decode13b   (default) 64 sequences, Llama-2-13B attention shape (40 MHA heads, d=128), bf16,
               block 16, q_len 1, context U{512..4096}, blocks scattered in a pool with 10% free;
               6 sequences fork (copy-on-write of their partially filled last block).
-              Metric: algorithmic HBM bytes / step time, GB/s.
+              Metric: algorithmic HBM bytes / step time, GB/s.  The line also carries the metric's
+              prefill half, measured in the same process with the same --steps / --warmup:
+              "mixed_prefill" (the mixed_gqa workload) and "long_prefill" (longprefill), each with
+              its own value (TFLOP/s), roofline, cpu_baseline, e2e and clocks
+              (--headline-only leaves them out).
   decode13b_fp8  the same batch with FP8 E4M3 K/V caches (scale 1/32 for K and V): half the K/V
               bytes per token.  Metric: GB/s (of the 8-bit bytes); the line also gives tokens/s.
   mixed_gqa   32 resumed conversations (history U{1024..16384}, new turn U{16..512}) + 32 decode
@@ -120,6 +124,13 @@ class ClockSampler:
             self.t.start()
         except OSError:
             self.proc = None
+            return self
+        # the sampler is live once its first line arrives; the timed region starts after that,
+        # and only lines from then on count
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.01)
+        self.lines = []
         return self
 
     def _read(self):
@@ -128,6 +139,11 @@ class ClockSampler:
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            # a timed region shorter than the sampling interval still gets the sample taken
+            # right after it
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 0.5 and self.proc.poll() is None:
+                time.sleep(0.01)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -175,6 +191,125 @@ def _tc_enabled(batch):
             and 16 <= batch.block_size <= 128)
 
 
+def attn_accounting(batch, cow_frac=0.0, seed=0, kv8=False):
+    """Host-only accounting of one attention step over ``batch``: the copy-on-write fork pairs
+    (a fraction of sequences copy their partially filled last block to a free block) and the
+    step's algorithmic bytes and FLOPs.  Both arms of the bench use it, so their configs agree."""
+    B = batch.block_size
+    n = batch.seq_lens
+    used = np.zeros(batch.num_blocks, bool)
+    for i in range(batch.num_seqs):
+        used[batch.block_tables[i, :(n[i] + B - 1) // B]] = True
+    free = np.flatnonzero(~used)
+    rng = np.random.default_rng(seed)
+    k = min(int(round(cow_frac * batch.num_seqs)), len(free))
+    forks = rng.choice(batch.num_seqs, k, replace=False) if k else np.zeros(0, np.int64)
+    pairs = np.array([[batch.block_tables[i, (n[i] - 1) // B], free[j]] for j, i in enumerate(forks)],
+                     dtype=np.int64).reshape(-1, 2)
+    es = 4 if batch.dtype == "f32" else 2
+    ek = 1 if kv8 else es                           # bytes of one cached element
+    Hq, Hkv, d = batch.num_q_heads, batch.num_kv_heads, batch.head_dim
+    T = batch.total_q
+    nb = (n + B - 1) // B
+    return {"pairs": pairs,
+            "bytes_attn": float(n.sum() * Hkv * d * ek * 2 + 2 * T * Hq * d * es + nb.sum() * 4 + batch.num_seqs * 8),
+            "bytes_append": float(2 * T * Hkv * d * (es + ek) + 8 * T),
+            "bytes_copy": float(len(pairs) * 2 * 2 * Hkv * B * d * ek + pairs.size * 8),
+            "flops": attn_flops(batch.ctx_lens, batch.q_lens, Hq, d),
+            "pool_bytes": 2 * int(np.prod(batch.k_cache.shape)) * ek}
+
+
+def kitty_record_bytes(promoted, head_dim=128):
+    """Bytes of one (page, KV head) record of the 2-bit page format, from its documented layout:
+    K scale and minimum per channel, V scale and minimum per token (float32), 32 promoted-id
+    bytes, 2-bit K low bits and V codes of 128 tokens, and the promoted channels' high bits."""
+    T = 128
+    return 4 * 2 * head_dim + 4 * 2 * T + 32 + T * head_dim // 4 + T * promoted // 4 + T * head_dim // 4
+
+
+def kitty_accounting(batch, R=None):
+    """Host-only accounting of one 2-bit page decode step (append, one page quantised, attention)."""
+    T = 128
+    R = R or kitty_record_bytes(batch.promoted, batch.head_dim)
+    S, Hq, Hkv, d = batch.num_seqs, batch.num_q_heads, batch.num_kv_heads, batch.head_dim
+    n = batch.ctx_lens.astype(np.int64) + 1
+    nfull, tail = n // T, n % T
+    es = 2
+    return {"bytes_attn": float((nfull * Hkv * R).sum() + (tail * Hkv * d * es * 2).sum()
+                                + 2 * S * Hq * d * es + ((n + T - 1) // T).sum() * 4 + S * 8),
+            "bytes_append": float(2 * int((tail > 0).sum()) * Hkv * d * es * 2 + 8 * S),
+            "bytes_copy": float(2 * Hkv * T * d * es + Hkv * R + 16),
+            "flops": attn_flops(batch.ctx_lens, batch.q_lens, Hq, d),
+            "pool_bytes": batch.num_pages * Hkv * R + 2 * int(np.prod(batch.res_k.shape)) * es}
+
+
+# (copy-on-write fraction, seed of the fork draw) of the attention workloads
+ATTN_COW = {"decode13b": (0.1, 2), "decode13b_fp8": (0.1, 2), "mixed_gqa": (0.0, 3), "longprefill": (0.0, 4)}
+
+
+def workload_batch(name, args):
+    """The workload's synthetic host-side batch (or KV-movement plan), the same in both arms."""
+    seqs = getattr(args, "seqs", None)
+    if name in ("decode13b", "decode13b_fp8", "layout"):
+        return W.decode13b(seed=2, num_seqs=seqs or 64, poison=False)
+    if name == "decode13b_kitty":
+        return W.decode13b_kitty(seed=2, num_seqs=seqs or 64)
+    if name in ("mixed_gqa", "swap_pipeline"):
+        half = (seqs or 64) // 2
+        return W.mixed_gqa(seed=3, n_resume=half, n_decode=half, poison=False)
+    if name == "longprefill":
+        return W.longprefill(seed=4, num_seqs=seqs or 8, poison=False)
+    if name == "kvmove":
+        sessions = seqs or 64
+        return W.kvmove_plan(seed=5, num_layers=args.layers, num_sessions=sessions,
+                             swap_sessions=max(1, sessions // 8))
+    raise ValueError(name)
+
+
+def kvmove_accounting(plan):
+    L, hkv, B, d = plan.num_layers, plan.num_kv_heads, plan.block_size, plan.head_dim
+    T = len(plan.slot_mapping)
+    bb = plan.block_bytes
+    return {"bytes_cow": float(len(plan.cow_pairs) * 2 * L * bb * 2),
+            "bytes_append": float(2 * L * T * hkv * d * 2 * 2 + 8 * T),
+            "bytes_swap": float(len(plan.swap_pairs) * 2 * L * bb * 2),
+            "pool_bytes": L * 2 * plan.num_blocks * hkv * B * d * 2}
+
+
+def workload_config(name, args, world, batch):
+    """The JSON line's ``config``: what the workload is and its sizes, computed on the host from
+    the batch alone, so that the native and the reference arm print the same dict."""
+    cfg = {"workload": workload_text(name, args)}
+    if name in ATTN_COW:
+        a = attn_accounting(batch, *ATTN_COW[name], kv8=name.endswith("fp8"))
+        cfg["l2"] = "inputs larger than L2 (KV pool %.2f GB resident)" % (a["pool_bytes"] / 1e9)
+        cfg["bytes_per_step"] = a["bytes_attn"] + a["bytes_append"] + a["bytes_copy"]
+        cfg["attn_flops_per_step"] = a["flops"]
+    elif name == "decode13b_kitty":
+        a = kitty_accounting(batch)
+        cfg["l2"] = "inputs larger than L2 (page records + residual pages %.2f GB resident)" % (a["pool_bytes"] / 1e9)
+        cfg["bytes_per_step"] = a["bytes_attn"] + a["bytes_append"] + a["bytes_copy"]
+        cfg["attn_flops_per_step"] = a["flops"]
+    elif name == "kvmove":
+        a = kvmove_accounting(batch)
+        cfg["layers_resident"] = batch.num_layers
+        cfg["l2"] = "inputs larger than L2 (pool %.1f GB)" % (a["pool_bytes"] / 1e9)
+        cfg["bytes_per_step"] = a["bytes_cow"] + a["bytes_append"] + a["bytes_swap"]
+        cfg["cow_pairs"] = len(batch.cow_pairs)
+        cfg["swap_blocks"] = len(batch.swap_pairs)
+        cfg["append_tokens"] = len(batch.slot_mapping)
+    elif name == "swap_pipeline":
+        cfg["layers_resident"] = args.layers
+        cfg["l2"] = "inputs larger than L2 (%d-layer pool of the mixed batch)" % args.layers
+        cfg["attn_flops_per_step"] = args.layers * attn_flops(batch.ctx_lens, batch.q_lens,
+                                                              batch.num_q_heads, batch.head_dim)
+    elif name == "layout":
+        cfg["layers"] = args.layers
+        cfg["l2"] = "inputs larger than L2 (two %d-layer pools of the decode batch)" % args.layers
+    cfg["parallelism"] = f"replicas x{world}"
+    return cfg
+
+
 class AttnStep:
     """block_copy + kv_append + pa_forward over one AttnBatch, all inputs resident on the GPU."""
 
@@ -205,18 +340,8 @@ class AttnStep:
             "ctx": up(batch.ctx_lens).pin_memory(),
             "ql": up(batch.q_lens).pin_memory(),
         }
-        # copy-on-write forks: a fraction of sequences copy their last block to a free block
-        B = batch.block_size
-        n = batch.seq_lens
-        used = np.zeros(batch.num_blocks, bool)
-        for i in range(batch.num_seqs):
-            used[batch.block_tables[i, :(n[i] + B - 1) // B]] = True
-        free = np.flatnonzero(~used)
-        rng = np.random.default_rng(seed)
-        k = min(int(round(cow_frac * batch.num_seqs)), len(free))
-        forks = rng.choice(batch.num_seqs, k, replace=False) if k else np.zeros(0, np.int64)
-        pairs = np.array([[batch.block_tables[i, (n[i] - 1) // B], free[j]] for j, i in enumerate(forks)],
-                         dtype=np.int64).reshape(-1, 2)
+        acct = attn_accounting(batch, cow_frac, seed, kv8)
+        pairs = acct["pairs"]
         self.host["pairs"] = up(pairs).pin_memory()
         self.dev_in = {k2: v.to(dev) for k2, v in self.host.items()}
         # K and V caches are the two planes of one pool, so one block_copy moves both
@@ -236,15 +361,9 @@ class AttnStep:
         self.ws = torch.empty(max(256, pkg.forward_workspace_size(self.dev_in["q"], self.k_cache,
                                                                  self.dev_in["bt"], self.dev_in["ctx"])),
                               dtype=torch.uint8, device=dev)
-        es = 4 if batch.dtype == "f32" else 2
-        ek = 1 if kv8 else es                           # bytes of one cached element
-        Hq, Hkv, d = batch.num_q_heads, batch.num_kv_heads, batch.head_dim
+        self.bytes_attn, self.bytes_append = acct["bytes_attn"], acct["bytes_append"]
+        self.bytes_copy, self.flops = acct["bytes_copy"], acct["flops"]
         T = batch.total_q
-        nb = (n + B - 1) // B
-        self.bytes_attn = float(n.sum() * Hkv * d * ek * 2 + 2 * T * Hq * d * es + nb.sum() * 4 + batch.num_seqs * 8)
-        self.bytes_append = float(2 * T * Hkv * d * (es + ek) + 8 * T)
-        self.bytes_copy = float(len(pairs) * 2 * 2 * Hkv * B * d * ek + pairs.size * 8)
-        self.flops = attn_flops(batch.ctx_lens, batch.q_lens, Hq, d)
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
         self.d2h_bytes = self.out.numel() * self.out.element_size()
         # block_copy (if any fork) + kv_append + pa_forward's planner and CUDA-core kernel (which
@@ -335,12 +454,9 @@ class KittyStep:
         self.out_host = torch.empty_like(self.host["q"]).pin_memory()
         need = pkg.kitty_workspace_size(self.dev_in["q"], self.pages, self.res_k, self.dev_in["bt"], P)
         self.ws = torch.empty(max(256, need), dtype=torch.uint8, device=dev)
-        es = 2
-        self.bytes_attn = float((nfull * Hkv * R).sum() + (tail * Hkv * d * es * 2).sum()
-                                + 2 * S * Hq * d * es + ((n + T - 1) // T).sum() * 4 + S * 8)
-        self.bytes_append = float(2 * int((tail > 0).sum()) * Hkv * d * es * 2 + 8 * S)
-        self.bytes_copy = float(2 * Hkv * T * d * es + Hkv * R + 16)
-        self.flops = attn_flops(batch.ctx_lens, batch.q_lens, Hq, d)
+        acct = kitty_accounting(batch, R)
+        self.bytes_attn, self.bytes_append = acct["bytes_attn"], acct["bytes_append"]
+        self.bytes_copy, self.flops = acct["bytes_copy"], acct["flops"]
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
         self.d2h_bytes = self.out.numel() * self.out.element_size()
         self.launches_per_step = 3          # kv_append, kv_quantize_pages, the decode kernel
@@ -348,7 +464,7 @@ class KittyStep:
         self.bound_note = ("bound by instruction issue, not HBM: 288 mixed-precision FMAs and 144 ANDs per "
                            "(key, head) at 16 warps per SM, 65% issue-active under ncu; frac is of HBM bytes")
         self.dtype_label = f"bf16 q/out, 2-bit K/V with {P} of 128 key channels at 4 bits, fp32 accumulate"
-        self.pool_bytes = (self.pages.numel() + 2 * self.res_k.numel() * es)
+        self.pool_bytes = acct["pool_bytes"]
 
     def step(self, ev=None):
         inp = self.dev_in
@@ -396,10 +512,8 @@ class KVMoveStep:
         self.swap = torch.from_numpy(plan.swap_pairs).to(dev)
         self.slots = torch.from_numpy(plan.slot_mapping).to(dev)
         self.cow_planes = self.pool.view(L * 2, nb, hkv, B, d)
-        bb = plan.block_bytes
-        self.bytes_cow = float(len(plan.cow_pairs) * 2 * L * bb * 2)
-        self.bytes_append = float(2 * L * T * hkv * d * 2 * 2 + 8 * T)
-        self.bytes_swap = float(len(plan.swap_pairs) * 2 * L * bb * 2)
+        acct = kvmove_accounting(plan)
+        self.bytes_cow, self.bytes_append, self.bytes_swap = acct["bytes_cow"], acct["bytes_append"], acct["bytes_swap"]
         self.flops = 0.0
         self.launches_per_step = 1 + 1 + L
         self.h2d_bytes = self.bytes_swap / 2 + self.new.numel() * 2 + 8 * T + plan.cow_pairs.nbytes + plan.swap_pairs.nbytes
@@ -598,21 +712,12 @@ def h2d_peak_gbs(dev, nbytes=1 << 30, reps=5):
     return nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
 
 
-def build_attn_step(name, dev, seqs=None):
-    if name in ("decode13b", "decode13b_fp8"):
-        b = W.decode13b(seed=2, num_seqs=seqs or 64, poison=False)
-        return AttnStep(b, dev, cow_frac=0.1, seed=2, kv8=name.endswith("fp8")), b
+def build_attn_step(name, dev, args):
+    b = workload_batch(name, args)
     if name == "decode13b_kitty":
-        b = W.decode13b_kitty(seed=2, num_seqs=seqs or 64)
         return KittyStep(b, dev), b
-    if name == "mixed_gqa":
-        half = (seqs or 64) // 2
-        b = W.mixed_gqa(seed=3, n_resume=half, n_decode=half, poison=False)
-        return AttnStep(b, dev, cow_frac=0.0, seed=3), b
-    if name == "longprefill":
-        b = W.longprefill(seed=4, num_seqs=seqs or 8, poison=False)
-        return AttnStep(b, dev, cow_frac=0.0, seed=4), b
-    raise ValueError(name)
+    cow, seed = ATTN_COW[name]
+    return AttnStep(b, dev, cow_frac=cow, seed=seed, kv8=name.endswith("fp8")), b
 
 
 WORKLOAD_TEXT = {
@@ -721,6 +826,35 @@ def oracle_sample(b: W.AttnBatch, budget_s: float, max_rows=None):
     return t_total, kv_bytes, flops, rows, threads
 
 
+def oracle_token_sample(b: W.AttnBatch, budget_s: float, tokens_per_call: int = 8):
+    """Times the float64 oracle on query tokens (all heads each) drawn uniformly over the batch's
+    new tokens, ``tokens_per_call`` per call, for about ``budget_s`` seconds: for batches whose
+    single sequences take longer than the budget.  Returns (seconds, kv_bytes, flops, tokens,
+    threads); FLOPs count 4 * d * Hq per visible key of each token, as in the GPU metric."""
+    import oracle
+
+    threads = oracle.max_threads()
+    es = 4 if b.dtype == "f32" else 2
+    rng = np.random.default_rng(0)
+    cu = np.concatenate([[0], np.cumsum(b.q_lens)])
+    T = int(cu[-1])
+    t_total, kv_bytes, flops, toks = 0.0, 0.0, 0.0, []
+    while t_total < budget_s:
+        pick = rng.integers(0, T, tokens_per_call)
+        seqs = np.searchsorted(cu, pick, side="right") - 1
+        rows = np.array([(i, p - cu[i], h) for i, p in zip(seqs, pick) for h in range(b.num_q_heads)],
+                        dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.paged_attention_batch(b, rows=rows, threads=threads)
+        t_total += time.perf_counter() - t0
+        for i, p in zip(seqs, pick):
+            keys = int(b.ctx_lens[i]) + int(p - cu[i]) + 1
+            kv_bytes += keys * b.num_kv_heads * b.head_dim * es * 2
+            flops += 4.0 * b.head_dim * b.num_q_heads * keys
+            toks.append(int(p))
+    return t_total, kv_bytes, flops, toks, threads
+
+
 def kitty_oracle_sample(b: W.KittyBatch, budget_s: float):
     """Times the oracle's decode attention over 2-bit pages (it dequantises every page of the
     sequence, then runs the float64 attention) on whole sequences of the batch, longest first,
@@ -784,99 +918,97 @@ def metric_for(name):
     return ("paged-attn mixed-prefill TFLOP/s (causal-exact attention FLOPs / step time)", "TFLOP/s", True)
 
 
+def reference_attn(name, args, world, batch, per_step):
+    """The oracle timed on the workload: ``args.warmup`` untimed and ``args.steps`` timed steps, each
+    a bounded sample of about ``per_step`` seconds.  Returns (value, ms_per_step, sample text,
+    threads)."""
+    metric, unit, hib = metric_for(name)
+    total = args.steps + args.warmup
+    secs, kvb, fl, threads, desc = 0.0, 0.0, 0.0, 1, ""
+    for s_ in range(total):
+        if name == "longprefill":
+            t, kb, f, rows, threads = oracle_token_sample(batch, per_step)
+            desc = (f"float64 oracle rows of {len(rows)} query token(s) (all heads) drawn across the "
+                    f"{name} batch per step, ~{per_step:.2f}s each")
+        else:
+            t, kb, f, rows, threads = oracle_sample(batch, per_step)
+            desc = (f"float64 oracle rows of {len(rows)} sequence(s) (all heads, all new tokens) "
+                    f"of the {name} batch per step, ~{per_step:.2f}s each")
+        if s_ >= args.warmup:
+            secs += t
+            kvb += kb
+            fl += f
+    value = (kvb / secs / 1e9) if unit == "GB/s" else (fl / secs / 1e12)
+    return value, secs / max(1, args.steps) * 1e3, desc, threads
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
     name = args.workload
     metric, unit, hib = metric_for(name)
+    batch = workload_batch(name, args)
+    config = workload_config(name, args, world, batch)
+    total = args.steps + args.warmup
+    per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
+    base = {"impl": "reference", "metric": metric, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": hib, "scaling": "weak",
+            "vs_baseline": None, "data": "synthetic", "config": config}
     if name == "kvmove":
-        plan = W.kvmove_plan(seed=5, num_layers=args.layers)
-        total = args.steps + args.warmup
-        per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
-        secs, moved, reps_all = 0.0, 0.0, 0
+        secs, moved = 0.0, 0.0
         for s_ in range(total):
-            t, mv, reps = kvmove_oracle_sample(plan, per_step)
+            t, mv, reps = kvmove_oracle_sample(batch, per_step)
             if s_ >= args.warmup:
                 secs += t
                 moved += mv
         value = moved / secs / 1e9
-        line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(1, args.steps) * 1e3,
-                "higher_is_better": hib, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-                "data": "synthetic", "config": {"workload": workload_text(name, args)},
-                "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
-                                 "sample": "numpy block copy of 64 copy-on-write pairs and append of 256 tokens per repetition"},
-                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return
-    if name == "decode13b_kitty":
-        kb = W.decode13b_kitty(seed=2)
-        total = args.steps + args.warmup
-        per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
+        line = dict(base, value=value, ms_per_step=secs / max(1, args.steps) * 1e3, dtype="f16",
+                    cpu_baseline={"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                                  "sample": "numpy block copy of 64 copy-on-write pairs and append of 256 tokens per repetition"})
+    elif name == "decode13b_kitty":
         secs, moved, nrows, threads = 0.0, 0.0, 0, 1
         for s_ in range(total):
-            t, nb, _, rows, threads = kitty_oracle_sample(kb, per_step)
+            t, nb, _, rows, threads = kitty_oracle_sample(batch, per_step)
             if s_ >= args.warmup:
                 secs += t
                 moved += nb
                 nrows += len(rows)
         value = moved / secs / 1e9
-        line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(1, args.steps) * 1e3,
-                "higher_is_better": hib, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": {"workload": workload_text(name, args)},
-                "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
-                                 "sample": f"oracle decode attention over 2-bit pages (dequantise + float64 attention) "
-                                           f"on {nrows} whole sequence(s), ~{per_step:.2f}s per step"},
-                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return
-    b = {"decode13b": lambda: W.decode13b(seed=2, poison=False),
-         "decode13b_fp8": lambda: W.decode13b(seed=2, poison=False),
-         "mixed_gqa": lambda: W.mixed_gqa(seed=3, poison=False),
-         "swap_pipeline": lambda: W.mixed_gqa(seed=3, poison=False),
-         "layout": lambda: W.decode13b(seed=2, poison=False),
-         "longprefill": lambda: W.longprefill(seed=4, poison=False)}[name]()
-    total = args.steps + args.warmup
-    per_step = max(0.05, min(2.0, 150.0 / max(total, 1)))
-    vals, secs = [], 0.0
-    sample_desc = None
-    for s in range(total):
-        t, kvb, fl, rows, threads = oracle_sample(b, per_step)
-        if s >= args.warmup:
-            secs += t
-            vals.append((kvb, fl, t))
-        sample_desc = (f"float64 oracle rows of {len(rows)} sequence(s) (all heads, all new tokens) "
-                       f"of the {name} batch per step, ~{per_step:.2f}s each")
-    kvb = sum(v[0] for v in vals)
-    fl = sum(v[1] for v in vals)
-    value = (kvb / secs / 1e9) if unit == "GB/s" else (fl / secs / 1e12)
-    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": secs / max(1, len(vals)) * 1e3, "higher_is_better": hib,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_text(name, args)},
-            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
-                             "sample": sample_desc},
-            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        line = dict(base, value=value, ms_per_step=secs / max(1, args.steps) * 1e3, dtype="f64",
+                    cpu_baseline={"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                                  "sample": f"oracle decode attention over 2-bit pages (dequantise + float64 attention) "
+                                            f"on {nrows} whole sequence(s), ~{per_step:.2f}s per step"})
+    else:
+        value, ms, desc, threads = reference_attn(name, args, world, batch, per_step)
+        line = dict(base, value=value, ms_per_step=ms, dtype="f64",
+                    cpu_baseline={"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": desc})
+    line["e2e"] = {"value": line["value"], "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    if name == "decode13b" and not args.seqs and not args.headline_only:
+        # the same prefill objects as the native line, with the oracle's numbers
+        for sub, key in PREFILL_OBJECTS:
+            sb = workload_batch(sub, args)
+            sm, su, _ = metric_for(sub)
+            sv, sms, sdesc, sth = reference_attn(sub, args, world, sb, max(0.05, per_step / 4))
+            line[key] = {"metric": sm, "value": sv, "unit": su, "ms_per_step": sms, "dtype": "f64",
+                         "config": workload_config(sub, args, world, sb),
+                         "cpu_baseline": {"value": sv, "unit": su, "cores": sth, "kind": "oracle", "sample": sdesc},
+                         "e2e": {"value": sv, "unit": su, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------------------------------------
 # Native (CUDA) arm
 # ------------------------------------------------------------------------------------------------
-def run_native(args):
+def measure_attn_workload(name, args, dev, dist, world, local, peaks, peak_src, cpu_seconds):
+    """Times ``args.steps`` steps of an attention workload (block_copy + kv_append + attention)
+    after ``args.warmup`` untimed ones, with CUDA events on the launching stream and clock samples
+    during the timed region, then the same step end to end (host inputs in, output back); returns
+    the fields of the workload's JSON object (rank 0 also times the oracle on a sample)."""
     import torch
 
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = dist_init(world, True)
-    peaks, peak_src = load_peaks()
-    name = args.workload
     metric, unit, hib = metric_for(name)
-    step_obj, batch = build_attn_step(name, dev, args.seqs)
+    step_obj, batch = build_attn_step(name, dev, args)
     torch.cuda.synchronize()
 
     for _ in range(args.warmup):
@@ -884,7 +1016,7 @@ def run_native(args):
     torch.cuda.synchronize()
     flags = step_obj.pkg.device_status()
     if flags:
-        raise RuntimeError(f"device status after warm-up: {step_obj.pkg.status_names(flags)}")
+        raise RuntimeError(f"{name}: device status after warm-up: {step_obj.pkg.status_names(flags)}")
 
     K = args.steps
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -904,10 +1036,9 @@ def run_native(args):
     ms_step = elapsed_ms / K
 
     step_bytes = step_obj.bytes_attn + step_obj.bytes_append + step_obj.bytes_copy
-    if unit == "GB/s":
-        value = step_bytes * world / (ms_step * 1e-3) / 1e9
-    else:
-        value = step_obj.flops * world / (ms_step * 1e-3) / 1e12
+    work = step_bytes if unit == "GB/s" else step_obj.flops
+    scale_u = 1e9 if unit == "GB/s" else 1e12
+    value = work * world / (ms_step * 1e-3) / scale_u
 
     # end to end through the public API: H2D of the step's inputs, the step, D2H of the output
     Ke = min(K, max(20, K // 5))
@@ -922,11 +1053,18 @@ def run_native(args):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev) / Ke
-    e2e_val = (step_bytes if unit == "GB/s" else step_obj.flops) * world / (e2e_ms * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
+    e2e_val = work * world / (e2e_ms * 1e-3) / scale_u
     flags = step_obj.pkg.device_status()
 
-    if rank != 0:
-        return
+    res = {"metric": metric, "unit": unit, "higher_is_better": hib, "value": value, "ms_per_step": ms_step,
+           "attn_ms": attn_ms, "device_status": flags, "clocks": clocks.summary(),
+           "gpu_launches": step_obj.launches_per_step * K,
+           "dtype": getattr(step_obj, "dtype_label",
+                            "bf16 q/out, e4m3 K/V, fp32 accumulate" if step_obj.kv8 else batch.dtype),
+           "config": workload_config(name, args, world, batch),
+           "query_tokens_per_s": getattr(batch, "total_q", batch.num_seqs) * world / (attn_ms * 1e-3),
+           "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": step_obj.h2d_bytes,
+                   "d2h_bytes_per_step": step_obj.d2h_bytes, "ms_per_step": e2e_ms}}
     if unit == "GB/s":
         achieved = step_obj.bytes_attn / (attn_ms * 1e-3) / 1e9
         traffic, tsrc = measured_traffic(name, step_obj.bytes_attn)
@@ -944,41 +1082,68 @@ def run_native(args):
         traffic, tsrc = measured_traffic(name, step_obj.bytes_attn)
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
                 "frac": achieved / pk, "traffic": traffic, "traffic_source": tsrc,
-                "algorithmic_flops": step_obj.flops,
-                "kernel": "pa_forward (plan + tcgen05 tensor-core prefill + CUDA-core decode with fused split merge)",
+                "algorithmic_flops": step_obj.flops, "algorithmic_bytes": step_obj.bytes_attn,
+                "kernel": "pa_forward (plan + tcgen05 tensor-core prefill + tensor-core GQA / CUDA-core "
+                          "decode with fused split merge)",
                 "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+    res["roofline"] = roof
+    del step_obj
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
-    cpu = None
-    if world == 1 or rank == 0:
+    res["cpu_baseline"] = None
+    if world == 1 or dist.get_rank() == 0:
         if isinstance(batch, W.KittyBatch):
-            t, kvb, fl, rows, threads = kitty_oracle_sample(batch, args.cpu_seconds)
+            t, kvb, fl, rows, threads = kitty_oracle_sample(batch, cpu_seconds)
             what = "oracle decode attention over 2-bit pages (dequantise + float64 attention)"
-        else:
-            t, kvb, fl, rows, threads = oracle_sample(batch, args.cpu_seconds)
+            unit_rows = "whole sequence(s)"
+        elif batch.total_q > 4 * batch.num_seqs and name == "longprefill":
+            t, kvb, fl, rows, threads = oracle_token_sample(batch, cpu_seconds)
             what = "float64 oracle"
+            unit_rows = "query tokens (all heads) drawn across the batch"
+        else:
+            t, kvb, fl, rows, threads = oracle_sample(batch, cpu_seconds)
+            what = "float64 oracle"
+            unit_rows = "whole sequence(s)"
         cval = kvb / t / 1e9 if unit == "GB/s" else fl / t / 1e12
-        cpu = {"value": cval, "unit": unit, "cores": threads, "kind": "oracle",
-               "sample": f"{what} on {len(rows)} whole sequence(s) of the batch, repeated "
-                         f"passes allowed (all heads, all new tokens), {t:.1f}s; attention only"}
-    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": hib,
-            "scaling": "weak", "vs_baseline": None,
-            "dtype": getattr(step_obj, "dtype_label",
-                             "bf16 q/out, e4m3 K/V, fp32 accumulate" if step_obj.kv8 else batch.dtype),
-            "data": "synthetic",
-            "config": {"workload": workload_text(name, args),
-                       "l2": "inputs larger than L2 (KV pool %.2f GB resident)" % (
-                           getattr(step_obj, "pool_bytes", step_obj.pool.numel() * step_obj.pool.element_size()) / 1e9),
-                       "query_tokens_per_s": getattr(batch, "total_q", batch.num_seqs) * world / (attn_ms * 1e-3),
-                       "bytes_per_step": step_bytes, "attn_flops_per_step": step_obj.flops,
-                       "parallelism": f"replicas x{world}"},
-            "roofline": roof, "cpu_baseline": cpu,
-            "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": step_obj.h2d_bytes,
-                    "d2h_bytes_per_step": step_obj.d2h_bytes, "ms_per_step": e2e_ms},
-            "gpu_launches": step_obj.launches_per_step * K,
-            "attn_ms": attn_ms, "device_status": flags,
-            "clocks": clocks.summary()}
-    print(json.dumps(line), flush=True)
+        res["cpu_baseline"] = {"value": cval, "unit": unit, "cores": threads, "kind": "oracle",
+                               "sample": f"{what} on {len(rows)} {unit_rows} of the batch, repeated "
+                                         f"passes allowed (all heads, all new tokens), {t:.1f}s; attention only"}
+    return res
+
+
+# The prefill workloads measured beside the decode headline: the metric's second half
+PREFILL_OBJECTS = (("mixed_gqa", "mixed_prefill"), ("longprefill", "long_prefill"))
+
+
+def run_native(args):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, True)
+    peaks, peak_src = load_peaks()
+    name = args.workload
+    r = measure_attn_workload(name, args, dev, dist, world, local, peaks, peak_src, args.cpu_seconds)
+    line = {"metric": r["metric"], "value": r["value"], "unit": r["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": r["higher_is_better"],
+            "scaling": "weak", "vs_baseline": None, "dtype": r["dtype"], "data": "synthetic",
+            "config": r["config"], "roofline": r["roofline"], "cpu_baseline": r["cpu_baseline"],
+            "e2e": r["e2e"], "gpu_launches": r["gpu_launches"], "attn_ms": r["attn_ms"],
+            "query_tokens_per_s": r["query_tokens_per_s"], "device_status": r["device_status"],
+            "clocks": r["clocks"]}
+    if name == "decode13b" and not args.seqs and not args.headline_only:
+        # the headline metric's other half, measured in the same process with the same steps and
+        # warm-up: attention TFLOP/s of the mixed multi-turn batch and of the long prefill
+        for sub, key in PREFILL_OBJECTS:
+            s = measure_attn_workload(sub, args, dev, dist, world, local, peaks, peak_src,
+                                      max(1.0, args.cpu_seconds / 2))
+            line[key] = {k: s[k] for k in ("metric", "value", "unit", "ms_per_step", "attn_ms", "dtype",
+                                            "config", "roofline", "cpu_baseline", "e2e", "gpu_launches",
+                                            "query_tokens_per_s", "device_status", "clocks")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def kvmove_oracle_sample(plan: W.KVMovePlan, budget_s: float):
@@ -1022,9 +1187,7 @@ def run_native_kvmove(args):
     dist = dist_init(world, True)
     peaks, peak_src = load_peaks()
     metric, unit, hib = metric_for("kvmove")
-    sessions = args.seqs or 64
-    plan = W.kvmove_plan(seed=5, num_layers=args.layers, num_sessions=sessions,
-                         swap_sessions=max(1, sessions // 8))
+    plan = workload_batch("kvmove", args)
     step_obj = KVMoveStep(plan, dev)
     h2d = h2d_peak_gbs(dev)
     torch.cuda.synchronize()
@@ -1056,8 +1219,11 @@ def run_native_kvmove(args):
     if rank != 0:
         return
     cow_gbs = step_obj.bytes_cow / (cow_ms * 1e-3) / 1e9
+    traffic, tsrc = measured_traffic("kvmove", step_obj.bytes_cow)
     roof = {"bound": "hbm", "achieved": cow_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": cow_gbs / peaks["hbm_gbs"], "traffic": None,
+            "frac": cow_gbs / peaks["hbm_gbs"], "traffic": traffic, "traffic_source": tsrc,
+            "traffic_note": "below the algorithmic bytes: a block shared by r sequences is copied r-1 times "
+                            "and read from DRAM once; lines still dirty in L2 when the kernel ends are not counted",
             "algorithmic_bytes": step_obj.bytes_cow,
             "kernel": "block_copy (copy-on-write, device pool, all resident layers, K and V)",
             "peak_source": f"hbm_gbs of {peak_src}"}
@@ -1069,11 +1235,7 @@ def run_native_kvmove(args):
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": hib,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "config": {"workload": workload_text("kvmove", args), "layers_resident": plan.num_layers,
-                       "l2": "inputs larger than L2 (pool %.1f GB)" % (step_obj.pool.numel() * 2 / 1e9),
-                       "bytes_per_step": step_bytes, "cow_pairs": len(plan.cow_pairs),
-                       "swap_blocks": len(plan.swap_pairs), "append_tokens": len(plan.slot_mapping),
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config("kvmove", args, world, plan),
             "roofline": roof,
             "swap_in": {"achieved": swap_gbs, "unit": "GB/s (host bytes read)", "peak": h2d,
                         "frac": swap_gbs / h2d, "peak_source": "pinned host->device copy measured in this run",
@@ -1097,8 +1259,7 @@ def run_native_swap(args):
     dist = dist_init(world, True)
     peaks, peak_src = load_peaks()
     metric, unit, hib = metric_for("swap_pipeline")
-    half = (args.seqs or 64) // 2
-    batch = W.mixed_gqa(seed=3, n_resume=half, n_decode=half, poison=False)
+    batch = workload_batch("swap_pipeline", args)
     st = SwapPipelineStep(batch, dev, args.layers)
     h2d = h2d_peak_gbs(dev)
     K, Wm = args.steps, args.warmup
@@ -1188,9 +1349,8 @@ def run_native_swap(args):
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": Wm,
             "ms_per_step": ms["pipelined_staged"], "higher_is_better": hib, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_text("swap_pipeline", args), "layers_resident": Lr,
-                       "l2": "inputs larger than L2 (pool %.1f GB)" % (st.pool.numel() * 2 / 1e9),
-                       "attn_flops_per_step": st.flops, "parallelism": f"replicas x{world}"},
+            "config": workload_config("swap_pipeline", args, world, batch),
+            "pool_gb": st.pool.numel() * 2 / 1e9,
             "roofline": roof, "pipeline": pipe, "cpu_baseline": cpu,
             "e2e": {"value": st.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": unit,
                     "h2d_bytes_per_step": h2d_bytes,
@@ -1209,7 +1369,7 @@ def run_native_layout(args):
     dist = dist_init(world, True)
     peaks, peak_src = load_peaks()
     metric, unit, hib = metric_for("layout")
-    batch = W.decode13b(seed=2, num_seqs=args.seqs or 64, poison=False)
+    batch = workload_batch("layout", args)
     st = LayoutStep(batch, dev, args.layers)
     h2d = h2d_peak_gbs(dev)
     K, Wm = args.steps, args.warmup
@@ -1271,9 +1431,8 @@ def run_native_layout(args):
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": Wm,
             "ms_per_step": ms["attn_block_first"], "higher_is_better": hib, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_text("layout", args), "layers": st.L,
-                       "l2": "inputs larger than L2 (two pools of %.1f GB)" % (st.lf.numel() * 2 / 1e9),
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config("layout", args, world, batch),
+            "pool_gb": st.lf.numel() * 2 / 1e9,
             "roofline": roof,
             "layouts": {"attn_gbs": gbs, "block_first_over_layer_first": gbs["attn_block_first"] / gbs["attn_layer_first"],
                         "ms": {k: round(v, 4) for k, v in ms.items()}, "swap_in": swap},
@@ -1294,6 +1453,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=8,
                     help="kvmove / swap_pipeline: layers resident on the GPU")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="decode13b: leave out the mixed-prefill and long-prefill objects of the line")
     ap.add_argument("--seqs", type=int, default=None,
                     help="number of sequences or sessions (defaults 64 / 64 / 8 / 64; smaller for profiling runs)")
     args = ap.parse_args()
