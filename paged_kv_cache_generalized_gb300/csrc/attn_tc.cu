@@ -48,8 +48,8 @@ constexpr int kKeys = 128;          // keys per KV tile (UMMA N of QK^T, K of PV
 constexpr int kDim = 128;           // head_dim
 constexpr int kPanel = 128 * 128;   // bytes of one 64-column panel of a 128-row tile (16 KiB)
 constexpr int kTile = 2 * kPanel;   // one 128 x 128 16-bit tile (32 KiB)
-constexpr int kThreads = 352;
-constexpr int kKWarp = 0, kMmaWarp = 1, kVWarp = 2, kSoftmax0 = 3;
+constexpr int kThreads = 384;
+constexpr int kKWarp = 0, kMmaWarp = 1, kVWarp = 2, kSoftmax0 = 3, kMma1Warp = 11;
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns of S_u and O_u for query tile u of the pair
 __host__ __device__ constexpr uint32_t tmem_s(int u) { return u ? 128u : 0u; }
@@ -75,10 +75,10 @@ enum Bar {
     kKFull0 = 0, kKEmpty0 = kKFull0 + kKStages, kVFull0 = kKEmpty0 + kKStages,
     kVEmpty0 = kVFull0 + kVStages, kSFull0 = kVEmpty0 + kVStages, kPFull0 = kSFull0 + 2,
     kOReady0 = kPFull0 + 2, kQFull = kOReady0 + 2, kQEmpty, kDrain, kItemFull0, kItemEmpty0 = kItemFull0 + 2,
-    kMerge = kItemEmpty0 + 2, kMergeDone, kNumBars
+    kMerge = kItemEmpty0 + 2, kMergeDone, kTurn0, kNumBars = kTurn0 + 2
 };
 // Items are claimed by the K producer and handed to the other ten warps through a two-slot ring.
-constexpr int kItemConsumers = 2 + 8;
+constexpr int kItemConsumers = 3 + 8;
 static_assert(kNumBars * 8 + 4 + 8 <= 256, "barrier area");
 
 // ---- tcgen05 / TMA wrappers -----------------------------------------------------------------
@@ -406,6 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t count = 1;
             if (b == kPFull0 || b == kPFull0 + 1) count = 4;
             if (b == kItemEmpty0 || b == kItemEmpty0 + 1) count = kItemConsumers;
+            // released by both MMA issuers
+            if ((b >= kKEmpty0 && b < kKEmpty0 + kKStages) || (b >= kVEmpty0 && b < kVEmpty0 + kVStages) ||
+                b == kQEmpty || b == kDrain)
+                count = 2;
             if (b == kMerge || b == kMergeDone) count = 4;
             mbar_init(&bars[b], count);
         }
@@ -509,12 +513,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < nst; ++s)
             if (armed[s]) mbar_wait(&bars[full0 + s], (armed[s] - 1) & 1);
         if (armed_q) mbar_wait(&bars[kQFull], (armed_q - 1) & 1);
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------------ MMA issuer
-        // One thread runs this role: no warp-collective step sits between two MMA groups, so the
-        // tensor pipe is fed as soon as the operands of the next group are ready.
+    } else if (warp == kMmaWarp || warp == kMma1Warp) {
+        // ------------------------------------------------------------------ MMA issuers
+        // One thread per query-tile slot u issues that slot's MMAs (lane 0 of warp 1: slot 0, lane 0
+        // of warp 11: slot 1); the two streams share the tensor core.  A thread's mbarrier check is
+        // ordered behind the MMAs it has issued but the tensor core has not yet accepted, so a lone
+        // issuer leaves the pipe idle at every check; with two, one thread's checks overlap the
+        // other's queued MMAs.  Per 128-key step a thread waits for everything its next two groups
+        // need (V(j), K(j+1), P_u(j)) in a row, then issues PV_u(j) and S_u(j+1) back to back.
+        // S_u(j+1) overwrites the columns PV_u(j) reads P from; both come from the same thread, in
+        // that order, and the tensor core keeps that order.  A commit takes a slot in the tensor
+        // core's queue, so a turn commits once, after S_u(j+1): its completion also means PV_u(j) is
+        // done (a commit tracks every earlier MMA of its thread).  The slot's softmax warps, which
+        // wait for that barrier anyway, release the K stage S_u(j+1) read, the V stage PV_u(j) read
+        // and, after the slot's last S of an item, the Q tiles; the slot's last PV of an item
+        // commits O-ready.  K and V stages are released once per slot (empty barriers of count 2):
+        // for a load its slot does not read, the issuing thread arrives once the load has landed
+        // (so no slot can arrive twice on one stage before the other has arrived once).
+        const int u = warp == kMmaWarp ? 0 : 1;
         if (lane == 0) {
-            uint32_t iter = 0, items = 0, pcount[2] = {0, 0};
+            uint32_t iter = 0, items = 0, pcount = 0;
             bool ok = true;
             const uint32_t q_base = smem_addr(smem + kSmQ), k_base = smem_addr(smem + kSmK),
                            v_base = smem_addr(smem + kSmV);
@@ -524,11 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             auto wait_k = [&](uint32_t g) -> bool { return wait_bar(kKFull0 + g % kKStages, (g / kKStages) & 1); };
+            auto wait_v = [&](uint32_t g) -> bool { return wait_bar(kVFull0 + g % kVStages, (g / kVStages) & 1); };
             // Descriptors are built once; a tile, stage or k-step moves only the start-address
             // field (address / 16, below 2^14 for any shared-memory address).
             const uint64_t dq = smem_desc(q_base, 16, 1024), dk = smem_desc(k_base, 16, 1024),
                            dv = smem_desc(v_base, kPanel, 1024);
-            auto issue_s_from = [&](int u, uint32_t g, int qs) {   // S_u = Q_qs K(g)^T
+            auto issue_s = [&](uint32_t g, int qs) {   // S_u = Q_qs K(g)^T
                 const uint64_t a = dq + (uint64_t)(qs * (kTile >> 4)),
                                b = dk + (uint64_t)((g % kKStages) * (kTile >> 4));
                 const uint32_t d = tmem + tmem_s(u);
@@ -540,9 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(&bars[kSFull0 + u]);
             };
             // O_u += P_u V(g) over the first `ksteps` 16-key steps (P is zero past them)
-            auto issue_pv = [&](int u, uint32_t g, bool first, int ksteps) -> bool {
-                if (!wait_bar(kPFull0 + u, pcount[u] & 1)) return false;
-                ++pcount[u];
+            auto issue_pv = [&](uint32_t g, bool first, int ksteps) {
                 const uint64_t b = dv + (uint64_t)((g % kVStages) * (kTile >> 4));
                 const uint32_t d = tmem + tmem_o(u), a = tmem + tmem_s(u);
                 if (ksteps == kKeys / 16) {
@@ -554,25 +571,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < ksteps; ++k)
                         umma_ts(d, a + k * 8, b + (uint64_t)(k * 128), idesc_pv, (!first || k > 0) ? 1u : 0u);
                 }
-                umma_commit(&bars[kOReady0 + u]);
-                return true;
             };
-            // V rows [first, 16 * ceil(first / 16)) of stage vs (free or stale slots past the last
-            // key, possibly NaN) are zeroed so that P = 0 times them stays 0; returns the 16-key
-            // steps that hold keys
-            auto zero_tail = [&](int vs, int64_t valid) -> int {
+            // The 16-key steps of V stage vs this slot reads when `valid` of its keys are visible, and
+            // the zeroed V rows [first_stale, 16 * steps) under them (slots past the item's last key:
+            // free or stale, possibly NaN; P = 0 times them must stay 0).  Both threads may zero the
+            // same rows; both write zeros.
+            auto v_steps = [&](int vs, int64_t valid, int64_t first_stale) -> int {
                 if (valid >= kKeys) return kKeys / 16;
                 const int ksteps = (int)((valid + 15) / 16);
-                const int first = (int)valid, end = ksteps * 16;
-                unsigned char *vb = smem + kSmV + vs * kTile;
-                for (int r = first; r < end; ++r)
+                const int end = ksteps * 16;
+                if (first_stale < end) {
+                    unsigned char *vb = smem + kSmV + vs * kTile;
+                    for (int r = (int)first_stale; r < end; ++r)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        *reinterpret_cast<uint4 *>(vb + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(vb + kPanel + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                fence_proxy_async_smem();
+                        for (int c = 0; c < 8; ++c) {
+                            *reinterpret_cast<uint4 *>(vb + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(vb + kPanel + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    fence_proxy_async_smem();
+                }
                 return ksteps;
+            };
+            // Turns alternate strictly, slot 0 first: a thread's k-th turn starts once the other
+            // thread has ended its turn before it (turn barrier u is arrived by thread 1 - u).  The
+            // arrive is ordered after the thread's MMAs, so the tensor core receives the groups in
+            // turn order, as from one issuer: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).
+            uint32_t turns = 0;
+            auto take_turn = [&]() -> bool {
+                if (u == 0 && turns == 0) return true;
+                return wait_bar(kTurn0 + u, (u == 0 ? turns - 1 : turns) & 1);
+            };
+            auto end_turn = [&]() {
+                mbar_arrive(&bars[kTurn0 + (1 - u)]);
+                ++turns;
             };
             for (uint32_t n = 0; ok; ++n, ++items) {
                 const int slot = n & 1;
@@ -581,84 +612,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars[kItemEmpty0 + slot]);
                 if (it < 0) break;
                 const Item t = decode_item(p, it);
+                const bool split = t.split;
+                const int cnt = (u == 0 || t.two || split) ? t.nt[u] : 0;   // KV tiles this slot walks
+                const int c0 = t.nt[0], nload = t.nload, kt0 = t.kt0[u];
+                // load index (within the item) of this slot's i-th KV tile
+                auto ld = [&](int i) -> int { return split ? (i < c0 ? 2 * i + u : c0 + i) : i; };
+                const int qs = split ? 0 : u;                  // Q tile of this slot's S
+                // last key any row of this slot sees, and past which V rows of a load are stale
+                const int64_t last_key = split ? (u == 0 ? (int64_t)c0 * kKeys - 1 : t.pmax[0]) : t.pmax[u];
+                const int64_t item_last = split ? last_key : (t.two ? t.pmax[1] : t.pmax[0]);
+                // Releases of the loads this slot does not read: wait for the K (or V) tile to land,
+                // then arrive on its empty barrier.  K and V have their own cursors: the K tile of a
+                // load is released by the step in which some slot's S reads it, the V tile by the
+                // step in which some slot's PV reads it (a V tile released with its K tile would wait
+                // for a PV of the other slot that comes after this thread's turn).
+                int relk = 0, relv = 0;
+                auto mine = [&](int L) -> bool {
+                    // a split's slots alternate over the first 2 c0 loads, slot 1 has the rest;
+                    // otherwise a slot reads loads 0 .. cnt - 1
+                    return cnt > 0 && (split ? (L < 2 * c0 ? (L & 1) == u : u == 1) : L < cnt);
+                };
+                auto release_others = [&](int kupto, int vupto) -> bool {
+                    for (; relk < kupto; ++relk) {
+                        if (mine(relk)) continue;
+                        const uint32_t g = iter + (uint32_t)relk;
+                        if (!wait_k(g)) return false;
+                        mbar_arrive(&bars[kKEmpty0 + g % kKStages]);
+                    }
+                    for (; relv < vupto; ++relv) {
+                        if (mine(relv)) continue;
+                        const uint32_t g = iter + (uint32_t)relv;
+                        if (!wait_v(g)) return false;
+                        mbar_arrive(&bars[kVEmpty0 + g % kVStages]);
+                    }
+                    return true;
+                };
+                // The item's groups in turns: the initial S, then per step PV(i) + S(i + 1); both
+                // threads take 1 + nsteps turns (nsteps = the longer slot's tile count), passing a
+                // turn when their slot has nothing in it.
+                const int nsteps = max(t.nt[0], (t.two || split) ? t.nt[1] : 0);
+                // Loads of the other slot are released step by step, up to the loads any slot reads
+                // in the step: a thread that held them back would keep the producers from refilling
+                // the stages the other thread waits for.  Exclusive bounds; step -1 is the first S.
+                auto kbound = [&](int i) -> int {       // K of every slot's next tile (S(i + 1))
+                    const int b = split ? (i + 1 < c0 ? 2 * i + 4 : c0 + i + 2) : i + 2;
+                    return b < nload ? b : nload;
+                };
+                auto vbound = [&](int i) -> int {       // V of every slot's tile (PV(i))
+                    const int b = i < 0 ? 0 : (split ? (i < c0 ? 2 * i + 2 : c0 + i + 1) : i + 1);
+                    return b < nload ? b : nload;
+                };
                 if (!wait_bar(kQFull, items & 1)) { ok = false; break; }
-                if (t.split) {
-                    // Slot u runs its own KV tiles against Q slot 0, in the order PV_0(i), S_0(i+1),
-                    // PV_1(i), S_1(i+1) of a pair; every S and PV has its own K or V load (load
-                    // position ld(u, i) of the item), released as soon as it is done.
-                    const int c0 = t.nt[0], c1 = t.nt[1];
-                    auto ld = [&](int u, int i) -> uint32_t { return iter + (uint32_t)(i < c0 ? 2 * i + u : c0 + i); };
-                    for (int u = 0; u < 2 && ok; ++u) {
-                        if (!wait_k(ld(u, 0))) { ok = false; break; }
-                        issue_s_from(u, ld(u, 0), 0);
-                        umma_commit(&bars[kKEmpty0 + ld(u, 0) % kKStages]);
+                if (!release_others(kbound(-1), vbound(-1))) { ok = false; break; }
+                if (cnt > 0 && !wait_k(iter + (uint32_t)ld(0))) { ok = false; break; }
+                if (!take_turn()) { ok = false; break; }
+                if (cnt > 0) issue_s(iter + (uint32_t)ld(0), qs);
+                end_turn();
+                for (int i = 0; i < nsteps && ok; ++i) {
+                    const bool has = i < cnt, more = i + 1 < cnt;
+                    const uint32_t g = iter + (uint32_t)(has ? ld(i) : 0);
+                    const uint32_t gn = more ? iter + (uint32_t)ld(i + 1) : 0u;
+                    // everything PV_u(i) and S_u(i+1) need, checked before the turn
+                    if (!release_others(kbound(i), vbound(i))) { ok = false; break; }
+                    if (has) {
+                        if (!wait_v(g)) { ok = false; break; }
+                        if (more && !wait_k(gn)) { ok = false; break; }
+                        if (!wait_bar(kPFull0 + u, pcount & 1)) { ok = false; break; }
+                        ++pcount;
                     }
-                    for (int i = 0; i < c1 && ok; ++i) {
-                        for (int u = 0; u < 2; ++u) {
-                            const int cnt = u ? c1 : c0;
-                            if (i >= cnt) continue;
-                            const uint32_t g = ld(u, i);
-                            const int vs = g % kVStages;
-                            if (!wait_bar(kVFull0 + vs, (g / kVStages) & 1)) { ok = false; break; }
-                            const int ksteps = (u == 1 && i == c1 - 1)
-                                                   ? zero_tail(vs, t.pmax[0] + 1 - (int64_t)(t.kt0[1] + i) * kKeys)
-                                                   : kKeys / 16;
-                            if (!issue_pv(u, g, i == 0, ksteps)) { ok = false; break; }
-                            umma_commit(&bars[kVEmpty0 + vs]);
-                            if (i + 1 < cnt) {
-                                if (!wait_k(ld(u, i + 1))) { ok = false; break; }
-                                issue_s_from(u, ld(u, i + 1), 0);
-                                umma_commit(&bars[kKEmpty0 + ld(u, i + 1) % kKStages]);
-                            }
-                        }
+                    if (!take_turn()) { ok = false; break; }
+                    if (has) {
+                        const int vs = g % kVStages;
+                        const int64_t key0 = (int64_t)(kt0 + i) * kKeys;
+                        const int ksteps = v_steps(vs, last_key + 1 - key0, item_last + 1 - key0);
+                        issue_pv(g, i == 0, ksteps);
+                        if (more) issue_s(gn, qs);
+                        else umma_commit(&bars[kOReady0 + u]);   // the slot's last PV of the item
                     }
-                    if (!ok) break;
-                    umma_commit(&bars[kQEmpty]);
-                    iter += t.nload;
-                    continue;
+                    end_turn();
                 }
-                if (!wait_k(iter)) { ok = false; break; }
-                issue_s_from(0, iter, 0);
-                if (t.two) issue_s_from(1, iter, 1);
-                umma_commit(&bars[kKEmpty0 + iter % kKStages]);
-                for (int kt = 0; kt < t.ntiles; ++kt) {
-                    const uint32_t g = iter + kt;
-                    const bool last = kt + 1 == t.ntiles;
-                    const bool act0 = kt < t.nt[0];
-                    const int vs = g % kVStages;
-                    if (!wait_bar(kVFull0 + vs, (g / kVStages) & 1)) { ok = false; break; }
-                    // Keys past the last one any row of the pair sees have P = 0: PV skips the 16-key
-                    // steps made only of them, and the V rows of such keys inside the last step
-                    // (free or stale slots, possibly NaN) are zeroed so that 0 * V stays 0.
-                    const int64_t valid = (t.two ? t.pmax[1] : t.pmax[0]) + 1 - (int64_t)kt * kKeys;
-                    int ksteps = kKeys / 16;
-                    if (valid < kKeys) {
-                        ksteps = (int)((valid + 15) / 16);
-                        const int first = (int)valid, end = ksteps * 16;
-                        unsigned char *vb = smem + kSmV + vs * kTile;
-                        for (int r = first; r < end; ++r)
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                *reinterpret_cast<uint4 *>(vb + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                                *reinterpret_cast<uint4 *>(vb + kPanel + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                            }
-                        fence_proxy_async_smem();
-                    }
-                    if (act0 && !issue_pv(0, g, kt == 0, ksteps)) { ok = false; break; }
-                    if (!last) {
-                        if (!wait_k(g + 1)) { ok = false; break; }
-                        if (kt + 1 < t.nt[0]) issue_s_from(0, g + 1, 0);
-                    }
-                    if (t.two && !issue_pv(1, g, kt == 0, ksteps)) { ok = false; break; }
-                    umma_commit(&bars[kVEmpty0 + vs]);
-                    if (!last) {
-                        if (t.two) issue_s_from(1, g + 1, 1);
-                        umma_commit(&bars[kKEmpty0 + (g + 1) % kKStages]);
-                    }
-                }
-                // Q is free once every S of the pair is done
-                umma_commit(&bars[kQEmpty]);
-                iter += t.ntiles;
+                if (!ok) break;
+                if (!release_others(nload, nload)) { ok = false; break; }
+                if (cnt == 0) mbar_arrive(&bars[kQEmpty]);
+                iter += nload;
             }
             if (!ok) report(p.status, PA_DEV_TIMEOUT);
             // no tensor-core work of this CTA may be in flight when its tensor memory is freed
@@ -678,13 +714,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) *nsplit = 0;
         __syncwarp();
         uint32_t scount = 0;                           // S / PV tiles of this query tile so far
+        uint32_t ocount = 0;                           // items of this slot so far (O-ready phases)
+        uint32_t iter = 0;                             // K/V loads of the items so far
+        // one thread per slot releases the K/V stages and the Q tiles the slot's MMAs have read
+        const bool releaser = warp == kSoftmax0 + 4 * u && lane == 0;
         bool ok = true;
         for (uint32_t n = 0; ok; ++n) {
             const int it = receive_item(n);
             if (it == -2) { ok = false; break; }
             if (it < 0) break;
             const Item t = decode_item(p, it);
+            const uint32_t item_iter = iter;
+            iter += t.nload;
             if (u == 1 && !t.two && !t.split) continue;
+            // load index of the slot's s-th KV tile (as the MMA issuer counts them)
+            const int c0 = t.nt[0];
+            auto slot_load = [&](int s_) -> uint32_t {
+                return item_iter + (uint32_t)(t.split ? (s_ < c0 ? 2 * s_ + u : c0 + s_) : s_);
+            };
             const int64_t pmin = t.pmin[u], pmax = t.pmax[u];
             const int kt_end = t.kt0[u] + t.nt[u];
             const int j = t.j0[u] + row / p.group, hh = row % p.group;
@@ -694,6 +741,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kt = t.kt0[u]; kt < kt_end; ++kt, ++scount) {
                 if (!warp_wait(&bars[kSFull0 + u], scount & 1)) { ok = false; break; }
                 tc_fence_after();
+                if (releaser) {
+                    // S_u(s) is complete, and with it PV_u(s - 1): their K and V stages are free
+                    const int s_ = kt - t.kt0[u];
+                    mbar_arrive(&bars[kKEmpty0 + slot_load(s_) % kKStages]);
+                    if (s_ > 0) mbar_arrive(&bars[kVEmpty0 + slot_load(s_ - 1) % kVStages]);
+                    if (kt + 1 == kt_end) mbar_arrive(&bars[kQEmpty]);   // the slot's last S
+                }
                 uint32_t raw[kKeys];
                 float *x = reinterpret_cast<float *>(raw);   // raw scores q.k (unscaled)
                 const int64_t key0 = (int64_t)kt * kKeys;
@@ -751,8 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // of its rows must (alpha = 1 for the others), after the previous PV is complete
                 // (l > 0 after the slot's first tile: every row sees a key there)
                 if (l > 0.f && __any_sync(0xffffffffu, rescale)) {
-                    if (!warp_wait(&bars[kOReady0 + u], (scount - 1) & 1)) { ok = false; break; }
-                    tc_fence_after();
+                    // PV_u(s - 1) is complete: it came before S_u(s) from the same issuer
                     const float alpha = rescale ? fast_exp2(m - muse) : 1.f;
                     l *= alpha;
 #pragma unroll 1
@@ -774,8 +827,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // epilogue: O / l -> out, after this tile's last PV
-            if (!warp_wait(&bars[kOReady0 + u], (scount - 1) & 1)) { ok = false; break; }
+            if (!warp_wait(&bars[kOReady0 + u], ocount & 1)) { ok = false; break; }
+            ++ocount;
             tc_fence_after();
+            if (releaser) mbar_arrive(&bars[kVEmpty0 + slot_load(t.nt[u] - 1) % kVStages]);
             const bool store = row < t.rows_valid[u];
             T *orow = reinterpret_cast<T *>(p.out) +
                       ((t.tok0 + j) * p.q_heads + (int64_t)t.kvh * p.group + hh) * kDim;
