@@ -13,22 +13,30 @@
 //   S_t = Q_t K^T   (tcgen05.mma, M=N=128, K=d=128, Q_t and K from shared memory)
 //   P_t = exp2(S_t * scale * log2 e - m_t), causal mask on diagonal tiles only, 16-bit
 //   O_t += P_t V    (tcgen05.mma, P_t from tensor memory (over S_t), V from shared memory)
-// The MMA warp interleaves the two tiles -- PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) -- so the tensor
-// cores work on one tile while the other tile's softmax runs.  The running max is only moved (and
-// O_t rescaled in tensor memory) when it grows by more than 2^8; the final O / l is exact anyway.
+// The tensor core receives the two tiles' groups interleaved -- PV_0(j), S_0(j+1), PV_1(j),
+// S_1(j+1) -- so it works on one tile while the other tile's softmax runs.  Each tile's groups
+// come from their own issuing thread, the two taking turns: an issuer's mbarrier checks queue
+// behind the MMAs it has issued, so one issuer for both tiles left the tensor core idle at every
+// check, while with two, one thread's checks overlap the other's MMAs.  A turn commits once.
+// The running max is only moved (and O_t rescaled in tensor memory) when it grows by more than
+// 2^8; the final O / l is exact anyway.  Tiles below the diagonal take the row max from the
+// reduction form of the tensor-memory load.
 // A lone tile (odd tile count per KV head) with 4 or more KV tiles runs its key range as two
 // halves in the pair's two slots (both from the one Q tile, each half with its own K/V loads),
 // merged in the epilogue by the logsumexp rule, so that it too overlaps softmax with the MMAs.
 //
-// Warp roles (352 threads, one CTA per SM, persistent; items claimed from a global counter):
+// Warp roles (384 threads, one CTA per SM, persistent; items claimed from a global counter):
 //   warp 0      TMA producer for Q (both tiles, once per item) and K: per 128-key tile one 3-D
 //               box (64 columns x B rows of one (block, head)) per block and panel, 128-byte
 //               swizzled, 3 stages; block-table entries of the next tile fetched ahead.
-//   warp 1      MMA issuer (one lane) and tensor-memory owner; zeroes V rows past the last key of
-//               a pair's final tile (those slots may hold anything, NaN included).
+//   warp 1      MMA issuer of tile 0 (one lane) and tensor-memory owner.
+//   warp 11     MMA issuer of tile 1 (one lane).  Each issuer zeroes the V rows past the last
+//               key of an item's final tile that its PV reads (those slots may hold anything,
+//               NaN included).
 //   warp 2      TMA producer for V (2 stages).
 //   warps 3-6   softmax of tile 0, warps 7-10 softmax of tile 1: one thread per row
-//               (tensor-memory lane), S -> P per KV tile, epilogue O / l -> out.
+//               (tensor-memory lane), S -> P per KV tile, epilogue O / l -> out; one warp per
+//               tile also releases the K/V stages and Q tiles its tile's MMAs have finished with.
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
 // Every wait is bounded; on a timeout the role reports PA_DEV_TIMEOUT and stops, the kernel
 // drains what it issued, frees its tensor memory and returns.
@@ -77,7 +85,7 @@ enum Bar {
     kOReady0 = kPFull0 + 2, kQFull = kOReady0 + 2, kQEmpty, kDrain, kItemFull0, kItemEmpty0 = kItemFull0 + 2,
     kMerge = kItemEmpty0 + 2, kMergeDone, kTurn0, kNumBars = kTurn0 + 2
 };
-// Items are claimed by the K producer and handed to the other ten warps through a two-slot ring.
+// Items are claimed by the K producer and handed to the other eleven warps through a two-slot ring.
 constexpr int kItemConsumers = 3 + 8;
 static_assert(kNumBars * 8 + 4 + 8 <= 256, "barrier area");
 
