@@ -183,6 +183,18 @@ def attn_flops(ctx, ql, hq, d):
     return 4.0 * d * hq * pairs
 
 
+TC_MIN_ROWS = 16   # query rows per KV head from which a sequence takes the tensor-core kernel
+
+
+def tc_rows(batch):
+    """Mask of the sequences libpagedkv runs on its tcgen05 kernel (q_len x GQA group >= 16 query
+    rows per KV head, in a batch of a supported shape, scale > 0, same-dtype caches)."""
+    g = batch.num_q_heads // batch.num_kv_heads
+    if not _tc_enabled(batch) or batch.total_q <= batch.num_seqs:
+        return np.zeros(batch.num_seqs, bool)
+    return batch.q_lens.astype(np.int64) * g >= TC_MIN_ROWS
+
+
 def _tc_enabled(batch):
     """Whether libpagedkv routes this batch's multi-token turns to its tensor-core kernel (bf16 or
     f16, head_dim 128, a GQA group dividing 128, blocks of 16..128 tokens)."""
@@ -211,11 +223,15 @@ def attn_accounting(batch, cow_frac=0.0, seed=0, kv8=False):
     Hq, Hkv, d = batch.num_q_heads, batch.num_kv_heads, batch.head_dim
     T = batch.total_q
     nb = (n + B - 1) // B
+    tc = tc_rows(batch) if not kv8 else np.zeros(batch.num_seqs, bool)
     return {"pairs": pairs,
+            "bytes_attn_tc": float(n[tc].sum() * Hkv * d * ek * 2 + 2 * batch.q_lens[tc].sum() * Hq * d * es
+                                   + nb[tc].sum() * 4 + tc.sum() * 8),
             "bytes_attn": float(n.sum() * Hkv * d * ek * 2 + 2 * T * Hq * d * es + nb.sum() * 4 + batch.num_seqs * 8),
             "bytes_append": float(2 * T * Hkv * d * (es + ek) + 8 * T),
             "bytes_copy": float(len(pairs) * 2 * 2 * Hkv * B * d * ek + pairs.size * 8),
             "flops": attn_flops(batch.ctx_lens, batch.q_lens, Hq, d),
+            "flops_tc": attn_flops(batch.ctx_lens[tc], batch.q_lens[tc], Hq, d),
             "pool_bytes": 2 * int(np.prod(batch.k_cache.shape)) * ek}
 
 
@@ -311,7 +327,8 @@ def workload_config(name, args, world, batch):
 
 
 class AttnStep:
-    """block_copy + kv_append + pa_forward over one AttnBatch, all inputs resident on the GPU."""
+    """block_copy + pa_forward_append (the new tokens' K/V into their slots, then the attention)
+    over one AttnBatch, all inputs resident on the GPU."""
 
     def __init__(self, batch: W.AttnBatch, dev, cow_frac=0.0, seed=0, kv8=False):
         import torch
@@ -363,30 +380,34 @@ class AttnStep:
                               dtype=torch.uint8, device=dev)
         self.bytes_attn, self.bytes_append = acct["bytes_attn"], acct["bytes_append"]
         self.bytes_copy, self.flops = acct["bytes_copy"], acct["flops"]
+        self.flops_tc, self.bytes_attn_tc = acct["flops_tc"], acct["bytes_attn_tc"]
         T = batch.total_q
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
         self.d2h_bytes = self.out.numel() * self.out.element_size()
-        # block_copy (if any fork) + kv_append + pa_forward's planner and CUDA-core kernel (which
-        # merges its own splits) (+ the tensor-core kernel when the batch has multi-token turns it
-        # supports)
-        tc = T > batch.num_seqs and _tc_enabled(batch)
-        self.launches_per_step = (1 if len(pairs) else 0) + 1 + 2 + (1 if tc else 0)
+        # block_copy (if any fork) + the planner (whose extra blocks write the new tokens; E4M3
+        # caches take a quantising append launch of their own) + the decode kernel (which merges
+        # its own splits) (+ the tensor-core kernel when some turn takes it)
+        self.has_tc = bool(tc_rows(batch).any()) and not kv8
+        self.launches_per_step = (1 if len(pairs) else 0) + (1 if kv8 else 0) + 2 + (1 if self.has_tc else 0)
 
     def _copy(self, inp):
         if inp["pairs"].shape[0]:
             self.pkg.block_copy(self.pool, self.pool, inp["pairs"])
 
     def step(self, ev=None):
+        """One step; ``ev`` = (call start, call stop, tc start, tc stop, decode start, decode stop)
+        events, the last four recorded by the library around its kernels."""
         inp = self.dev_in
         self._copy(inp)
-        self.pkg.kv_append(inp["k_new"], inp["v_new"], inp["slots"], self.k_cache, self.v_cache,
-                           k_scale=self.ks, v_scale=self.vs)
         if ev is not None:
+            self.pkg.set_timing_events(tc=(ev[2], ev[3]) if self.has_tc else None, cc=(ev[4], ev[5]))
             ev[0].record()
-        self.pkg.pa_forward(inp["q"], self.k_cache, self.v_cache, inp["bt"], inp["ctx"], inp["ql"],
-                            self.b.scale, out=self.out, workspace=self.ws, k_scale=self.ks, v_scale=self.vs)
+        self.pkg.pa_forward_append(inp["q"], inp["k_new"], inp["v_new"], inp["slots"], self.k_cache,
+                                   self.v_cache, inp["bt"], inp["ctx"], inp["ql"], self.b.scale, out=self.out,
+                                   workspace=self.ws, k_scale=self.ks, v_scale=self.vs)
         if ev is not None:
             ev[1].record()
+            self.pkg.set_timing_events()
 
     def e2e_step(self):
         for k2, v in self.host.items():
@@ -1019,7 +1040,12 @@ def measure_attn_workload(name, args, dev, dist, world, local, peaks, peak_src, 
         raise RuntimeError(f"{name}: device status after warm-up: {step_obj.pkg.status_names(flags)}")
 
     K = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kernel_events = isinstance(step_obj, AttnStep)
+    nev = 6 if kernel_events else 2
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(nev)) for _ in range(K)]
+    for e in evs:                   # create every CUDA event before the timed region
+        for x in e:
+            x.record()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize()
@@ -1031,7 +1057,10 @@ def measure_attn_workload(name, args, dev, dist, world, local, peaks, peak_src, 
         torch.cuda.synchronize()
     barrier(dist)
     elapsed_ms = start.elapsed_time(stop)
-    attn_ms = sum(a.elapsed_time(b_) for a, b_ in evs) / K
+    attn_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    # the library-recorded brackets of its tensor-core and decode kernels
+    tc_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K if kernel_events and step_obj.has_tc else None
+    cc_ms = sum(e[4].elapsed_time(e[5]) for e in evs) / K if kernel_events else None
     elapsed_ms = max_over_ranks(dist, elapsed_ms, dev)
     ms_step = elapsed_ms / K
 
@@ -1066,25 +1095,38 @@ def measure_attn_workload(name, args, dev, dist, world, local, peaks, peak_src, 
            "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": step_obj.h2d_bytes,
                    "d2h_bytes_per_step": step_obj.d2h_bytes, "ms_per_step": e2e_ms}}
     if unit == "GB/s":
-        achieved = step_obj.bytes_attn / (attn_ms * 1e-3) / 1e9
+        # the decode kernel alone when the library bracketed it, else the whole attention call
+        kern_ms = cc_ms if cc_ms else attn_ms
+        achieved = step_obj.bytes_attn / (kern_ms * 1e-3) / 1e9
         traffic, tsrc = measured_traffic(name, step_obj.bytes_attn)
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "traffic_source": tsrc,
-                "algorithmic_bytes": step_obj.bytes_attn,
+                "algorithmic_bytes": step_obj.bytes_attn, "kernel_ms": kern_ms,
                 "kernel": getattr(step_obj, "kernel_name",
-                                  "pa_forward (plan + split-KV CUDA-core attention with fused split merge)"),
+                                  "the decode kernel of pa_forward_append (split-KV, fused split merge), "
+                                  "between events the library records around its launch"),
+                "call_ms": attn_ms, "call_achieved": step_obj.bytes_attn / (attn_ms * 1e-3) / 1e9,
                 "peak_source": f"hbm_gbs of {peak_src}"}
         if getattr(step_obj, "bound_note", None):
             roof["note"] = step_obj.bound_note
     else:
-        achieved = step_obj.flops / (attn_ms * 1e-3) / 1e12
         pk = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-        traffic, tsrc = measured_traffic(name, step_obj.bytes_attn)
+        tflops, kern_ms = (step_obj.flops_tc, tc_ms) if tc_ms else (step_obj.flops, attn_ms)
+        achieved = tflops / (kern_ms * 1e-3) / 1e12
+        # DRAM bytes of the tensor-core kernel's launch (its own capture where the call also runs
+        # the decode kernel, else the call's)
+        tbytes = step_obj.bytes_attn_tc if tc_ms else step_obj.bytes_attn
+        traffic, tsrc = measured_traffic(name + "_tc", tbytes)
+        if tsrc is None:
+            traffic, tsrc = measured_traffic(name, tbytes)
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
                 "frac": achieved / pk, "traffic": traffic, "traffic_source": tsrc,
-                "algorithmic_flops": step_obj.flops, "algorithmic_bytes": step_obj.bytes_attn,
-                "kernel": "pa_forward (plan + tcgen05 tensor-core prefill + tensor-core GQA / CUDA-core "
-                          "decode with fused split merge)",
+                "algorithmic_flops": tflops, "kernel_ms": kern_ms,
+                "kernel": "tc_attention_kernel (tcgen05) on the turns it runs, between events the library "
+                          "records around its launch",
+                "call_ms": attn_ms, "call_flops": step_obj.flops,
+                "call_achieved": step_obj.flops / (attn_ms * 1e-3) / 1e12,
+                "decode_bracket_ms": cc_ms, "algorithmic_bytes": tbytes,
                 "peak_source": f"bf16_tflops (burst) of {peak_src}"}
     res["roofline"] = roof
     del step_obj

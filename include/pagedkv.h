@@ -98,12 +98,13 @@ typedef enum { PA_KV_SAME = 0, PA_KV_E4M3 = 1 } pa_kv_dtype;
  * everything else run on the split-KV decode kernels: 2-4 query rows per KV head of bf16/f16
  * caches with d = 128 as mma.m16n8k16 tensor-core fragments (P rounded to the 16-bit type before
  * P V), one row per KV head, E4M3 caches, fp32 and d = 64 on CUDA cores.
- * Streams: when some sequence takes the tensor-core kernel, that kernel runs on a library-owned
- * high-priority stream of the current device, forked from `stream` after the planner and joined
- * back before the call's last kernel, so that the CUDA-core work fills the SMs it leaves.  To the
+ * Streams: when some sequence takes the tensor-core kernel, that kernel runs on `stream` right
+ * after the planner, and the decode kernel runs on a library-owned high-priority stream of the
+ * current device, forked from `stream` after the planner and joined back at the end of the call,
+ * so that the decode work fills the SMs the tensor-core kernel's CTAs leave as they finish.  To the
  * caller the call stays ordered on `stream` (also under stream capture, as a fork/join); host
  * threads that call pa_forward at the same time serialise briefly on the fork/join enqueue, and
- * their tensor-core kernels run one after another on that device's side stream.
+ * their decode kernels of such calls run one after another on that device's side stream.
  * ---------------------------------------------------------------------------------------- */
 typedef struct {
     int32_t dtype;              /* pa_dtype of q, out, k_cache and v_cache */
@@ -127,6 +128,27 @@ pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, co
                      const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
                      float scale, void *out, void *workspace, size_t workspace_bytes,
                      pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * pa_set_timing_events: time the attention kernels of later pa_forward calls with CUDA events.
+ *
+ * Not part of the method: a measurement hook, because the call's kernels run on two streams and
+ * overlap, so events the caller records around the call cannot bracket one kernel.
+ * Each later pa_forward / pa_forward_append / pa_forward_no_alloc call (on any thread, until the
+ * next pa_set_timing_events) records
+ *   tc_start, tc_stop  right before and after the tcgen05 kernel's launch, on the stream it runs
+ *                      on (the caller's; only calls that launch it);
+ *   cc_start, cc_stop  right before and after the launch of the decode kernel (tensor-core GQA
+ *                      or CUDA-core split-KV; every call launches it, after the planner), on the
+ *                      stream it runs on (the side stream when the call also launches the
+ *                      tcgen05 kernel, else the caller's).
+ * cudaEventElapsedTime(start, stop) is then that kernel's device time (plus launch gaps).
+ * Arguments are cudaEvent_t handles created by the caller (timing enabled) on the device of the
+ * later calls, owned by the caller; NULL for both of a pair records nothing.  Returns
+ * PA_ERR_INVALID_ARG (and changes nothing) if only one of a pair is NULL.  A pair re-recorded by
+ * a later call holds the later call's times.
+ * ---------------------------------------------------------------------------------------- */
+pa_status pa_set_timing_events(void *tc_start, void *tc_stop, void *cc_start, void *cc_stop);
 
 /* ------------------------------------------------------------------------------------------
  * pa_forward_no_alloc: pa_forward without a caller-provided workspace.
@@ -196,6 +218,33 @@ typedef struct {
 pa_status kv_append(const kv_append_dims *dims, const void *k_new, const void *v_new,
                     const int64_t *slot_mapping, void *k_cache, void *v_cache,
                     pa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * pa_forward_append: kv_append of the step's new tokens, then pa_forward, in one call.
+ *
+ * The decode or prefill step of "SOSP 2023論文解説: PagedAttention" (sections
+ * "ブロックテーブルによるメモリ管理" and "PagedAttentionアルゴリズム"): the new tokens' K/V go
+ * into their slots, then every new token attends over its sequence's cached-plus-new positions.
+ * Same result as kv_append (one layer, num_tokens = dims->total_q) followed by pa_forward with
+ * the same arguments, bit for bit.  For same-dtype caches the writes are done by extra blocks of
+ * pa_forward's first launch (its planner), so the step costs no launch of its own; E4M3 caches
+ * take a separate quantising kv_append launch first.
+ *
+ *   k_new, v_new  [T, Hkv, d] device arrays of dtype `dims->dtype` (T = dims->total_q: the new
+ *                 tokens are the call's query tokens, in q's order), 16-byte aligned.
+ *   slot_mapping  int64 [T] device array: the token's slot (physical block * B + offset); < 0
+ *                 skips the token; >= num_blocks * B is skipped and flagged PA_DEV_BAD_SLOT.
+ *   k_cache, v_cache  written (the slots) and then read (the attention); other arguments,
+ *                 layouts, supported shapes and the stream behaviour as for pa_forward and
+ *                 kv_append.  The caller's block tables and ctx_lens must already count the new
+ *                 tokens' blocks, as for pa_forward.
+ * Errors: every argument check of kv_append and pa_forward, before any device work.
+ * ---------------------------------------------------------------------------------------- */
+pa_status pa_forward_append(const pa_dims *dims, const void *q, const void *k_new, const void *v_new,
+                            const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                            const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
+                            float scale, void *out, void *workspace, size_t workspace_bytes,
+                            pa_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * block_copy: copy whole blocks, every plane, bit for bit.

@@ -8,4 +8,5 @@ from .pagedkv import (PA_KV_E4M3, PA_KV_SAME, PagedKVError, block_copy, device_s
                       forward_workspace_size, kitty_record_bytes, kitty_workspace_size, kv_append,
                       kv_quantize_pages,
                       library_path, load_library, pa_forward, pa_forward_kitty,
-                      pa_forward_no_alloc, status_names, version)
+                      pa_forward_append, pa_forward_no_alloc, set_timing_events, status_names,
+                      version)

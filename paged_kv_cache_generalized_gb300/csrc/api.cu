@@ -3,10 +3,12 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "kv_append.cuh"
 
 namespace pkv {
 namespace {
@@ -46,7 +48,7 @@ int sm_count() {
 
 namespace {
 
-// A high-priority stream per device on which a call's tensor-core kernel runs beside its CUDA-core
+// A high-priority stream per device on which a call's decode kernel runs beside its tensor-core
 // kernel, with the events that fork it from and join it back to the caller's stream.  Created on
 // first use and kept until exit; the fork/join enqueue is serialised across host threads.
 struct SideStream {
@@ -54,6 +56,15 @@ struct SideStream {
     cudaEvent_t fork = nullptr, join = nullptr;
 };
 std::mutex g_side_mu;
+
+// Caller-owned CUDA events recorded around the attention kernels of later calls
+// (pa_set_timing_events): tensor-core kernel start / stop, CUDA-core kernel start / stop.
+std::atomic<void *> g_timing[4];
+
+bool record_timing(int which, cudaStream_t st) {
+    void *e = g_timing[which].load(std::memory_order_relaxed);
+    return !e || cudaEventRecord(static_cast<cudaEvent_t>(e), st) == cudaSuccess;
+}
 
 SideStream *side_stream() {
     static SideStream side[kMaxDevices];
@@ -199,10 +210,14 @@ size_t pa_forward_workspace_size(const pa_dims *dims) {
     return ws_layout(*dims).total;
 }
 
-pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
-                     const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
-                     float scale, void *out, void *workspace, size_t workspace_bytes,
-                     pa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The argument checks of pa_forward, before any device work.
+pa_status forward_checks(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
+                         float scale, const void *out, const void *workspace, size_t workspace_bytes) {
     const pa_status st = check_dims(dims);
     if (st != PA_OK) return st;
     const pa_dims &d = *dims;
@@ -217,6 +232,20 @@ pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, co
     if (overlap(q, rows_bytes, out, rows_bytes)) return PA_ERR_INVALID_ARG;
     const WsLayout lay = ws_layout(d);
     if (!workspace || workspace_bytes < lay.total || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+    return PA_OK;
+}
+
+// pa_forward, with the step's new tokens optionally written by the planner's launch (`append`,
+// same-dtype caches) before the attention kernels run.
+pa_status forward_impl(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
+                       float scale, void *out, void *workspace, size_t workspace_bytes, pa_stream_t stream,
+                       const AppendParams *append) {
+    const pa_status st = forward_checks(dims, q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale, out,
+                                        workspace, workspace_bytes);
+    if (st != PA_OK) return st;
+    const pa_dims &d = *dims;
+    const WsLayout lay = ws_layout(d);
     FwdArgs a;
     a.dims = d;
     a.q = q;
@@ -234,24 +263,93 @@ pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, co
     if (!a.status || a.num_sms <= 0) return PA_ERR_CUDA;
     a.maybe_prefill = d.total_q > d.num_seqs;
     a.tc = a.maybe_prefill && scale > 0.f && d.kv_dtype == PA_KV_SAME && tc_supported(d);
+    AppendParams ap;
+    if (append) {
+        ap = *append;
+        ap.status = a.status;
+        a.append = &ap;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (launch_plan(a, s) != cudaSuccess) return PA_ERR_CUDA;
     if (a.tc) {
-        // tensor-core tiles on the high-priority side stream; the CUDA-core items take the SMs
-        // its CTAs leave; both only read the plan and write disjoint output rows
+        // the tensor-core kernel right after the planner on the caller's stream, so that its CTAs
+        // (one per SM, each holding the SM's whole register file) are dispatched first; the decode
+        // kernel, forked onto the side stream, takes each SM as its tensor-core CTA finishes.  Both
+        // only read the plan and write disjoint output rows.
         std::lock_guard<std::mutex> lock(g_side_mu);
         SideStream *x = side_stream();
         if (!x) return PA_ERR_CUDA;
         if (cudaEventRecord(x->fork, s) != cudaSuccess || cudaStreamWaitEvent(x->stream, x->fork, 0) != cudaSuccess)
             return PA_ERR_CUDA;
-        if (launch_tc(a, x->stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_simt(a, s) != cudaSuccess) return PA_ERR_CUDA;
+        if (!record_timing(0, s) || launch_tc(a, s) != cudaSuccess || !record_timing(1, s)) return PA_ERR_CUDA;
+        if (!record_timing(2, x->stream) || launch_simt(a, x->stream) != cudaSuccess || !record_timing(3, x->stream))
+            return PA_ERR_CUDA;
         if (cudaEventRecord(x->join, x->stream) != cudaSuccess || cudaStreamWaitEvent(s, x->join, 0) != cudaSuccess)
             return PA_ERR_CUDA;
-    } else if (launch_simt(a, s) != cudaSuccess) {
+    } else if (!record_timing(2, s) || launch_simt(a, s) != cudaSuccess || !record_timing(3, s)) {
         return PA_ERR_CUDA;
     }
     return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_set_timing_events(void *tc_start, void *tc_stop, void *cc_start, void *cc_stop) {
+    if (!tc_start != !tc_stop || !cc_start != !cc_stop) return PA_ERR_INVALID_ARG;
+    g_timing[0].store(tc_start);
+    g_timing[1].store(tc_stop);
+    g_timing[2].store(cc_start);
+    g_timing[3].store(cc_stop);
+    return PA_OK;
+}
+
+pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
+                     float scale, void *out, void *workspace, size_t workspace_bytes,
+                     pa_stream_t stream) {
+    return forward_impl(dims, q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale, out, workspace,
+                        workspace_bytes, stream, nullptr);
+}
+
+pa_status pa_forward_append(const pa_dims *dims, const void *q, const void *k_new, const void *v_new,
+                            const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                            const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,
+                            float scale, void *out, void *workspace, size_t workspace_bytes,
+                            pa_stream_t stream) {
+    const pa_status st = forward_checks(dims, q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale, out,
+                                        workspace, workspace_bytes);
+    if (st != PA_OK) return st;
+    const pa_dims &d = *dims;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8)) return PA_ERR_INVALID_ARG;
+    // the new tokens are the call's query tokens: [total_q, Hkv, d] of dims->dtype
+    kv_append_dims ad;
+    ad.dtype = d.dtype;
+    ad.num_tokens = d.total_q;
+    ad.num_kv_heads = d.num_kv_heads;
+    ad.head_dim = d.head_dim;
+    ad.block_size = d.block_size;
+    ad.num_blocks = d.num_blocks;
+    ad.kv_block_stride = d.kv_block_stride;
+    ad.num_layers = 1;
+    ad.new_layer_stride = 0;
+    ad.cache_layer_stride = 0;
+    ad.kv_dtype = d.kv_dtype;
+    ad.k_scale = d.k_scale;
+    ad.v_scale = d.v_scale;
+    if (d.kv_dtype == PA_KV_E4M3) {
+        // quantising append: its own launch, then the attention call
+        const pa_status sa = kv_append(&ad, k_new, v_new, slot_mapping, k_cache, v_cache, stream);
+        if (sa != PA_OK) return sa;
+        return forward_impl(dims, q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale, out, workspace,
+                            workspace_bytes, stream, nullptr);
+    }
+    AppendParams ap;
+    fill_append_params(ad, k_new, v_new, slot_mapping, k_cache, v_cache, nullptr, ap);
+    return forward_impl(dims, q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale, out, workspace,
+                        workspace_bytes, stream, &ap);
 }
 
 pa_status kv_append(const kv_append_dims *dims, const void *k_new, const void *v_new,

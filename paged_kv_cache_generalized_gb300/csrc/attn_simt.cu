@@ -28,6 +28,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "kv_append.cuh"
 
 namespace pkv {
 namespace {
@@ -51,6 +52,7 @@ struct PlanParams {
 };
 
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanAppendUnroll = 2;
 
 // In-place exclusive scan of a[0..n) (a[n] receives the total), one CTA.
 __device__ int64_t block_exclusive_scan(int32_t *a, int n) {
@@ -93,7 +95,13 @@ __device__ int64_t block_exclusive_scan(int32_t *a, int n) {
     return total;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
+// Block 0 plans; with a fused append (pa_forward_append) the other blocks write the step's new
+// tokens into the caches meanwhile, so the attention kernels launched after this one read them.
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p, AppendParams ap) {
+    if (blockIdx.x > 0) {   // the fused cache append (two units per thread fit 64 registers)
+        append_loop<kPlanAppendUnroll>(ap, blockIdx.x - 1, gridDim.x - 1);
+        return;
+    }
     __shared__ int64_t red[32];
     const int tid = threadIdx.x;
     const int S = p.num_seqs;
@@ -1477,7 +1485,16 @@ cudaError_t launch_plan(const FwdArgs &a, cudaStream_t s) {
     p.rows = L.rows_per_item;
     p.tc = a.tc ? 1 : 0;
     p.total_warps = a.num_sms * 8;
-    plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+    AppendParams ap{};
+    int64_t grid = 1;
+    if (a.append && a.append->total_units > 0) {
+        ap = *a.append;
+        const int64_t per_cta = (int64_t)kPlanThreads * kPlanAppendUnroll;
+        int64_t n = (ap.total_units + per_cta - 1) / per_cta;
+        n = n < (int64_t)a.num_sms * 2 ? n : (int64_t)a.num_sms * 2;
+        grid += n;
+    }
+    plan_kernel<<<(unsigned)grid, kPlanThreads, 0, s>>>(p, ap);
     return cudaGetLastError();
 }
 

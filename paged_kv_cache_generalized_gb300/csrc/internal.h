@@ -66,6 +66,8 @@ int rows_per_item(const pa_dims &d);
 bool tc_supported(const pa_dims &d);
 bool tc_shape_supported(const pa_dims &d);  // attn_tc.cu
 
+struct AppendParams;    // kv_append.cuh
+
 struct FwdArgs {
     pa_dims dims;
     const void *q;
@@ -82,6 +84,7 @@ struct FwdArgs {
     int num_sms;
     bool tc;            // tensor-core kernel available for this call
     bool maybe_prefill; // some sequence may have q_len > 1
+    const AppendParams *append = nullptr;   // new tokens written by the planner's launch (or none)
 };
 
 cudaError_t launch_plan(const FwdArgs &a, cudaStream_t s);
@@ -91,6 +94,9 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_kv_append(const kv_append_dims &d, const void *k_new, const void *v_new,
                              const int64_t *slots, void *k_cache, void *v_cache, unsigned *status,
                              int num_sms, cudaStream_t s);
+// The same-dtype append's parameters (kv_move.cu); d.kv_dtype must be PA_KV_SAME.
+void fill_append_params(const kv_append_dims &d, const void *k_new, const void *v_new, const int64_t *slots,
+                        void *k_cache, void *v_cache, unsigned *status, AppendParams &p);
 cudaError_t launch_block_copy(const block_copy_dims &d, const void *src, void *dst,
                               const int64_t *pairs, unsigned *status, int num_sms,
                               cudaStream_t s);

@@ -9,73 +9,13 @@
 // Serving with Pensieve", sections "GPU-CPU 2層キャッシュ構造" / "パイプライン化されたswap-in".
 #include "common.cuh"
 #include "internal.h"
+#include "kv_append.cuh"
 
 namespace pkv {
 namespace {
 
-struct AppendParams {
-    const uint4 *k_new;
-    const uint4 *v_new;
-    const int64_t *slots;
-    uint4 *k_cache;
-    uint4 *v_cache;
-    unsigned *status;
-    int64_t num_tokens;
-    int64_t units_per_layer;   // num_tokens * Hkv * chunks
-    int64_t total_units;       // * num_layers
-    int64_t num_blocks;
-    int64_t block_stride16;    // 16-byte units between physical blocks
-    int64_t new_layer16;       // 16-byte units between layers of k_new / v_new
-    int64_t cache_layer16;     // 16-byte units between layers of the caches
-    int32_t kv_heads;
-    int32_t chunks;            // 16-byte units per (token, head) row: d * elem / 16
-    int32_t block_size;
-};
-
-constexpr int kAppendUnroll = 4;
-
-// One thread moves kAppendUnroll 16-byte units of K and of V per iteration (all loads issued
-// before the stores).  Unit u -> (layer, token, head, chunk) with chunk fastest, so consecutive
-// threads read consecutive bytes of k_new and write one contiguous row of a cache block.
-__global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x * kAppendUnroll;
-    for (int64_t base = ((int64_t)blockIdx.x * blockDim.x) * kAppendUnroll + threadIdx.x;
-         base < p.total_units; base += stride) {
-        uint4 kv[kAppendUnroll], vv[kAppendUnroll];
-        int64_t dst[kAppendUnroll];
-#pragma unroll
-        for (int k = 0; k < kAppendUnroll; ++k) {
-            const int64_t u = base + (int64_t)k * blockDim.x;
-            dst[k] = -1;
-            if (u >= p.total_units) continue;
-            const int64_t layer = u / p.units_per_layer;
-            const int64_t in_layer = u - layer * p.units_per_layer;
-            const int64_t row = in_layer / p.chunks;           // token * Hkv + head
-            const int c = (int)(in_layer - row * p.chunks);
-            const int64_t t = row / p.kv_heads;
-            const int h = (int)(row - t * p.kv_heads);
-            const int64_t slot = __ldg(p.slots + t);
-            if (slot < 0) continue;                             // padding
-            const int64_t blk = slot / p.block_size;
-            if (blk >= p.num_blocks) {
-                if (c == 0 && h == 0 && layer == 0) report(p.status, PA_DEV_BAD_SLOT);
-                continue;
-            }
-            const int off = (int)(slot - blk * p.block_size);
-            const int64_t src = layer * p.new_layer16 + row * p.chunks + c;
-            dst[k] = layer * p.cache_layer16 + blk * p.block_stride16 +
-                     ((int64_t)h * p.block_size + off) * p.chunks + c;
-            kv[k] = __ldcs(p.k_new + src);
-            vv[k] = __ldcs(p.v_new + src);
-        }
-#pragma unroll
-        for (int k = 0; k < kAppendUnroll; ++k) {
-            if (dst[k] < 0) continue;
-            p.k_cache[dst[k]] = kv[k];
-            p.v_cache[dst[k]] = vv[k];
-        }
-    }
-}
+// The same-dtype append (kv_append.cuh's loop over the whole grid).
+__global__ void __launch_bounds__(256) kv_append_kernel(AppendParams p) { append_loop(p, blockIdx.x, gridDim.x); }
 
 // E4M3 caches: the new tokens (bf16 / f16 / f32) are quantised on the way in.  One unit is 16
 // consecutive elements of one (layer, token, head) row: read, widened to fp32, multiplied by the
@@ -226,13 +166,9 @@ cudaError_t launch_kv_append_e4m3(const kv_append_dims &d, const void *k_new, co
 
 }  // namespace
 
-cudaError_t launch_kv_append(const kv_append_dims &d, const void *k_new, const void *v_new,
-                             const int64_t *slots, void *k_cache, void *v_cache, unsigned *status,
-                             int num_sms, cudaStream_t s) {
-    if (d.kv_dtype == PA_KV_E4M3)
-        return launch_kv_append_e4m3(d, k_new, v_new, slots, k_cache, v_cache, status, num_sms, s);
+void fill_append_params(const kv_append_dims &d, const void *k_new, const void *v_new, const int64_t *slots,
+                        void *k_cache, void *v_cache, unsigned *status, AppendParams &p) {
     const int eb = elem_bytes(d.dtype);
-    AppendParams p;
     p.k_new = static_cast<const uint4 *>(k_new);
     p.v_new = static_cast<const uint4 *>(v_new);
     p.slots = slots;
@@ -253,6 +189,15 @@ cudaError_t launch_kv_append(const kv_append_dims &d, const void *k_new, const v
     p.cache_layer16 = cls * eb / 16;
     p.units_per_layer = d.num_tokens * d.num_kv_heads * (int64_t)p.chunks;
     p.total_units = p.units_per_layer * d.num_layers;
+}
+
+cudaError_t launch_kv_append(const kv_append_dims &d, const void *k_new, const void *v_new,
+                             const int64_t *slots, void *k_cache, void *v_cache, unsigned *status,
+                             int num_sms, cudaStream_t s) {
+    if (d.kv_dtype == PA_KV_E4M3)
+        return launch_kv_append_e4m3(d, k_new, v_new, slots, k_cache, v_cache, status, num_sms, s);
+    AppendParams p;
+    fill_append_params(d, k_new, v_new, slots, k_cache, v_cache, status, p);
     if (p.total_units == 0) return cudaSuccess;
     const int64_t per_cta = 256LL * kAppendUnroll;
     int64_t grid = (p.total_units + per_cta - 1) / per_cta;

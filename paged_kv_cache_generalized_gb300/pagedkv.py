@@ -31,7 +31,7 @@ PA_KV_SAME, PA_KV_E4M3 = 0, 1
 _E4M3 = tuple(t for t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if t is not None)
 _ELEM = {torch.float32: 4, torch.bfloat16: 2, torch.float16: 2}
 
-EXPORTED = ("pa_forward_workspace_size", "pa_forward", "pa_forward_no_alloc", "kv_append",
+EXPORTED = ("pa_forward_workspace_size", "pa_forward", "pa_forward_no_alloc", "pa_forward_append", "pa_set_timing_events", "kv_append",
             "block_copy", "pa_get_device_status", "pa_status_string", "pa_version",
             "pa_kitty_record_bytes", "pa_kitty_workspace_size", "kv_quantize_pages",
             "pa_forward_kitty")
@@ -99,6 +99,11 @@ def load_library(path: str | None = None):
     lib.pa_forward_no_alloc.restype = ctypes.c_int
     lib.pa_forward_no_alloc.argtypes = [ctypes.POINTER(PaDims), P, P, P, P, P, P, ctypes.c_float,
                                         P, P]
+    lib.pa_forward_append.restype = ctypes.c_int
+    lib.pa_forward_append.argtypes = [ctypes.POINTER(PaDims), P, P, P, P, P, P, P, P, P,
+                                      ctypes.c_float, P, P, sz, P]
+    lib.pa_set_timing_events.restype = ctypes.c_int
+    lib.pa_set_timing_events.argtypes = [P, P, P, P]
     lib.kv_append.restype = ctypes.c_int
     lib.kv_append.argtypes = [ctypes.POINTER(KvAppendDims), P, P, P, P, P, P]
     lib.block_copy.restype = ctypes.c_int
@@ -233,6 +238,67 @@ def pa_forward_no_alloc(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, sca
                                  ctypes.c_float(scale), _ptr(out), _stream(stream))
     _check(rc, "pa_forward_no_alloc")
     return out
+
+
+def _append_args(q, k_new, v_new, slot_mapping, k_cache):
+    """Checks the new-token arguments of pa_forward_append (raises ValueError)."""
+    T, _, d = q.shape
+    hkv = k_cache.shape[1]
+    if k_new.shape != (T, hkv, d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must be [T, Hkv, d] with q's T and d")
+    if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise ValueError("k_new and v_new must have q's dtype")
+    if not k_new.is_contiguous() or not v_new.is_contiguous():
+        raise ValueError("k_new and v_new must be contiguous")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.shape != (T,) or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous int64 [T]")
+
+
+def pa_forward_append(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, ctx_lens, q_lens,
+                      scale=None, out=None, workspace=None, stream=None, k_scale=None, v_scale=None):
+    """Writes the step's new tokens into their slots, then runs pa_forward (see
+    ``pa_forward_append`` in include/pagedkv.h); same result as ``kv_append`` followed by
+    ``pa_forward``.  k_new/v_new: [T, Hkv, d] in q's dtype, one row per query token;
+    slot_mapping: int64 [T].  Returns ``out``."""
+    dims = _forward_args(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, k_scale, v_scale)
+    _append_args(q, k_new, v_new, slot_mapping, k_cache)
+    lib = load_library()
+    if scale is None:
+        scale = 1.0 / float(dims.head_dim) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    need = int(lib.pa_forward_workspace_size(ctypes.byref(dims)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.pa_forward_append(ctypes.byref(dims), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                               _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(ctx_lens),
+                               _ptr(q_lens), ctypes.c_float(scale), _ptr(out), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "pa_forward_append")
+    return out
+
+
+def _event_handle(ev):
+    """Raw cudaEvent_t of a torch.cuda.Event (recorded once on the current stream first, since
+    torch creates the CUDA event at its first record)."""
+    if ev is None:
+        return None
+    if not ev.cuda_event:
+        ev.record()
+    return ctypes.c_void_p(ev.cuda_event)
+
+
+def set_timing_events(tc=None, cc=None):
+    """Records (start, stop) torch.cuda.Event pairs around the attention kernels of later calls
+    (see ``pa_set_timing_events`` in include/pagedkv.h): ``tc`` around the tcgen05 kernel, ``cc``
+    around the decode kernel, each on the stream that kernel runs on.  None stops recording that
+    pair."""
+    lib = load_library()
+    ts, te = (None, None) if tc is None else tc
+    cs, ce = (None, None) if cc is None else cc
+    rc = lib.pa_set_timing_events(_event_handle(ts), _event_handle(te), _event_handle(cs),
+                                  _event_handle(ce))
+    _check(rc, "pa_set_timing_events")
 
 
 def kitty_record_bytes(promoted: int, head_dim: int = 128) -> int:

@@ -109,6 +109,36 @@ def test_forward_rejects_null_and_misaligned_pointers(lib):
     assert rc == 1
 
 
+def test_forward_append_rejects_bad_arguments(lib):
+    """pa_forward_append runs pa_forward's checks and the append's own, all before device work."""
+    d = _dims()
+    W = ctypes.c_void_p(0x40000)
+    out = ctypes.c_void_p(0x20000)
+
+    def call(dims, q=FAKE, kn=FAKE, vn=FAKE, sm=FAKE, ws=W, wsb=1 << 30):
+        return lib.pa_forward_append(ctypes.byref(dims), q, kn, vn, sm, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                     ctypes.c_float(0.1), out, ws, wsb, None)
+
+    assert call(_dims(num_q_heads=6, num_kv_heads=4)) == 1          # pa_forward's dims check
+    assert call(_dims(head_dim=96)) == 2
+    assert call(d, kn=None) == 1                                     # no new K
+    assert call(d, sm=None) == 1                                     # no slot mapping
+    assert call(d, vn=ctypes.c_void_p(0x10008)) == 1                 # new V not 16-byte aligned
+    assert call(d, sm=ctypes.c_void_p(0x10004)) == 1                 # slots not 8-byte aligned
+    need = lib.pa_forward_workspace_size(ctypes.byref(d))
+    assert call(d, wsb=need - 1) == 3                                # workspace checked first
+    assert call(d, q=out) == 1                                       # out aliasing q
+    e = _dims(kv_dtype=1, k_scale=0.0, v_scale=1.0)                  # E4M3 without a valid scale
+    assert call(e) == 1
+
+
+def test_timing_events_refuse_half_pairs(lib):
+    """A start without a stop (or the reverse) is refused and changes nothing; all NULL clears."""
+    assert lib.pa_set_timing_events(FAKE, None, None, None) == 1
+    assert lib.pa_set_timing_events(None, None, None, FAKE) == 1
+    assert lib.pa_set_timing_events(None, None, None, None) == 0
+
+
 def test_append_and_copy_reject_bad_arguments(lib):
     from paged_kv_cache_generalized_gb300.pagedkv import BlockCopyDims, KvAppendDims
 

@@ -45,3 +45,35 @@ def test_good_arguments_pass_the_checks():
                             a["q_lens"], None, None)
     assert (dims.num_seqs, dims.total_q, dims.num_q_heads, dims.num_kv_heads) == (2, 3, 8, 2)
     assert (dims.head_dim, dims.block_size, dims.num_blocks, dims.max_blocks_per_seq) == (128, 16, 10, 4)
+
+
+BAD_APPEND = {
+    "k_new rows differ from q": dict(k_new=torch.zeros(2, 2, 128, dtype=torch.bfloat16)),
+    "k_new heads differ from caches": dict(k_new=torch.zeros(3, 4, 128, dtype=torch.bfloat16)),
+    "v_new shape differs": dict(v_new=torch.zeros(3, 2, 64, dtype=torch.bfloat16)),
+    "k_new dtype differs from q": dict(k_new=torch.zeros(3, 2, 128, dtype=torch.float16)),
+    "non-contiguous v_new": dict(v_new=torch.zeros(3, 128, 2, dtype=torch.bfloat16).transpose(1, 2)),
+    "int32 slot mapping": dict(slot_mapping=torch.zeros(3, dtype=torch.int32)),
+    "slot mapping too short": dict(slot_mapping=torch.zeros(2, dtype=torch.int64)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(BAD_APPEND))
+def test_forward_append_refuses_bad_new_tokens(case):
+    a = _args()
+    a.update(k_new=torch.zeros(3, 2, 128, dtype=torch.bfloat16),
+             v_new=torch.zeros(3, 2, 128, dtype=torch.bfloat16),
+             slot_mapping=torch.zeros(3, dtype=torch.int64))
+    a.update(BAD_APPEND[case])
+    with pytest.raises(ValueError):
+        pk.pa_forward_append(**a)
+
+
+@pytest.mark.parametrize("case", sorted(BAD))
+def test_forward_append_refuses_what_pa_forward_refuses(case):
+    a = _args(**BAD[case])
+    a.update(k_new=torch.zeros(3, 2, 128, dtype=torch.bfloat16),
+             v_new=torch.zeros(3, 2, 128, dtype=torch.bfloat16),
+             slot_mapping=torch.zeros(3, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        pk.pa_forward_append(**a)
