@@ -21,9 +21,7 @@
 // The running max is only moved (and O_t rescaled in tensor memory) when it grows by more than
 // 2^8; the final O / l is exact anyway.  Tiles below the diagonal take the row max from the
 // reduction form of the tensor-memory load.
-// A lone tile (odd tile count per KV head) with 4 or more KV tiles runs its key range as two
-// halves in the pair's two slots (both from the one Q tile, each half with its own K/V loads),
-// merged in the epilogue by the logsumexp rule, so that it too overlaps softmax with the MMAs.
+// A lone tile (odd tile count per KV head) runs in slot 0 alone; slot 1 passes its turns.
 //
 // Warp roles (384 threads, one CTA per SM, persistent; items claimed from a global counter):
 //   warp 0      TMA producer for Q (both tiles, once per item) and K: per 128-key tile one 3-D
@@ -72,18 +70,13 @@ constexpr int kSmQ = 0;                          // two Q tiles
 constexpr int kSmK = kSmQ + 2 * kTile;
 constexpr int kSmV = kSmK + kKStages * kTile;
 constexpr int kSmBar = kSmV + kVStages * kTile;
-constexpr int kSmMerge = kSmBar + 256;           // (m, l) of a split tile's second half, per row
-constexpr int kSmBytes = kSmMerge + kRows * 8 + 64 + 1024;   // + split counters, alignment slack
-// A lone query tile (no partner tile in its sequence and KV head) with at least this many KV
-// tiles is split: the two halves of its key range run as the pair's two tiles and are merged
-// in the epilogue, so its softmax overlaps the tensor cores as a pair's does.
-constexpr int kSplitMinTiles = 4;
+constexpr int kSmBytes = kSmBar + 256 + 1024;   // + alignment slack
 
 enum Bar {
     kKFull0 = 0, kKEmpty0 = kKFull0 + kKStages, kVFull0 = kKEmpty0 + kKStages,
     kVEmpty0 = kVFull0 + kVStages, kSFull0 = kVEmpty0 + kVStages, kPFull0 = kSFull0 + 2,
     kOReady0 = kPFull0 + 2, kQFull = kOReady0 + 2, kQEmpty, kDrain, kItemFull0, kItemEmpty0 = kItemFull0 + 2,
-    kMerge = kItemEmpty0 + 2, kMergeDone, kTurn0, kNumBars = kTurn0 + 2
+    kTurn0 = kItemEmpty0 + 2, kNumBars = kTurn0 + 2
 };
 // Items are claimed by the K producer and handed to the other eleven warps through a two-slot ring.
 constexpr int kItemConsumers = 3 + 8;
@@ -264,15 +257,12 @@ struct TcParams {
 
 // One work item: query tiles qt0 = 2*pi and qt1 = 2*pi + 1 (if it exists) of one (sequence,
 // KV head).  Tile 1 holds later rows, so its causal range (and KV tile count) covers tile 0's.
-// A split item is one query tile whose key range runs in two halves, KV tiles [0, h) in slot 0
-// and [h, nt) in slot 1 (kt0 = first KV tile of each slot), both slots using query tile 0.
+// The item loads KV tiles 0 .. ntiles - 1 once, in order; both slots read them from tile 0.
 struct Item {
-    int seq, kvh, ntiles;         // ntiles: MMA steps (KV tiles of the longer slot)
-    int nload;                    // K (and V) tiles loaded for the item
+    int seq, kvh, ntiles;         // ntiles: KV tiles loaded = MMA steps (the longer slot's count)
     int64_t tok0;
     bool two;                     // tile 1 exists
-    bool split;                   // a lone tile run as two halves of its key range
-    int j0[2], rows_valid[2], nt[2], kt0[2];
+    int j0[2], rows_valid[2], nt[2];
     int64_t pmin[2], pmax[2];
 };
 
@@ -298,25 +288,8 @@ __device__ __forceinline__ Item decode_item(const TcParams &p, int it) {
         t.pmax[u] = c + t.j0[u] + (t.rows_valid[u] - 1) / p.group;
         t.nt[u] = (int)((t.pmax[u] + kKeys) / kKeys);
     }
-    t.split = !t.two && t.nt[0] >= kSplitMinTiles;
-    t.kt0[0] = t.kt0[1] = 0;
-    if (t.split) {
-        const int h = t.nt[0] / 2;
-        t.kt0[1] = h;
-        t.nt[1] = t.nt[0] - h;
-        t.nt[0] = h;
-    }
-    t.ntiles = t.two || t.split ? t.nt[1] : t.nt[0];
-    t.nload = t.split ? t.nt[0] + t.nt[1] : t.ntiles;
+    t.ntiles = t.two ? t.nt[1] : t.nt[0];
     return t;
-}
-
-// KV tile of an item's ld-th K/V load.  A split item interleaves its halves: load 2i + u is
-// slot u's i-th tile while both slots run, then slot 1's remaining tiles follow in order.
-__device__ __forceinline__ int load_tile(const Item &t, int ld) {
-    if (!t.split) return ld;
-    const int c0 = t.nt[0];
-    return ld < 2 * c0 ? ((ld & 1) ? c0 + (ld >> 1) : (ld >> 1)) : ld;
 }
 
 // Physical block of each lane's block in KV tile kt (lanes < blocks of the tile), clamped.
@@ -334,64 +307,6 @@ __device__ __forceinline__ int tile_block(const TcParams &p, const int32_t *bt_r
         }
     }
     return phys;
-}
-
-// Epilogue of a split tile (a lone query tile whose key range ran as two halves, one per slot).
-// The slot-1 warp hands its rows' (m, l) to the slot-0 warp of the same tensor-memory lanes and
-// waits until that warp has read its O; the slot-0 warp merges the halves with the logsumexp
-// rule, out = (2^(m0-M) O_0 + 2^(m1-M) O_1) / (2^(m0-M) l_0 + 2^(m1-M) l_1), M = max(m0, m1)
-// (both finite: every row sees keys in both halves), and writes the row (orow, if stored).
-// Returns false if a wait timed out.  Not inlined, so that the softmax loop's registers are
-// allocated without it.
-template <typename T>
-__device__ __noinline__ bool split_epilogue(int u, uint64_t *bars, float2 *merge_ml, uint32_t *nsplit, int row,
-                                            int lane, uint32_t lane_base, float m, float l, T *orow) {
-    const uint32_t ns = *nsplit;
-    if (u == 1) {
-        merge_ml[row] = make_float2(m, l);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kMerge]);
-        const bool merged = warp_wait(&bars[kMergeDone], ns & 1);
-        if (lane == 0) *nsplit = ns + 1;
-        __syncwarp();
-        tc_fence_after();
-        return merged;
-    }
-    if (!warp_wait(&bars[kMerge], ns & 1)) return false;
-    if (lane == 0) *nsplit = ns + 1;
-    __syncwarp();
-    tc_fence_after();
-    const float2 ml1 = merge_ml[row];
-    const float M = fmaxf(m, ml1.x);
-    const float w0 = fast_exp2(m - M), w1 = fast_exp2(ml1.x - M);
-    const float inv = 1.f / (w0 * l + w1 * ml1.y);
-    const float a0 = w0 * inv, a1 = w1 * inv;
-#pragma unroll 1
-    for (int c = 0; c < kDim / 32; ++c) {
-        uint32_t r0[32], r1[32];
-        tmem_load32(lane_base + tmem_o(0) + c * 32, r0);
-        tmem_load32(lane_base + tmem_o(1) + c * 32, r1);
-        if (orow) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float x[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    x[i] = a0 * __uint_as_float(r0[q4 * 8 + i]) + a1 * __uint_as_float(r1[q4 * 8 + i]);
-                uint4 v;
-                v.x = pack2<T>(x[0], x[1]);
-                v.y = pack2<T>(x[2], x[3]);
-                v.z = pack2<T>(x[4], x[5]);
-                v.w = pack2<T>(x[6], x[7]);
-                *reinterpret_cast<uint4 *>(orow + c * 32 + q4 * 8) = v;
-            }
-        }
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars[kMergeDone]);
-    return true;
 }
 
 template <typename T>
@@ -418,7 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((b >= kKEmpty0 && b < kKEmpty0 + kKStages) || (b >= kVEmpty0 && b < kVEmpty0 + kVStages) ||
                 b == kQEmpty || b == kDrain)
                 count = 2;
-            if (b == kMerge || b == kMergeDone) count = 4;
             mbar_init(&bars[b], count);
         }
         mbar_fence_init();
@@ -496,11 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t pmax = t.two ? t.pmax[1] : t.pmax[0];
             const int32_t *bt_row = p.bt + (int64_t)t.seq * p.max_blocks;
             int nblk_next = 0;
-            int phys_next = tile_block(p, bt_row, pmax, load_tile(t, 0), bpt, lane, nblk_next);
-            for (int ld = 0; ld < t.nload; ++ld, ++iter) {
+            int phys_next = tile_block(p, bt_row, pmax, 0, bpt, lane, nblk_next);
+            for (int ld = 0; ld < t.ntiles; ++ld, ++iter) {
                 const int phys = phys_next, nblk = nblk_next;
-                if (ld + 1 < t.nload)
-                    phys_next = tile_block(p, bt_row, pmax, load_tile(t, ld + 1), bpt, lane, nblk_next);
+                if (ld + 1 < t.ntiles)
+                    phys_next = tile_block(p, bt_row, pmax, ld + 1, bpt, lane, nblk_next);
                 const int s = iter % nst;
                 const uint32_t use = iter / nst;
                 if (use > 0 && !warp_wait(&bars[empty0 + s], (use - 1) & 1)) { ok = false; break; }
@@ -620,26 +534,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars[kItemEmpty0 + slot]);
                 if (it < 0) break;
                 const Item t = decode_item(p, it);
-                const bool split = t.split;
-                const int cnt = (u == 0 || t.two || split) ? t.nt[u] : 0;   // KV tiles this slot walks
-                const int c0 = t.nt[0], nload = t.nload, kt0 = t.kt0[u];
-                // load index (within the item) of this slot's i-th KV tile
-                auto ld = [&](int i) -> int { return split ? (i < c0 ? 2 * i + u : c0 + i) : i; };
-                const int qs = split ? 0 : u;                  // Q tile of this slot's S
+                const int cnt = (u == 0 || t.two) ? t.nt[u] : 0;   // KV tiles this slot walks
+                const int nload = t.ntiles;
                 // last key any row of this slot sees, and past which V rows of a load are stale
-                const int64_t last_key = split ? (u == 0 ? (int64_t)c0 * kKeys - 1 : t.pmax[0]) : t.pmax[u];
-                const int64_t item_last = split ? last_key : (t.two ? t.pmax[1] : t.pmax[0]);
+                const int64_t last_key = t.pmax[u];
+                const int64_t item_last = t.two ? t.pmax[1] : t.pmax[0];
                 // Releases of the loads this slot does not read: wait for the K (or V) tile to land,
                 // then arrive on its empty barrier.  K and V have their own cursors: the K tile of a
                 // load is released by the step in which some slot's S reads it, the V tile by the
                 // step in which some slot's PV reads it (a V tile released with its K tile would wait
                 // for a PV of the other slot that comes after this thread's turn).
                 int relk = 0, relv = 0;
-                auto mine = [&](int L) -> bool {
-                    // a split's slots alternate over the first 2 c0 loads, slot 1 has the rest;
-                    // otherwise a slot reads loads 0 .. cnt - 1
-                    return cnt > 0 && (split ? (L < 2 * c0 ? (L & 1) == u : u == 1) : L < cnt);
-                };
+                auto mine = [&](int L) -> bool { return L < cnt; };   // a slot reads loads 0 .. cnt - 1
                 auto release_others = [&](int kupto, int vupto) -> bool {
                     for (; relk < kupto; ++relk) {
                         if (mine(relk)) continue;
@@ -658,28 +564,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The item's groups in turns: the initial S, then per step PV(i) + S(i + 1); both
                 // threads take 1 + nsteps turns (nsteps = the longer slot's tile count), passing a
                 // turn when their slot has nothing in it.
-                const int nsteps = max(t.nt[0], (t.two || split) ? t.nt[1] : 0);
+                const int nsteps = t.ntiles;
                 // Loads of the other slot are released step by step, up to the loads any slot reads
                 // in the step: a thread that held them back would keep the producers from refilling
                 // the stages the other thread waits for.  Exclusive bounds; step -1 is the first S.
-                auto kbound = [&](int i) -> int {       // K of every slot's next tile (S(i + 1))
-                    const int b = split ? (i + 1 < c0 ? 2 * i + 4 : c0 + i + 2) : i + 2;
-                    return b < nload ? b : nload;
-                };
-                auto vbound = [&](int i) -> int {       // V of every slot's tile (PV(i))
-                    const int b = i < 0 ? 0 : (split ? (i < c0 ? 2 * i + 2 : c0 + i + 1) : i + 1);
-                    return b < nload ? b : nload;
-                };
+                auto kbound = [&](int i) -> int { return min(i + 2, nload); };   // K of S(i + 1)
+                auto vbound = [&](int i) -> int { return min(i + 1, nload); };   // V of PV(i)
                 if (!wait_bar(kQFull, items & 1)) { ok = false; break; }
                 if (!release_others(kbound(-1), vbound(-1))) { ok = false; break; }
-                if (cnt > 0 && !wait_k(iter + (uint32_t)ld(0))) { ok = false; break; }
+                if (cnt > 0 && !wait_k(iter)) { ok = false; break; }
                 if (!take_turn()) { ok = false; break; }
-                if (cnt > 0) issue_s(iter + (uint32_t)ld(0), qs);
+                if (cnt > 0) issue_s(iter, u);
                 end_turn();
                 for (int i = 0; i < nsteps && ok; ++i) {
                     const bool has = i < cnt, more = i + 1 < cnt;
-                    const uint32_t g = iter + (uint32_t)(has ? ld(i) : 0);
-                    const uint32_t gn = more ? iter + (uint32_t)ld(i + 1) : 0u;
+                    const uint32_t g = iter + (uint32_t)(has ? i : 0);
+                    const uint32_t gn = more ? iter + (uint32_t)(i + 1) : 0u;
                     // everything PV_u(i) and S_u(i+1) need, checked before the turn
                     if (!release_others(kbound(i), vbound(i))) { ok = false; break; }
                     if (has) {
@@ -691,10 +591,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!take_turn()) { ok = false; break; }
                     if (has) {
                         const int vs = g % kVStages;
-                        const int64_t key0 = (int64_t)(kt0 + i) * kKeys;
+                        const int64_t key0 = (int64_t)i * kKeys;
                         const int ksteps = v_steps(vs, last_key + 1 - key0, item_last + 1 - key0);
                         issue_pv(g, i == 0, ksteps);
-                        if (more) issue_s(gn, qs);
+                        if (more) issue_s(gn, u);
                         else umma_commit(&bars[kOReady0 + u]);   // the slot's last PV of the item
                     }
                     end_turn();
@@ -718,9 +618,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const uint32_t s_tmem = lane_base + tmem_s(u), o_tmem = lane_base + tmem_o(u);
         const float c_log2 = p.scale_log2;            // > 0 (other scales use CUDA cores)
-        uint32_t *nsplit = reinterpret_cast<uint32_t *>(smem + kSmMerge + kRows * 8) + warp;  // split items so far
-        if (lane == 0) *nsplit = 0;
-        __syncwarp();
         uint32_t scount = 0;                           // S / PV tiles of this query tile so far
         uint32_t ocount = 0;                           // items of this slot so far (O-ready phases)
         uint32_t iter = 0;                             // K/V loads of the items so far
@@ -733,27 +630,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it < 0) break;
             const Item t = decode_item(p, it);
             const uint32_t item_iter = iter;
-            iter += t.nload;
-            if (u == 1 && !t.two && !t.split) continue;
-            // load index of the slot's s-th KV tile (as the MMA issuer counts them)
-            const int c0 = t.nt[0];
-            auto slot_load = [&](int s_) -> uint32_t {
-                return item_iter + (uint32_t)(t.split ? (s_ < c0 ? 2 * s_ + u : c0 + s_) : s_);
-            };
+            iter += t.ntiles;
+            if (u == 1 && !t.two) continue;
             const int64_t pmin = t.pmin[u], pmax = t.pmax[u];
-            const int kt_end = t.kt0[u] + t.nt[u];
+            const int kt_end = t.nt[u];
             const int j = t.j0[u] + row / p.group, hh = row % p.group;
             int64_t prow = pmin + row / p.group;
             if (prow > pmax) prow = pmax;               // padding rows: finite, never stored
             float m = -INFINITY, l = 0.f;
-            for (int kt = t.kt0[u]; kt < kt_end; ++kt, ++scount) {
+            for (int kt = 0; kt < kt_end; ++kt, ++scount) {
                 if (!warp_wait(&bars[kSFull0 + u], scount & 1)) { ok = false; break; }
                 tc_fence_after();
                 if (releaser) {
                     // S_u(s) is complete, and with it PV_u(s - 1): their K and V stages are free
-                    const int s_ = kt - t.kt0[u];
-                    mbar_arrive(&bars[kKEmpty0 + slot_load(s_) % kKStages]);
-                    if (s_ > 0) mbar_arrive(&bars[kVEmpty0 + slot_load(s_ - 1) % kVStages]);
+                    mbar_arrive(&bars[kKEmpty0 + (item_iter + kt) % kKStages]);
+                    if (kt > 0) mbar_arrive(&bars[kVEmpty0 + (item_iter + kt - 1) % kVStages]);
                     if (kt + 1 == kt_end) mbar_arrive(&bars[kQEmpty]);   // the slot's last S
                 }
                 uint32_t raw[kKeys];
@@ -838,18 +729,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!warp_wait(&bars[kOReady0 + u], ocount & 1)) { ok = false; break; }
             ++ocount;
             tc_fence_after();
-            if (releaser) mbar_arrive(&bars[kVEmpty0 + slot_load(t.nt[u] - 1) % kVStages]);
+            if (releaser) mbar_arrive(&bars[kVEmpty0 + (item_iter + t.nt[u] - 1) % kVStages]);
             const bool store = row < t.rows_valid[u];
             T *orow = reinterpret_cast<T *>(p.out) +
                       ((t.tok0 + j) * p.q_heads + (int64_t)t.kvh * p.group + hh) * kDim;
-            if (t.split) {
-                if (!split_epilogue<T>(u, bars, reinterpret_cast<float2 *>(smem + kSmMerge), nsplit, row, lane,
-                                       lane_base, m, l, store ? orow : nullptr)) {
-                    ok = false;
-                    break;
-                }
-                continue;
-            }
             const float inv = 1.f / l;
 #pragma unroll 1
             for (int c = 0; c < kDim / 32; ++c) {

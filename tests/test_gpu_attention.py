@@ -201,16 +201,20 @@ TC_CASES = [
     ("tc_gqa8_f16", [260], [40], 16, 2, 64, "f16", None),
     ("tc_b128", [300], [129], 2, 1, 128, "bf16", None),
     ("tc_long", [3000], [300], 1, 1, 16, "bf16", None),
-    # lone query tiles (odd tile count per KV head) with 4 or more KV tiles run as two halves of
-    # their key range merged in the epilogue: 4 and 5 KV tiles (the smallest splits, even and
-    # odd), a ragged last KV tile, partly filled query tiles, every block size, f16, MHA and
-    # GQA, and a lone tile next to a pair
-    ("split_4_tiles", [400], [32], 8, 2, 32, "bf16", None),
-    ("split_5_tiles_f16", [520], [32], 8, 2, 16, "f16", None),
-    ("split_ragged_mha", [1000, 2222], [100, 77], 2, 2, 64, "bf16", None),
-    ("split_b128_gqa8", [5000], [16], 16, 2, 128, "bf16", None),
-    ("split_beside_pair", [3000, 700], [96, 48], 8, 2, 16, "bf16", None),
-    ("split_tiny_scale", [1500], [32], 4, 1, 32, "bf16", 1e-30),
+    # lone query tiles (odd tile count per KV head: slot 0 alone, slot 1 passes its turns): 4 and
+    # 5 KV tiles, a ragged last KV tile, partly filled query tiles, every block size, f16, MHA
+    # and GQA, a lone tile next to a pair, a tiny scale
+    ("lone_4_tiles", [400], [32], 8, 2, 32, "bf16", None),
+    ("lone_5_tiles_f16", [520], [32], 8, 2, 16, "f16", None),
+    ("lone_ragged_mha", [1000, 2222], [100, 77], 2, 2, 64, "bf16", None),
+    ("lone_b128_gqa8", [5000], [16], 16, 2, 128, "bf16", None),
+    ("lone_beside_pair", [3000, 700], [96, 48], 8, 2, 16, "bf16", None),
+    ("lone_tiny_scale", [1500], [32], 4, 1, 32, "bf16", 1e-30),
+    # few items over long contexts (200+ KV tiles per lone tile)
+    ("lone_long_context", [30000, 17000, 25000], [16, 16, 48], 64, 8, 32, "bf16", None),
+    # more items than CTAs (24 sequences x 8 KV heads of lone tiles, some beside pairs)
+    ("lone_many_items", [600 + 37 * i for i in range(24)], [16] * 20 + [48, 32, 16, 48], 64, 8, 16,
+     "bf16", None),
 ]
 
 

@@ -4,7 +4,7 @@ the GPU here, so the guards carry the out-of-bounds-write check).
 The output and the caller's workspace sit between 4 KiB guards filled with a seeded byte
 pattern; after the call the guards must hold exactly the same bytes, so a write one byte past
 either end of `out` or of the workspace fails.  The outputs are also compared with the float64
-oracle, so the call did its work.  Cases: the mixed batch (tensor-core prefill tiles, split lone
+oracle, so the call did its work.  Cases: the mixed batch (tensor-core prefill tiles, lone
 tiles, GQA decode on tensor-core fragments, split-KV merges), MHA decode with many splits, fp32
 at head_dim 64, E4M3 caches, and decode over 2-bit pages."""
 import numpy as np
@@ -70,7 +70,7 @@ def _forward_guarded(b, d, seed, **kw):
 CASES = [
     ("canary_mixed_gqa", [500, 100, 3000, 33, 0, 700, 1500], [1, 130, 1, 17, 64, 1, 40], 32, 8, 128, 32, "bf16"),
     ("canary_decode_mha", [4096, 700, 33, 2000, 0, 513], [1] * 6, 16, 16, 128, 16, "bf16"),
-    ("canary_prefill_lone_split", [2000, 9000], [20, 12], 16, 4, 128, 16, "f16"),
+    ("canary_prefill_lone", [2000, 9000], [20, 12], 16, 4, 128, 16, "f16"),
     ("canary_d64_f32", [250, 17, 90], [1, 33, 5], 4, 2, 64, 16, "f32"),
 ]
 
