@@ -1128,6 +1128,13 @@ def measure_attn_workload(name, args, dev, dist, world, local, peaks, peak_src, 
                 "call_achieved": step_obj.flops / (attn_ms * 1e-3) / 1e12,
                 "decode_bracket_ms": cc_ms, "algorithmic_bytes": tbytes,
                 "peak_source": f"bf16_tflops (burst) of {peak_src}"}
+        if cc_ms and tc_ms and step_obj.bytes_attn > tbytes:
+            # the decode rows' KV bytes over the decode kernel's bracket, which also holds its wait
+            # for the SMs the tensor-core kernel's tail frees (the two kernels share the call)
+            dec_bytes = step_obj.bytes_attn - tbytes
+            roof["decode_part"] = {"algorithmic_bytes": dec_bytes, "bracket_ms": cc_ms,
+                                   "achieved_gbs": dec_bytes / (cc_ms * 1e-3) / 1e9,
+                                   "note": "bracket includes waiting for SMs held by the tensor-core kernel"}
     res["roofline"] = roof
     del step_obj
     torch.cuda.synchronize()

@@ -94,7 +94,11 @@ typedef enum { PA_KV_SAME = 0, PA_KV_E4M3 = 1 } pa_kv_dtype;
  * kv_block_stride counts codes (bytes); every sequence runs on the CUDA-core kernels (the
  * tensor-core kernel needs both MMA operands of one type).
  * Sequences with q_len * g >= 16 query rows per KV head run on the tcgen05 tensor-core kernel when
- * the dtype is bf16/f16, d = 128, g divides 128 and scale > 0; decode steps, short turns and
+ * the dtype is bf16/f16, d = 128, g divides 128 and scale > 0 (one work item per KV head and pair
+ * of 128-row query tiles; when a call has fewer such items than SMs, each item's key range is
+ * cut into chunks run by separate CTAs and merged by the logsumexp rule of the split-KV merge, at
+ * most 120 chunk items; the workspace of dims with total_q > num_seqs holds their 15.5 MiB of
+ * partial rows); decode steps, short turns and
  * everything else run on the split-KV decode kernels: 2-4 query rows per KV head of bf16/f16
  * caches with d = 128 as mma.m16n8k16 tensor-core fragments (P rounded to the 16-bit type before
  * P V), one row per KV head, E4M3 caches, fp32 and d = 64 on CUDA cores.

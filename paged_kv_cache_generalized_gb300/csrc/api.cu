@@ -179,6 +179,15 @@ WsLayout ws_layout(const pa_dims &d) {
     L.parts_ml = take((size_t)L.max_parts * R * sizeof(float) * 2);
     L.parts_o = take((size_t)L.max_parts * R * d.head_dim * sizeof(float));
     L.unit_cnt = take((size_t)L.max_parts * sizeof(uint32_t));
+    // chunk partials of the tensor-core kernel, for dims it may take: some sequence may have
+    // several query tokens, and the shape is one it supports (decided from the dims alone, so
+    // that the size does not depend on the device)
+    const int g = d.num_kv_heads > 0 ? d.num_q_heads / d.num_kv_heads : 0;
+    L.tc_chunks = d.total_q > d.num_seqs && (d.dtype == PA_BF16 || d.dtype == PA_F16) &&
+                  d.kv_dtype == PA_KV_SAME && d.head_dim == 128 &&
+                  g >= 1 && g <= kTcTileRows && kTcTileRows % g == 0 && d.block_size >= 16 && d.block_size <= 128;
+    L.tc_arrive = take(L.tc_chunks ? (size_t)kMaxTcChunkItems * 8 * sizeof(uint32_t) : 0);
+    L.tc_part = take(L.tc_chunks ? (size_t)kMaxTcChunkItems * 2 * kTcTileRows * kTcPartFloats * sizeof(float) : 0);
     L.total = off;
     return L;
 }

@@ -45,10 +45,11 @@ struct PlanParams {
     uint32_t *counters;
     int32_t *cu_q, *simt_cu, *parts_cu, *comb_cu, *groups, *nchunk, *tc_cu, *tc_seq;
     uint32_t *unit_cnt;
+    uint32_t *tc_arrive;               // chunk arrival counters (when the workspace holds them)
     unsigned *status;
     int64_t total_q;
     int64_t max_parts;
-    int num_seqs, kv_heads, group, block_size, max_blocks, rows, tc, total_warps;
+    int num_seqs, kv_heads, group, block_size, max_blocks, rows, tc, total_warps, tc_chunk_ok;
 };
 
 constexpr int kPlanThreads = 1024;
@@ -225,19 +226,88 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p, Append
             p.tc_seq[rank] = i;
         }
         __syncthreads();
+        // pair items (one per KV head and pair of query tiles) of each ranked sequence
         for (int r = tid; r < S; r += kPlanThreads) {
             const int i = p.tc_seq[r];
-            int32_t tiles = 0;
+            int32_t pairs = 0;
             if (i >= 0) {
                 const int64_t rows = (int64_t)p.qlen[i] * p.group;
                 const int64_t tph = (rows + kTcTileRows - 1) / kTcTileRows;
-                tiles = p.kv_heads * (int32_t)((tph + kTcTilesPerItem - 1) / kTcTilesPerItem);
+                pairs = p.kv_heads * (int32_t)((tph + kTcTilesPerItem - 1) / kTcTilesPerItem);
             }
-            p.tc_cu[r] = tiles;
+            p.tc_cu[r] = pairs;
         }
         __syncthreads();
-        const int64_t n_tiles = block_exclusive_scan(p.tc_cu, S);
-        if (tid == 0) p.counters[kTcTotal] = (uint32_t)n_tiles;
+        int64_t n_items = block_exclusive_scan(p.tc_cu, S);
+        // Fewer pair items than CTAs: split each pair's key range into chunks of about lc KV
+        // tiles, so that the chunks fill the grid (at most one per CTA and kMaxTcChunkItems in
+        // all).  The KV tile count of every distinct pair (the same for each KV head) goes to
+        // shared memory, then warp 0 searches the chunk length.
+        __shared__ int s_lc;
+        __shared__ int s_nt[kMaxTcChunkItems];
+        const int ctas = p.total_warps / 8;   // the tensor-core grid: one CTA per SM
+        const int cap = ctas < kMaxTcChunkItems ? ctas : kMaxTcChunkItems;
+        const bool few = p.tc_chunk_ok && n_items > 0 && n_items < cap;   // block-uniform
+        if (tid == 0) s_lc = 0;
+        if (few) {
+            for (int r = tid; r < S; r += kPlanThreads) {
+                const int i = p.tc_seq[r];
+                if (i < 0) continue;
+                const int rows = p.qlen[i] * p.group;
+                const int pph = ((rows + kTcTileRows - 1) / kTcTileRows + 1) / 2;
+                const int at = p.tc_cu[r] / p.kv_heads;             // the sequence's first pair
+                for (int pi = 0; pi < pph; ++pi) s_nt[at + pi] = tc_pair_tiles(p.ctx[i], rows, p.group, pi);
+            }
+        }
+        __syncthreads();
+        if (few && tid < 32) {
+            const int npairs = (int)(n_items / p.kv_heads);
+            auto items_for = [&](int len) -> int64_t {   // items with chunk length len (0: KV tiles)
+                int64_t n = 0;
+                for (int k = tid; k < npairs; k += 32) n += len > 0 ? tc_pair_chunks(s_nt[k], len) : s_nt[k];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+                return n * p.kv_heads;
+            };
+            const int64_t tiles = items_for(0);
+            int64_t lo = (tiles + cap - 1) / cap;
+            if (lo < kTcMinChunkTiles) lo = kTcMinChunkTiles;
+            // the shortest chunk length whose items fit (items never grow with the length; long
+            // enough, every pair is one chunk and fits)
+            int64_t hi = lo;
+            while (items_for((int)hi) > cap) hi *= 2;
+            if (hi > lo) {
+                lo = hi / 2;                              // items_for(lo) > cap >= items_for(hi)
+                while (hi - lo > 1) {
+                    const int64_t mid = (lo + hi) / 2;
+                    if (items_for((int)mid) > cap) lo = mid;
+                    else hi = mid;
+                }
+            }
+            const int64_t chunked = items_for((int)hi);   // every lane takes part in the sums
+            if (tid == 0 && chunked > n_items) s_lc = (int)hi;
+        }
+        __syncthreads();
+        if (tid == 0) p.counters[kTcChunk] = (uint32_t)s_lc;
+        const int lc = s_lc;
+        if (lc > 0) {
+            for (int r = tid; r < S; r += kPlanThreads) {
+                const int i = p.tc_seq[r];
+                int32_t items = 0;
+                if (i >= 0) {
+                    const int rows = p.qlen[i] * p.group;
+                    const int pph = ((rows + kTcTileRows - 1) / kTcTileRows + 1) / 2;
+                    for (int pi = 0; pi < pph; ++pi)
+                        items += tc_pair_chunks(tc_pair_tiles(p.ctx[i], rows, p.group, pi), lc);
+                    items *= p.kv_heads;
+                }
+                p.tc_cu[r] = items;
+            }
+            for (int k = tid; k < kMaxTcChunkItems * 8; k += kPlanThreads) p.tc_arrive[k] = 0u;
+            __syncthreads();
+            n_items = block_exclusive_scan(p.tc_cu, S);
+        }
+        if (tid == 0) p.counters[kTcTotal] = (uint32_t)n_items;
     }
 }
 
@@ -1484,6 +1554,8 @@ cudaError_t launch_plan(const FwdArgs &a, cudaStream_t s) {
     p.max_blocks = a.dims.max_blocks_per_seq;
     p.rows = L.rows_per_item;
     p.tc = a.tc ? 1 : 0;
+    p.tc_chunk_ok = a.lay.tc_chunks ? 1 : 0;
+    p.tc_arrive = a.lay.tc_chunks ? reinterpret_cast<uint32_t *>(a.ws + L.tc_arrive) : nullptr;
     p.total_warps = a.num_sms * 8;
     AppendParams ap{};
     int64_t grid = 1;

@@ -249,6 +249,8 @@ struct TcParams {
     const int32_t *bt, *ctx, *qlen;
     const int32_t *cu_q, *tc_cu, *tc_seq;
     const uint32_t *counters;
+    float *part;                  // chunk partial rows: [item][tile][row][kTcPartFloats]
+    uint32_t *arrive;             // chunks finished: [first item of the pair][tile][warp]
     unsigned *status;
     int64_t num_blocks;
     float scale_log2;
@@ -256,17 +258,39 @@ struct TcParams {
 };
 
 // One work item: query tiles qt0 = 2*pi and qt1 = 2*pi + 1 (if it exists) of one (sequence,
-// KV head).  Tile 1 holds later rows, so its causal range (and KV tile count) covers tile 0's.
-// The item loads KV tiles 0 .. ntiles - 1 once, in order; both slots read them from tile 0.
+// KV head), over one chunk of the pair's key range.  Tile 1 holds later rows, so its causal range
+// (and KV tile count) covers tile 0's.  The item loads KV tiles k0 .. k0 + ntiles - 1 once, in
+// order; slot u reads them from k0 up to its own last tile nt[u] - 1.  Without chunking (the
+// launch has at least one pair per CTA) every pair is one chunk, k0 = 0.
 struct Item {
     int seq, kvh, ntiles;         // ntiles: KV tiles loaded = MMA steps (the longer slot's count)
+    int k0, nchunk, chunk, first; // first KV tile; chunks of the pair, this one; item of chunk 0
     int64_t tok0;
     bool two;                     // tile 1 exists
     int j0[2], rows_valid[2], nt[2];
     int64_t pmin[2], pmax[2];
 };
 
-__device__ __forceinline__ Item decode_item(const TcParams &p, int it) {
+// (KV head, pair, chunk, chunks of the pair) of item `local` of a sequence whose pairs run as
+// chunks of about lc KV tiles.  Out of line: only launches with few pairs take it.
+__device__ __noinline__ int4 chunk_walk(int64_t c, int rows, int g, int pph, int lc, int local) {
+    int per = 0;                                  // items per KV head
+    for (int q = 0; q < pph; ++q) per += tc_pair_chunks(tc_pair_tiles(c, rows, g, q), lc);
+    const int kvh = local / per;
+    int rem = local - kvh * per, pi = pph - 1, nchunk = 1;
+    for (; pi > 0; --pi) {
+        nchunk = tc_pair_chunks(tc_pair_tiles(c, rows, g, pi), lc);
+        if (rem < nchunk) break;
+        rem -= nchunk;
+    }
+    if (pi == 0) nchunk = tc_pair_chunks(tc_pair_tiles(c, rows, g, 0), lc);
+    return make_int4(kvh, pi, rem, nchunk);
+}
+
+// Item `it` of the launch; lc = KV tiles per chunk (0: pairs are not chunked).  Items are numbered
+// by sequence rank, then KV head, then pair (a sequence's last, longest pair first), then chunk,
+// so the chunks of one pair are consecutive items.
+__device__ __forceinline__ Item decode_item(const TcParams &p, int it, int lc) {
     Item t;
     const int rank = find_rank(p.tc_cu, p.num_seqs, it);
     t.seq = __ldg(p.tc_seq + rank);
@@ -274,10 +298,19 @@ __device__ __forceinline__ Item decode_item(const TcParams &p, int it) {
     const int rows = __ldg(p.qlen + t.seq) * p.group;
     const int tph = (rows + kRows - 1) / kRows;   // query tiles per KV head
     const int pph = (tph + 1) / 2;                // tile pairs per KV head
-    const int pi = pph - 1 - (local % pph);       // a sequence's last (longest) pair first
-    t.kvh = local / pph;
-    t.tok0 = __ldg(p.cu_q + t.seq);
     const int64_t c = __ldg(p.ctx + t.seq);
+    int pi, chunk = 0, nchunk = 1;
+    if (lc <= 0) {
+        pi = pph - 1 - (local % pph);
+        t.kvh = local / pph;
+    } else {
+        const int4 w = chunk_walk(c, rows, p.group, pph, lc, local);
+        t.kvh = w.x;
+        pi = w.y;
+        chunk = w.z;
+        nchunk = w.w;
+    }
+    t.tok0 = __ldg(p.cu_q + t.seq);
     t.two = 2 * pi + 1 < tph;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -288,7 +321,13 @@ __device__ __forceinline__ Item decode_item(const TcParams &p, int it) {
         t.pmax[u] = c + t.j0[u] + (t.rows_valid[u] - 1) / p.group;
         t.nt[u] = (int)((t.pmax[u] + kKeys) / kKeys);
     }
-    t.ntiles = t.two ? t.nt[1] : t.nt[0];
+    // chunk `chunk` of nchunk: KV tiles [k0, k1) of the pair's whole range (at least 2 each)
+    const int ntot = t.two ? t.nt[1] : t.nt[0];
+    t.k0 = (int)((int64_t)chunk * ntot / nchunk);
+    t.ntiles = (int)((int64_t)(chunk + 1) * ntot / nchunk) - t.k0;
+    t.nchunk = nchunk;
+    t.chunk = chunk;
+    t.first = it - chunk;
     return t;
 }
 
@@ -307,6 +346,80 @@ __device__ __forceinline__ int tile_block(const TcParams &p, const int32_t *bt_r
         }
     }
     return phys;
+}
+
+// Epilogue of a chunk item (a pair whose key range runs as several items).  The warp's 32 rows
+// write (m, l, O) -- running max in log2 units, sum, unnormalised O from tensor memory, O 16-byte
+// aligned in a 528-byte row -- to the item's partial slot; after a device-scope fence, the warp arrives on its (pair, tile, warp)
+// counter, and the warp that arrives last merges the pair's chunks row by row by the logsumexp
+// rule, out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c, M = max_c m_c (every row sees key 0
+// in the first chunk, so M is a real score; a chunk in which a row saw no key has l = 0, O = 0 and
+// m = -3e38, weight 0), and writes the row (orow, if stored).
+template <typename T>
+__device__ __noinline__ void chunk_epilogue(const TcParams &p, int it, const Item &t, int u, int quad, int row,
+                                            int lane, uint32_t o_tmem, float m, float l, T *orow) {
+    float *mine = p.part + ((size_t)(it * 2 + u) * kRows + row) * kTcPartFloats;
+    mine[0] = m;
+    mine[1] = l;
+#pragma unroll 1
+    for (int c = 0; c < kDim / 32; ++c) {
+        uint32_t r[32];
+        tmem_load32(o_tmem + c * 32, r);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+            reinterpret_cast<float4 *>(mine + kTcPartO + c * 32)[q4] =
+                make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
+                            __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
+    }
+    __threadfence();
+    __syncwarp();
+    uint32_t before = 0;
+    if (lane == 0) before = atomicAdd(p.arrive + ((size_t)t.first * 2 + u) * 4 + quad, 1u);
+    before = __shfl_sync(0xffffffffu, before, 0);
+    if (before != (uint32_t)(t.nchunk - 1)) return;
+    __threadfence();
+    auto slot = [&](int c) -> const float * {
+        return p.part + ((size_t)((t.first + c) * 2 + u) * kRows + row) * kTcPartFloats;
+    };
+    float M = -INFINITY;
+    for (int c = 0; c < t.nchunk; ++c) M = fmaxf(M, __ldcg(slot(c)));
+    float L = 0.f;
+    for (int c = 0; c < t.nchunk; ++c) {
+        const float mc = __ldcg(slot(c));
+        L += mc == -INFINITY ? 0.f : fast_exp2(mc - M) * __ldcg(slot(c) + 1);
+    }
+    const float inv = 1.f / L;
+#pragma unroll 1
+    for (int b = 0; b < kDim / 32; ++b) {
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+        for (int c = 0; c < t.nchunk; ++c) {
+            const float *sc = slot(c);
+            const float mc = __ldcg(sc);
+            if (mc == -INFINITY) continue;
+            const float w = fast_exp2(mc - M) * inv;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(sc + kTcPartO + b * 32) + q4);
+                acc[4 * q4] = fmaf(w, v.x, acc[4 * q4]);
+                acc[4 * q4 + 1] = fmaf(w, v.y, acc[4 * q4 + 1]);
+                acc[4 * q4 + 2] = fmaf(w, v.z, acc[4 * q4 + 2]);
+                acc[4 * q4 + 3] = fmaf(w, v.w, acc[4 * q4 + 3]);
+            }
+        }
+        if (orow) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint4 v;
+                v.x = pack2<T>(acc[q4 * 8 + 0], acc[q4 * 8 + 1]);
+                v.y = pack2<T>(acc[q4 * 8 + 2], acc[q4 * 8 + 3]);
+                v.z = pack2<T>(acc[q4 * 8 + 4], acc[q4 * 8 + 5]);
+                v.w = pack2<T>(acc[q4 * 8 + 6], acc[q4 * 8 + 7]);
+                *reinterpret_cast<uint4 *>(orow + b * 32 + q4 * 8) = v;
+            }
+        }
+    }
 }
 
 template <typename T>
@@ -349,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int total = (int)p.counters[kTcTotal];
+    const int lc = (int)p.counters[kTcChunk];
     uint32_t *next_item = const_cast<uint32_t *>(p.counters) + kTcNext;
     const int B = p.block_size;
     const int bpt = kKeys / B;   // blocks per KV tile
@@ -389,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it == -2) { ok = false; break; }
             }
             if (it < 0) break;
-            const Item t = decode_item(p, it);
+            const Item t = decode_item(p, it, lc);
             if (is_k) {
                 // both query tiles of the pair (the previous pair's S MMAs are done with Q)
                 if (items > 0 && !warp_wait(&bars[kQEmpty], (items - 1) & 1)) { ok = false; break; }
@@ -410,11 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t pmax = t.two ? t.pmax[1] : t.pmax[0];
             const int32_t *bt_row = p.bt + (int64_t)t.seq * p.max_blocks;
             int nblk_next = 0;
-            int phys_next = tile_block(p, bt_row, pmax, 0, bpt, lane, nblk_next);
+            int phys_next = tile_block(p, bt_row, pmax, t.k0, bpt, lane, nblk_next);
             for (int ld = 0; ld < t.ntiles; ++ld, ++iter) {
                 const int phys = phys_next, nblk = nblk_next;
                 if (ld + 1 < t.ntiles)
-                    phys_next = tile_block(p, bt_row, pmax, ld + 1, bpt, lane, nblk_next);
+                    phys_next = tile_block(p, bt_row, pmax, t.k0 + ld + 1, bpt, lane, nblk_next);
                 const int s = iter % nst;
                 const uint32_t use = iter / nst;
                 if (use > 0 && !warp_wait(&bars[empty0 + s], (use - 1) & 1)) { ok = false; break; }
@@ -533,8 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int it = item_ring[slot];
                 mbar_arrive(&bars[kItemEmpty0 + slot]);
                 if (it < 0) break;
-                const Item t = decode_item(p, it);
-                const int cnt = (u == 0 || t.two) ? t.nt[u] : 0;   // KV tiles this slot walks
+                const Item t = decode_item(p, it, lc);
+                // KV tiles this slot walks in the item: from k0 to its own last tile
+                const int cnt = (u == 0 || t.two) ? max(0, min(t.k0 + t.ntiles, t.nt[u]) - t.k0) : 0;
                 const int nload = t.ntiles;
                 // last key any row of this slot sees, and past which V rows of a load are stale
                 const int64_t last_key = t.pmax[u];
@@ -591,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!take_turn()) { ok = false; break; }
                     if (has) {
                         const int vs = g % kVStages;
-                        const int64_t key0 = (int64_t)i * kKeys;
+                        const int64_t key0 = (int64_t)(t.k0 + i) * kKeys;
                         const int ksteps = v_steps(vs, last_key + 1 - key0, item_last + 1 - key0);
                         issue_pv(g, i == 0, ksteps);
                         if (more) issue_s(gn, u);
@@ -628,23 +743,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int it = receive_item(n);
             if (it == -2) { ok = false; break; }
             if (it < 0) break;
-            const Item t = decode_item(p, it);
+            const Item t = decode_item(p, it, lc);
             const uint32_t item_iter = iter;
             iter += t.ntiles;
             if (u == 1 && !t.two) continue;
             const int64_t pmin = t.pmin[u], pmax = t.pmax[u];
-            const int kt_end = t.nt[u];
+            const int kt_end = min(t.k0 + t.ntiles, t.nt[u]);   // this slot's tiles: k0 .. kt_end - 1
             const int j = t.j0[u] + row / p.group, hh = row % p.group;
             int64_t prow = pmin + row / p.group;
             if (prow > pmax) prow = pmax;               // padding rows: finite, never stored
-            float m = -INFINITY, l = 0.f;
-            for (int kt = 0; kt < kt_end; ++kt, ++scount) {
+            // a finite start: in a chunk, a row may see no key in its first tiles (all scores
+            // -inf), and -inf - m must stay -inf (P = 0), not NaN
+            float m = -3.0e38f, l = 0.f;
+            for (int kt = t.k0; kt < kt_end; ++kt, ++scount) {
                 if (!warp_wait(&bars[kSFull0 + u], scount & 1)) { ok = false; break; }
                 tc_fence_after();
                 if (releaser) {
                     // S_u(s) is complete, and with it PV_u(s - 1): their K and V stages are free
-                    mbar_arrive(&bars[kKEmpty0 + (item_iter + kt) % kKStages]);
-                    if (kt > 0) mbar_arrive(&bars[kVEmpty0 + (item_iter + kt - 1) % kVStages]);
+                    const uint32_t ld = item_iter + (uint32_t)(kt - t.k0);   // the item's load of tile kt
+                    mbar_arrive(&bars[kKEmpty0 + ld % kKStages]);
+                    if (kt > t.k0) mbar_arrive(&bars[kVEmpty0 + (ld - 1) % kVStages]);
                     if (kt + 1 == kt_end) mbar_arrive(&bars[kQEmpty]);   // the slot's last S
                 }
                 uint32_t raw[kKeys];
@@ -701,9 +819,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lsum += a0 + a1;
                 }
                 // tensor-memory loads/stores are warp-collective: the whole warp rescales when any
-                // of its rows must (alpha = 1 for the others), after the previous PV is complete
-                // (l > 0 after the slot's first tile: every row sees a key there)
-                if (l > 0.f && __any_sync(0xffffffffu, rescale)) {
+                // of its rows with a key seen so far (l > 0) must, after the previous PV is complete
+                // (alpha = 1 for rows that need not; a row with l = 0 has O = 0, and its alpha is
+                // 2^-inf = 0)
+                if (__any_sync(0xffffffffu, rescale && l > 0.f)) {
                     // PV_u(s - 1) is complete: it came before S_u(s) from the same issuer
                     const float alpha = rescale ? fast_exp2(m - muse) : 1.f;
                     l *= alpha;
@@ -729,10 +848,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!warp_wait(&bars[kOReady0 + u], ocount & 1)) { ok = false; break; }
             ++ocount;
             tc_fence_after();
-            if (releaser) mbar_arrive(&bars[kVEmpty0 + (item_iter + t.nt[u] - 1) % kVStages]);
+            if (releaser) mbar_arrive(&bars[kVEmpty0 + (item_iter + (uint32_t)(kt_end - 1 - t.k0)) % kVStages]);
             const bool store = row < t.rows_valid[u];
             T *orow = reinterpret_cast<T *>(p.out) +
                       ((t.tok0 + j) * p.q_heads + (int64_t)t.kvh * p.group + hh) * kDim;
+            if (t.nchunk > 1) {
+                // one chunk of the pair's key range: this row's (m, l, O) to the item's partial
+                // slot; the last of the pair's chunks to finish (per warp of rows) merges them
+                chunk_epilogue<T>(p, it, t, u, quad, row, lane, o_tmem, m, l, store ? orow : nullptr);
+                tc_fence_before();
+                continue;
+            }
             const float inv = 1.f / l;
 #pragma unroll 1
             for (int c = 0; c < kDim / 32; ++c) {
@@ -800,6 +926,8 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s) {
     p.tc_cu = reinterpret_cast<const int32_t *>(a.ws + L.tc_cu);
     p.tc_seq = reinterpret_cast<const int32_t *>(a.ws + L.tc_seq);
     p.counters = reinterpret_cast<const uint32_t *>(a.ws + L.counters);
+    p.part = L.tc_chunks ? reinterpret_cast<float *>(a.ws + L.tc_part) : nullptr;
+    p.arrive = L.tc_chunks ? reinterpret_cast<uint32_t *>(a.ws + L.tc_arrive) : nullptr;
     p.status = a.status;
     p.num_blocks = d.num_blocks;
     p.scale_log2 = a.scale * 1.4426950408889634f;

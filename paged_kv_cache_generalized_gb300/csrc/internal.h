@@ -21,6 +21,37 @@ constexpr int kTcTileRows = 128;
 // Query tiles of one (sequence, KV head) processed together by one tensor-core work item (they
 // share every K/V tile load).
 constexpr int kTcTilesPerItem = 2;
+// Launches with fewer tensor-core pair items than CTAs split each pair's key range into chunks
+// run by separate CTAs and merged by the logsumexp rule; at most this many items then (each
+// chunk item has a partial-result slot of 2 x 128 rows in the workspace), each chunk at least
+// kTcMinChunkTiles KV tiles and at least 2 tiles.
+constexpr int kMaxTcChunkItems = 120;
+constexpr int kTcMinChunkTiles = 4;
+// At most this many chunks per pair: the warps that merge a pair read every chunk's partial rows
+// (528 bytes each), so the merge grows with the chunk count while the chunks' work shrinks.
+constexpr int kTcMaxChunksPerPair = 16;
+constexpr int kTcPartFloats = 4 + 128;   // per row: running max (log2 units), sum, 2 pad, o[128]
+constexpr int kTcPartO = 4;               // o starts 16 bytes into the row (rows are 528 bytes)
+
+// KV tiles (128 keys) of tensor-core pair pi of a sequence with c cached tokens and `rows` query
+// rows per KV head (q_len * g): through the causal position of the pair's last row.
+__host__ __device__ inline int tc_pair_tiles(int64_t c, int rows, int g, int pi) {
+    const int tph = (rows + kTcTileRows - 1) / kTcTileRows;
+    const int qt = 2 * pi + 1 < tph ? 2 * pi + 1 : 2 * pi;
+    const int valid = rows - qt * kTcTileRows < kTcTileRows ? rows - qt * kTcTileRows : kTcTileRows;
+    const int64_t pmax = c + (int64_t)qt * (kTcTileRows / g) + (valid - 1) / g;
+    return (int)((pmax + 128) / 128);
+}
+// Chunks of a pair of nt KV tiles for chunk length lc (0: no chunking): at most nt / 2, so that
+// every chunk holds at least 2 tiles, and at most kTcMaxChunksPerPair.
+__host__ __device__ inline int tc_pair_chunks(int nt, int lc) {
+    if (lc <= 0) return 1;
+    int c = (nt + lc - 1) / lc;
+    const int cap = nt / 2 < kTcMaxChunksPerPair ? nt / 2 : kTcMaxChunksPerPair;
+    if (c > cap) c = cap;
+    return c > 1 ? c : 1;
+}
+
 // Upper bound on the KV splits of one CUDA-core work item's rows.
 constexpr int kMaxSplits = 64;
 // The planner sizes splits for about 16 work items per warp of the persistent grid, capped here
@@ -39,6 +70,7 @@ enum Counter : int {
     kTcTotal = 3,     // number of tensor-core tiles
     kCombTotal = 4,   // number of split-KV rows to combine (row groups x rows)
     kChunkBlocks = 5, // KV blocks per CUDA-core split
+    kTcChunk = 6,     // KV tiles per tensor-core chunk (0: pair items are not chunked)
     kNumCounters = 16
 };
 
@@ -56,6 +88,9 @@ struct WsLayout {
     size_t parts_ml;   // float2 [max_parts * R]  (running max in log2 units, sum)
     size_t parts_o;    // float  [max_parts * R * d]
     size_t unit_cnt;   // uint32 [max_parts]  splits finished per split row group (zeroed by the planner)
+    size_t tc_arrive;  // uint32 [kMaxTcChunkItems * 8]  chunks finished per (pair, tile, warp)
+    size_t tc_part;    // float [kMaxTcChunkItems * 2 * 128 * kTcPartFloats]  chunk partial rows
+    bool tc_chunks;    // the two regions above exist (dims the tensor-core kernel may take)
     size_t total;
     int64_t max_parts;
     int rows_per_item; // R

@@ -217,6 +217,33 @@ TC_CASES = [
      "bf16", None),
 ]
 
+# Launches with fewer pair items than CTAs: each pair's key range runs as chunks on separate CTAs,
+# merged by the logsumexp rule (rows that see no key in some chunk, pairs whose tiles end in
+# different chunks, lone tiles, GQA 8, f16, block sizes 16-128)
+TC_CHUNK_CASES = [
+    ("chunk_one_turn_gqa8", [60000], [16], 16, 2, 32, "bf16", None),
+    ("chunk_two_turns_100k", [100000, 99000], [32, 32], 16, 4, 32, "bf16", None),
+    ("chunk_pairs_f16_b16", [16000], [256], 32, 8, 16, "f16", None),
+    ("chunk_ragged_mix", [30000, 17000, 25000, 900], [16, 16, 48, 130], 64, 8, 64, "bf16", None),
+    ("chunk_mha_b128", [20000], [200], 4, 4, 128, "bf16", None),
+    ("chunk_short_context", [1000], [40], 8, 2, 16, "bf16", None),
+]
+
+
+@pytest.mark.parametrize("case", TC_CHUNK_CASES, ids=[c[0] for c in TC_CHUNK_CASES])
+def test_tensor_core_key_range_chunks(case):
+    name, ctx, ql, hq, hkv, B, dtype, scale = case
+    b = W.make_attn_batch(name, ctx, ql, hq, hkv, 128, B, dtype, seed=zlib.crc32(name.encode()) % 1000,
+                          scale=scale)
+    out, counters = _forward_with_workspace(b)
+    assert counters[3] > 0, "no tile went to the tensor-core kernel"
+    assert counters[6] > 0, "the pairs were not chunked"
+    assert pkg.device_status() == 0
+    ref = oracle.paged_attention_batch(b, threads=8)
+    assert_close(as_f64(out), ref, b.dtype, name)
+    out2, _ = _forward_with_workspace(b)
+    assert torch.equal(out, out2)                      # the merge order does not depend on timing
+
 
 @pytest.mark.parametrize("case", TC_CASES, ids=[c[0] for c in TC_CASES])
 def test_tensor_core_path(case):
