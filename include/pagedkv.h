@@ -325,7 +325,11 @@ pa_status block_copy(const block_copy_dims *dims, const void *src, void *dst,
  *   [2048, 2080)      promoted channel ids, uint8, ascending in slots 0..P-1, later slots 0
  *   [2080, 6176)      K low 2 bits: token t, channel x at byte 2080 + 32 t + x / 4, bits 2 (x % 4)
  *   [6176, 6176+32P)  K high 2 bits of promoted slot k: byte 6176 + (P/4) t + k / 4, bits 2 (k % 4)
- *   [6176+32P, +4096) V codes: token t, channel x at byte 32 t + x / 4, bits 2 (x % 4)
+ *   [6176+32P, +4096) V codes: token t, channel x at byte 2048 (t / 64) + 16 x + (t % 64) / 4,
+ *                     bits 2 (t % 4) (channel-major within each half page of 64 tokens)
+ * The byte order is the library's own: K codes token-major (a 32-bit word holds 16 channels of
+ * one key) and V codes channel-major per half page (a word holds 16 tokens of one channel), the
+ * orders in which decode feeds them to the tensor cores.
  * A page pool is [num_pages, Hkv, record] (record-major, 16-byte aligned); residual pools are
  * [num_res_pages, Hkv, 128, 128] of `dtype`.
  * ---------------------------------------------------------------------------------------- */

@@ -36,9 +36,15 @@ Record of one (page, KV head), little-endian, byte offsets (d = 128, P promoted 
     [2048, 2080)      promoted channel ids, uint8, ascending in slots 0..P-1, later slots 0
     [2080, 6176)      K low bits: token t, channel x -> byte 32 t + x / 4, bits 2 (x % 4)
     [6176, 6176+32P)  K high bits of promoted slot k: byte (P / 4) t + k / 4, bits 2 (k % 4)
-    then 4096 bytes   V codes: token t, channel x -> byte 32 t + x / 4, bits 2 (x % 4)
+    then 4096 bytes   V codes: token t, channel x -> byte 2048 (t / 64) + 16 x + (t % 64) / 4,
+                      bits 2 (t % 4) (per half page, channel-major)
 
 A cached element's value is code x scale + minimum (a promoted key code is low + 4 x high).
+
+The byte layout is this implementation's own (the chapter fixes the dense/sparse split and the
+bit widths, not the order of the bytes).  K codes are token-major and V codes channel-major within
+each half page of 64 tokens, so that a 32-bit word of K codes holds 16 channels of one key and a
+word of V codes holds 16 tokens of one channel.
 """
 from __future__ import annotations
 
@@ -115,6 +121,19 @@ def _unpack2(b, n):
     return out.reshape(b.shape[0], n)
 
 
+def _pack_v(v_codes):
+    """[128 tokens, 128 channels] V codes -> 4096 bytes: for each half page h (tokens 64 h ..
+    64 h + 63), channel x's 64 codes in 16 bytes at 2048 h + 16 x, token t at bits 2 (t % 4) of
+    byte (t % 64) / 4."""
+    halves = [_pack2(v_codes[64 * h:64 * h + 64].T) for h in range(2)]   # [channel, 16 bytes]
+    return np.concatenate([x.reshape(-1) for x in halves])
+
+
+def _unpack_v(b):
+    b = np.asarray(b, dtype=np.uint8).reshape(2, HEAD_DIM, 16)
+    return np.concatenate([_unpack2(b[h], 64).T for h in range(2)], axis=0)
+
+
 def pack_record(f) -> np.ndarray:
     """The record's bytes (uint8 [record_bytes]) from ``quantize_page``'s fields."""
     P = f["promoted"]
@@ -128,7 +147,7 @@ def pack_record(f) -> np.ndarray:
     kc = f["k_codes"]
     rec[_OFF_KLO:khi_off] = _pack2(kc & 3).reshape(-1)
     rec[khi_off:vc_off] = _pack2(kc[:, f["pid"]] >> 2).reshape(-1)
-    rec[vc_off:vc_off + 32 * PAGE_TOKENS] = _pack2(f["v_codes"]).reshape(-1)
+    rec[vc_off:vc_off + 32 * PAGE_TOKENS] = _pack_v(f["v_codes"])
     return rec
 
 
@@ -145,7 +164,7 @@ def unpack_record(rec, promoted):
     k_codes = _unpack2(rec[_OFF_KLO:khi_off].reshape(PAGE_TOKENS, 32), HEAD_DIM)
     hi = _unpack2(rec[khi_off:vc_off].reshape(PAGE_TOKENS, P // 4), P)
     k_codes[:, pid] += 4 * hi
-    v_codes = _unpack2(rec[vc_off:vc_off + 32 * PAGE_TOKENS].reshape(PAGE_TOKENS, 32), HEAD_DIM)
+    v_codes = _unpack_v(rec[vc_off:vc_off + 32 * PAGE_TOKENS])
     return dict(k_codes=k_codes, pid=pid, ks=ks, km=km, v_codes=v_codes, vs=vs, vm=vm,
                 promoted=P)
 

@@ -77,7 +77,8 @@ def pin_hand_worked_bytes(K):
     # Promoted set (P = 16): channels 100..115, the only ones with large magnitude.  Channel 100
     # runs 100..115 (scale 1) with code 13 = 1 + 4 * 3 at token 2; the others are constant 50
     # (scale 0).  Channel 5 (2 bits) runs 0..3 with code 2 at token 1.  V token 0, channels 0..3
-    # hold codes 1, 2, 3, 0.  Every other value is 0.
+    # hold codes 1, 2, 3, 0; V token 1, channels 0..3 codes 3, 0, 0, 3; V token 70 (second half
+    # page), channel 2 code 3 and channel 3 code 1 (scale 1, minimum 0).  Every other value is 0.
     k = np.zeros((T, D), np.float32)
     v = np.zeros((T, D), np.float32)
     k[:, 100:116] = 50.0
@@ -85,6 +86,8 @@ def pin_hand_worked_bytes(K):
     k[2, 100], k[4, 100] = 113.0, 115.0
     k[1, 5], k[3, 5] = 2.0, 3.0
     v[0, :4] = [1.0, 2.0, 3.0, 0.0]
+    v[1, :4] = [3.0, 0.0, 0.0, 3.0]
+    v[70, :4] = [0.0, 0.0, 3.0, 1.0]
     f = K.quantize_page(k, v, 16)
     rec = K.pack_record(f)
     assert len(rec) == 10784
@@ -96,7 +99,14 @@ def pin_hand_worked_bytes(K):
     assert rec[2080 + 32 * 4 + 25] == 0x03 and rec[6176 + 4 * 4] == 0x03   # token 4, channel 100: 15
     assert np.count_nonzero(rec[2080:2080 + 4096]) == 4 and np.count_nonzero(rec[6176:6176 + 512]) == 2
     vc_off = 6176 + 32 * 16
-    assert rec[vc_off + 0] == 0x39               # 1 | 2 << 2 | 3 << 4 | 0 << 6
+    # V codes: half page, then channel (16 bytes each), then token (4 per byte, low bits first)
+    assert rec[vc_off + 0] == 0x0D               # channel 0: token 0 code 1, token 1 code 3 (bits 2-3)
+    assert rec[vc_off + 16] == 0x02              # channel 1: token 0 code 2
+    assert rec[vc_off + 32] == 0x03              # channel 2: token 0 code 3
+    assert rec[vc_off + 48] == 0x0C              # channel 3: token 1 code 3
+    assert rec[vc_off + 2048 + 32 + 1] == 0x30   # half 1, channel 2: token 70 = 64 + 6 -> byte 1, bits 4-5
+    assert rec[vc_off + 2048 + 48 + 1] == 0x10   # half 1, channel 3: token 70 code 1
+    assert np.count_nonzero(rec[vc_off:vc_off + 4096]) == 6
     f32 = lambda off: np.frombuffer(rec[off:off + 4].tobytes(), "<f4")[0]
     assert f32(1024) == 1.0                      # V scale of token 0
     assert f32(4 * 5) == 1.0 and f32(4 * 100) == 1.0 and f32(4 * 101) == 0.0   # K scales
@@ -282,6 +292,10 @@ PLANTED = {
                                      "c[..., 3] | (c[..., 2] << 2) | (c[..., 1] << 4) | (c[..., 0] << 6)"),
     "V per channel": ("vmin = v.min(axis=1)\n    vmax = v.max(axis=1)",
                       "vmin = v.min(axis=0)\n    vmax = v.max(axis=0)"),
+    "V codes token-major": ("halves = [_pack2(v_codes[64 * h:64 * h + 64].T) for h in range(2)]",
+                            "halves = [_pack2(v_codes[64 * h:64 * h + 64]) for h in range(2)]"),
+    "V halves swapped": ("np.concatenate([x.reshape(-1) for x in halves])",
+                         "np.concatenate([x.reshape(-1) for x in halves[::-1]])"),
     "round half up": ("r = np.rint((x - lo) / s)", "r = np.floor((x - lo) / s + np.float32(0.5))"),
     "last full page read as residual": ("nfull = n // PAGE_TOKENS",
                                         "nfull = (n - 1) // PAGE_TOKENS"),
