@@ -368,9 +368,12 @@ size_t pa_kitty_workspace_size(const pa_kitty_dims *dims);
  * p < floor(n_i / 128) is a record id in `pages`; when n_i % 128 > 0, block_tables[i][floor(n_i /
  * 128)] is a residual page id in res_k / res_v.  For query head h (KV head h / g):
  *     out[i, h, :] = sum_{p < n_i} softmax_p(scale * q[i, h, :] . K_i[p]) V_i[p]
- * with K_i[p], V_i[p] the dequantised values (or the residual page's values).  Arithmetic: the
- * dot products take the query times each channel's scale rounded to f16 and the codes exactly,
- * with fp32 accumulation; P times the V scale is rounded to f16 in the weighted V sum.
+ * with K_i[p], V_i[p] the dequantised values (or the residual page's values).  Arithmetic: per
+ * page, the query times each channel's scale is rounded to a 16-bit integer grid whose largest
+ * magnitude lies in [2^13, 2^14), and its products with the codes are summed exactly (int32); per
+ * half page (64 tokens), P times the token's V scale is rounded to a 16-bit grid the same way and
+ * its products with the V codes are summed exactly; the page's partial sums are scaled back to
+ * fp32.  The residual page runs in fp32 on the 16-bit values.
  * Workspace: pa_kitty_workspace_size(dims) bytes, 256-byte aligned, contents clobbered.
  * q_lens[i] != 1, ctx_lens[i] < 0 or n_i > max_pages_per_seq * 128 -> that sequence's rows are
  * not written, PA_DEV_BAD_LENGTHS; a page or residual id outside its pool -> that page is

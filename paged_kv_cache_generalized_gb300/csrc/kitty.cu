@@ -8,21 +8,26 @@
 // comparison with every other channel, ties to the lower id).  Codes by float32 subtract, divide
 // and round-half-even, four threads per channel (a quarter of the tokens each); 16 channels' low
 // bits meet in one word through shuffles, high bits through shared-memory ORs.  V: one warp per
-// token, a lane per 4 channels, min/max by shuffles.
+// token, a lane per 4 channels, min/max by shuffles; the codes by a thread per (half page,
+// channel, 16 tokens), packed channel-major per half page.
 //
 // kitty_decode_kernel: persistent, 16 warps per CTA (128 registers each), one CTA per SM.  Phase 1
 // streams the quantised pages: a work item is (sequence, query head, up to kChunkPages pages);
 // each warp runs a 2-stage ring of half pages (64 keys of one (page, KV head) record: the half's
 // codes, V scales and minimums, and on the first half the K scales, minimums and promoted ids),
 // filled by bulk copies with mbarrier completion, and claims its next item while the current one
-// computes, so the ring runs across items.  The a_x pairs sit in the warp's shared scratch.  Per
-// page the warp folds each channel's scale into the query (a_x = scale * q_x * s_x, and
-// b = scale * sum_x q_x min_x), so a key's score is b + sum_x a_x code_x.  The codes are never
-// unpacked: masking a 2-bit field of a 32-bit word in place leaves, in each 16-bit half, an f16
-// subnormal equal to code * 2^(2j - 24) (j = the field's position in the half), which a
-// mixed-precision FMA multiplies by a_x pre-scaled by 2^-2j as f16 -- one AND per two codes and one
-// FMA per code, fp32 accumulators.  One lane per key for QK^T; for PV a lane owns 16 channels
-// of every fourth key, and P * s_t (rounded to f16) meets the V codes the same way; the V minimum
+// computes, so the ring runs across items.  Per page the warp folds each channel's scale into the
+// query (a_x = scale * q_x * s_x, and b = scale * sum_x q_x min_x), so a key's score is
+// b + sum_x a_x code_x, and puts a_x on a 16-bit integer grid (the page's largest |a_x| at
+// 2^13..2^14).  The codes are never unpacked to floats: masking field j of a 32-bit word of codes
+// in place leaves four bytes code * 4^j (<= 192), and dp2a multiplies two of them by two 16-bit
+// weights and adds both to an int32 -- one AND per four codes and one instruction per two codes,
+// exact sums, the 4^j divided out once per field.  QK^T: one lane per key, the weights as pairs in
+// shared memory in the order of the masked bytes (channels j, 4 + j, 8 + j, 12 + j of a word); the
+// promoted channels' high bits the same way, times 4 after the sum.  After one online-softmax
+// step over the half's 64 keys, P times the token's V scale goes on the half's 16-bit grid (its
+// largest at 2^13..2^14) in shared memory, in the order of the channel-major V words' bytes, and
+// PV takes one lane per 4 channels the same way; the V minimum
 // contributes sum_t p_t min_t.  Phase 2 runs each sequence's residual page (fewer than 128
 // unquantised tokens) as one more item with plain loads.  Items of one row merge by the
 // logsumexp rule: the last split to finish reads the others' (m, l, o) records through L2.  Every
@@ -79,6 +84,7 @@ __global__ void __launch_bounds__(kQThreads) kitty_quantize_kernel(QuantParams p
     __shared__ int s_slot[kDim];                     // promoted slot of a channel, or -1
     __shared__ int s_cnt[4];
     __shared__ uint32_t s_hi[kPageTokens * kHiWords];
+    __shared__ float s_vlo[kPageTokens], s_vsc[kPageTokens];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t pair = blockIdx.x;
     const int h = blockIdx.y;
@@ -166,7 +172,7 @@ __global__ void __launch_bounds__(kQThreads) kitty_quantize_kernel(QuantParams p
         }
     }
 
-    // V: one warp per token, lane l owns channels 4l..4l+3
+    // V scale and minimum: one warp per token, lane l reads channels 4l..4l+3
     for (int t = warp; t < kPageTokens; t += kQThreads / 32) {
         float v[4];
         load_f<T, 4>(s_v + t * kDim + 4 * lane, v);
@@ -177,22 +183,31 @@ __global__ void __launch_bounds__(kQThreads) kitty_quantize_kernel(QuantParams p
             lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
             hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
         }
-        const float sv = __fdiv_rn(__fsub_rn(hi, lo), 3.f);
-        uint32_t b = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            uint32_t c = 0;
-            if (sv != 0.f) c = (uint32_t)fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[e], lo), sv)), 0.f), 3.f);
-            b |= c << (2 * e);
-        }
-        uint32_t w = b << (8 * (lane & 3));
-        w |= __shfl_xor_sync(0xffffffffu, w, 1);
-        w |= __shfl_xor_sync(0xffffffffu, w, 2);
-        if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(rec + off_vc(P) + t * 32)[lane >> 2] = w;
         if (lane == 0) {
+            const float sv = __fdiv_rn(__fsub_rn(hi, lo), 3.f);
+            s_vlo[t] = lo;
+            s_vsc[t] = sv;
             reinterpret_cast<float *>(rec + kOffVs)[t] = sv;
             reinterpret_cast<float *>(rec + kOffVm)[t] = lo;
         }
+    }
+    __syncthreads();
+    // V codes, channel-major per half page: thread (half hf, channel x, word w) packs tokens
+    // 64 hf + 16 w + i (i = 0..15) of channel x at bits 2 i of one 32-bit word
+    for (int i = tid; i < 2 * kDim * 4; i += kQThreads) {
+        const int w = i & 3, x = (i >> 2) & (kDim - 1), hf = i >> 9;
+        uint32_t word = 0;
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+            const int t = 64 * hf + 16 * w + k;
+            const float sv = s_vsc[t];
+            uint32_t c = 0;
+            if (sv != 0.f)
+                c = (uint32_t)fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(Elem<T>::to_f(s_v[t * kDim + x]), s_vlo[t]), sv)),
+                                          0.f), 3.f);
+            word |= c << (2 * k);
+        }
+        reinterpret_cast<uint32_t *>(rec + off_vc(P) + 2048 * hf + 16 * x)[w] = word;
     }
     __syncthreads();
     for (int i = tid; i < kPageTokens * kHiWords; i += kQThreads)
@@ -424,6 +439,19 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t &a, uint32_t &b, 
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
 }
 
+// d = c + a.lo * b.byte0 + a.hi * b.byte1 (dp2a_lo) or with bytes 2, 3 (dp2a_hi): two signed 16-bit
+// weights times two unsigned 8-bit codes, exact in int32.
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // Shared memory of the decode kernel: per warp kStages half-page stages and a scratch area, the
 // ring's mbarriers, then the per-sequence item prefix.
 __host__ __device__ constexpr size_t dec_smem_bytes(int P, int num_seqs) {
@@ -444,9 +472,13 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
                      warp * kStages;
     int *s_cu = reinterpret_cast<int *>(smem + (size_t)kDecWarps * (kStages * HS + kScratchBytes) +
                                         kDecWarps * kStages * 8);
-    float *s_a = reinterpret_cast<float *>(scratch);                       // a_x, fp32
-    uint16_t *s_lo = reinterpret_cast<uint16_t *>(scratch + 512);          // 64 f16 pairs
-    uint16_t *s_hi = reinterpret_cast<uint16_t *>(scratch + 512 + 256);    // 16 f16 pairs
+    // per warp: the page's query weights on a 16-bit grid (channel order), the same as dp2a
+    // pairs in the order of the unpacked low-bit and high-bit code bytes, and the half page's P
+    // on a 16-bit grid in the order of the unpacked V code bytes
+    int16_t *s_q16 = reinterpret_cast<int16_t *>(scratch);                 // [128]
+    int16_t *s_wlo = reinterpret_cast<int16_t *>(scratch + 256);           // [8 words][4 fields][2][2]
+    int16_t *s_whi = reinterpret_cast<int16_t *>(scratch + 512);           // [P / 16][4][2][2]
+    int16_t *s_p16 = reinterpret_cast<int16_t *>(scratch + 576);           // [4 words][4][2][2]
 
     // item prefix over sequences: sequence s has quant_chunks(n_s) * q_heads quantised items
     {
@@ -560,9 +592,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
 #pragma unroll
         for (int e = 0; e < 4; ++e) qs[e] *= p.scale_log2;
         float m_run = -INFINITY, l_l = 0.f, bv_l = 0.f;
-        float o[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = 0.f;
+        float o[4] = {0.f, 0.f, 0.f, 0.f};         // channels 4 lane .. 4 lane + 3, units of 2^-F
         int F_cur = 0;
         bool have_F = false;
         float b = 0.f, zmul = 0.f;                  // of the current page, set by its first half
@@ -580,56 +610,75 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
                 const unsigned char *st = ring + slot * HS;
                 if (page_ok) {
                     if (hh == 0) {
-                        // page prologue: a_x = scale q_x s_x, b = scale sum_x q_x min_x; f16 pairs
-                        // of a_x scaled by 2^(E - 2 (x % 4)), E putting max |a| in [2^12, 2^13)
+                        // page prologue: a_x = scale q_x s_x on a 16-bit grid, qi_x = rint(a_x 2^E)
+                        // with E putting max |a| in [2^13, 2^14); b = scale sum_x q_x min_x
                         const float4 ks = reinterpret_cast<const float4 *>(st + kHsKs)[lane];
                         const float4 km = reinterpret_cast<const float4 *>(st + kHsKm)[lane];
                         const float a[4] = {qs[0] * ks.x, qs[1] * ks.y, qs[2] * ks.z, qs[3] * ks.w};
                         b = wsum(qs[0] * km.x + qs[1] * km.y + qs[2] * km.z + qs[3] * km.w);
                         const float amax =
                             warp_max(fmaxf(fmaxf(fabsf(a[0]), fabsf(a[1])), fmaxf(fabsf(a[2]), fabsf(a[3]))));
-                        const int E = amax > 0.f ? max(-100, min(100, 12 - exponent_of(amax))) : 0;
-                        __syncwarp();                     // the previous page's pairs are read
+                        const int E = amax > 0.f ? max(-100, min(100, 13 - exponent_of(amax))) : 0;
+                        const float sE = pow2f(E);
+                        __syncwarp();                     // the previous page's weights are read
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int x = 4 * lane + e;
-                            s_a[x] = a[e];
-                            s_lo[((x >> 4) * 8 + (x & 7)) * 2 + ((x >> 3) & 1)] = f16_from_f32(a[e] * pow2f(E - 2 * e));
+                            // channel x = 4 lane + e = 16 w + 4 a + e: byte a of field e of word w
+                            const int16_t qi = (int16_t)__float2int_rn(a[e] * sE);
+                            const int w = lane >> 2, aa = lane & 3;
+                            s_q16[4 * lane + e] = qi;
+                            s_wlo[2 * ((w * 4 + e) * 2 + (aa >> 1)) + (aa & 1)] = qi;
                         }
                         __syncwarp();
                         if (lane < P) {
-                            const int x = st[kHsPid + lane];
-                            s_hi[((lane >> 4) * 8 + (lane & 7)) * 2 + ((lane >> 3) & 1)] =
-                                f16_from_f32(4.f * s_a[x] * pow2f(E - 2 * (lane & 3)));
+                            // promoted slot k = lane: its high-bit weight (x 4 after the sums)
+                            const int w = lane >> 4, i = lane & 15, aa = i >> 2, e = i & 3;
+                            s_whi[2 * ((w * 4 + e) * 2 + (aa >> 1)) + (aa & 1)] = s_q16[st[kHsPid + lane]];
                         }
                         __syncwarp();
-                        zmul = pow2f(24 - E);
+                        zmul = pow2f(-E);
                     }
-                    // V: F puts this half's largest token scale in [2^14, 2^15); o is kept in units of 2^F
+                    // V: F puts this half's largest token scale in [2^13, 2^14); o is kept in units of 2^-F
                     const float *vsc = reinterpret_cast<const float *>(st + kHsVs);
                     const float *vmn = reinterpret_cast<const float *>(st + kHsVm);
                     const float vmax = warp_max(fmaxf(vsc[lane], vsc[lane + 32]));
-                    const int F = vmax > 0.f ? max(-60, min(60, 14 - exponent_of(vmax))) : 0;
+                    const int F = vmax > 0.f ? max(-60, min(60, 13 - exponent_of(vmax))) : 0;
                     if (!have_F) {
                         F_cur = F;
                         have_F = true;
                     } else if (F != F_cur) {
                         const float r = pow2f(F - F_cur);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] *= r;
+                        for (int i = 0; i < 4; ++i) o[i] *= r;
                         F_cur = F;
                     }
                     const float psc = pow2f(F_cur);
-                    const int u = lane >> 3, wv = lane & 7;
-                    const uint32_t s_lo_a = smem_addr(s_lo), s_hi_a = smem_addr(s_hi);
+                    const uint32_t wlo_a = smem_addr(s_wlo), whi_a = smem_addr(s_whi);
 
+                    float z0 = 0.f, z1 = 0.f;               // keys lane and 32 + lane of the half
 #pragma unroll 1
                     for (int pass = 0; pass < 2; ++pass) {
                         const int t = pass * 32 + lane;
-                        // QK^T, one key per lane; the a_x pairs come from shared memory (broadcast)
+                        // QK^T, one key per lane: the codes unpacked to bytes (field j of a word holds
+                        // channels j, 4 + j, 8 + j, 12 + j) meet the weight pairs in dp2a (exact int32)
                         const uint4 *kl = reinterpret_cast<const uint4 *>(st + kHsKlo + t * 32);
                         const uint4 w0 = kl[0], w1 = kl[1];
                         const uint32_t kw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        // field j masked in place: bytes code * 4^j (<= 192), one accumulator per field,
+                        // the 4^j divided out exactly at the end
+                        int acc[4] = {0, 0, 0, 0}, acch[4] = {0, 0, 0, 0};
+#pragma unroll
+                        for (int wd = 0; wd < 8; ++wd) {
+                            uint32_t wp[8];
+                            lds128(wlo_a + wd * 32, wp[0], wp[1], wp[2], wp[3]);
+                            lds128(wlo_a + wd * 32 + 16, wp[4], wp[5], wp[6], wp[7]);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t u = kw[wd] & (0x03030303u << (2 * j));
+                                acc[j] = dp2a_lo(wp[2 * j], u, acc[j]);
+                                acc[j] = dp2a_hi(wp[2 * j + 1], u, acc[j]);
+                            }
+                        }
                         uint32_t hw[P / 16];
                         if constexpr (P == 32) {
                             const uint2 h2 = *reinterpret_cast<const uint2 *>(st + kHsKhi + t * 8);
@@ -638,65 +687,70 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
                         } else {
                             hw[0] = *reinterpret_cast<const uint32_t *>(st + kHsKhi + t * 4);
                         }
-                        float acc[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-#pragma unroll
-                        for (int wd = 0; wd < 8; ++wd) {
-                            uint32_t ap[8];
-                            lds128(s_lo_a + wd * 32, ap[0], ap[1], ap[2], ap[3]);
-                            lds128(s_lo_a + wd * 32 + 16, ap[4], ap[5], ap[6], ap[7]);
-                            const uint32_t x = kw[wd], y = x >> 8;
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                fma_h2(ap[j], x & (0x00030003u << (2 * j)), acc[2 * j], acc[2 * j + 1]);
-                                fma_h2(ap[4 + j], y & (0x00030003u << (2 * j)), acc[8 + 2 * j], acc[9 + 2 * j]);
-                            }
-                        }
 #pragma unroll
                         for (int wd = 0; wd < P / 16; ++wd) {
-                            uint32_t ap[8];
-                            lds128(s_hi_a + wd * 32, ap[0], ap[1], ap[2], ap[3]);
-                            lds128(s_hi_a + wd * 32 + 16, ap[4], ap[5], ap[6], ap[7]);
-                            const uint32_t x = hw[wd], y = x >> 8;
+                            uint32_t wp[8];
+                            lds128(whi_a + wd * 32, wp[0], wp[1], wp[2], wp[3]);
+                            lds128(whi_a + wd * 32 + 16, wp[4], wp[5], wp[6], wp[7]);
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                fma_h2(ap[j], x & (0x00030003u << (2 * j)), acc[2 * j], acc[2 * j + 1]);
-                                fma_h2(ap[4 + j], y & (0x00030003u << (2 * j)), acc[8 + 2 * j], acc[9 + 2 * j]);
+                                const uint32_t u = hw[wd] & (0x03030303u << (2 * j));
+                                acch[j] = dp2a_lo(wp[2 * j], u, acch[j]);
+                                acch[j] = dp2a_hi(wp[2 * j + 1], u, acch[j]);
                             }
                         }
+                        const int dot = (acc[0] + (acc[1] >> 2)) + ((acc[2] >> 4) + (acc[3] >> 6)) +
+                                        4 * ((acch[0] + (acch[1] >> 2)) + ((acch[2] >> 4) + (acch[3] >> 6)));
+                        const float z = fmaf((float)dot, zmul, b);
+                        if (pass == 0) z0 = z;
+                        else z1 = z;
+                    }
+                    // online softmax over the half's 64 keys (one max, so every P of the half
+                    // refers to the same m_run)
+                    const float mloc = warp_max(fmaxf(z0, z1));
+                    if (mloc > m_run) {
+                        const float al = fast_exp2(m_run - mloc);
+                        l_l *= al;
+                        bv_l *= al;
 #pragma unroll
-                        for (int i = 8; i > 0; i >>= 1)
+                        for (int i = 0; i < 4; ++i) o[i] *= al;
+                        m_run = mloc;
+                    }
 #pragma unroll
-                            for (int k = 0; k < i; ++k) acc[k] += acc[k + i];
-                        const float z = fmaf(acc[0], zmul, b);
-                        // online softmax
-                        const float mloc = warp_max(z);
-                        if (mloc > m_run) {
-                            const float al = fast_exp2(m_run - mloc);
-                            l_l *= al;
-                            bv_l *= al;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) o[i] *= al;
-                            m_run = mloc;
-                        }
-                        const float pz = fast_exp2(z - m_run);
+                    for (int pass = 0; pass < 2; ++pass) {
+                        const int t = pass * 32 + lane;
+                        const float pz = fast_exp2((pass == 0 ? z0 : z1) - m_run);
                         l_l += pz;
                         bv_l = fmaf(pz, vmn[t], bv_l);
-                        const uint32_t ph = f16_from_f32(pz * vsc[t] * psc);
-                        // PV: lane (u, wv) takes word wv (channels 16 wv .. 16 wv + 15) of keys 4 i + u
+                        // P times the V scale on the half page's 16-bit grid, stored where the V
+                        // pair products want it: token t = 16 w + 4 a + j -> field j of word w, byte a
+                        const int w = t >> 4, aa = (t >> 2) & 3, j = t & 3;
+                        s_p16[2 * ((w * 4 + j) * 2 + (aa >> 1)) + (aa & 1)] =
+                            (int16_t)__float2int_rn(pz * vsc[t] * psc);
+                    }
+                    __syncwarp();
+                    // P V: lane l takes channels 4 l .. 4 l + 3 over the half's 64 tokens; a V word
+                    // holds 16 tokens of one channel, field j of it tokens j, 4 + j, 8 + j, 12 + j
+                    {
+                        const uint4 *vc = reinterpret_cast<const uint4 *>(st + hs_vc(P) + 64 * lane);
+                        uint32_t pp[32];
+                        const uint32_t p_a = smem_addr(s_p16);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int tok = 4 * i + u;
-                            const uint16_t pt = (uint16_t)__shfl_sync(0xffffffffu, ph, tok);
-                            const uint32_t x =
-                                *reinterpret_cast<const uint32_t *>(st + hs_vc(P) + (pass * 32 + tok) * 32 + wv * 4);
-                            const uint32_t y = x >> 8;
+                        for (int i = 0; i < 8; ++i) lds128(p_a + 16 * i, pp[4 * i], pp[4 * i + 1], pp[4 * i + 2], pp[4 * i + 3]);
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                fma_h2s(x & (0x00030003u << (2 * j)), pt, o[2 * j], o[2 * j + 1]);
-                                fma_h2s(y & (0x00030003u << (2 * j)), pt, o[8 + 2 * j], o[9 + 2 * j]);
-                            }
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 v = vc[c];
+                            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+                            int af[4] = {0, 0, 0, 0};       // per field j, in units of 4^j
+#pragma unroll
+                            for (int w = 0; w < 4; ++w)
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const uint32_t u = vw[w] & (0x03030303u << (2 * j));
+                                    af[j] = dp2a_lo(pp[(w * 4 + j) * 2], u, af[j]);
+                                    af[j] = dp2a_hi(pp[(w * 4 + j) * 2 + 1], u, af[j]);
+                                }
+                            o[c] += (float)((af[0] + (af[1] >> 2)) + ((af[2] >> 4) + (af[3] >> 6)));
                         }
                     }
                 }
@@ -707,37 +761,19 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
         }
         if (dead) break;
 
-        // item epilogue: o[2 jj + h] holds channel 16 wv + jj + 8 h in units of 2^(2 (jj % 4) - 24 + F)
+        // item epilogue: out[x] = (o[x] 2^-F + sum_t p_t min_t) / l for this lane's 4 channels
         const float l = wsum(l_l), bv = wsum(bv_l);
+        const float f = pow2f(-F_cur);
+        float res[4];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            o[i] += __shfl_xor_sync(0xffffffffu, o[i], 8);
-            o[i] += __shfl_xor_sync(0xffffffffu, o[i], 16);
-        }
-        float res[16];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            const float f = pow2f(24 - 2 * (jj & 3) - F_cur);
-            res[jj] = fmaf(o[2 * jj], f, bv);
-            res[jj + 8] = fmaf(o[2 * jj + 1], f, bv);
-        }
+        for (int i = 0; i < 4; ++i) res[i] = fmaf(o[i], f, bv);
         if (cur.nch == 1) {
-            if (lane < 8) {
-                const float inv = 1.f / l;
-                float v0[8], v1[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v0[i] = res[i] * inv, v1[i] = res[8 + i] * inv;
-                T *dst = reinterpret_cast<T *>(p.out) + (size_t)row * kDim + 16 * lane;
-                store_f<T, 8>(dst, v0);
-                store_f<T, 8>(dst + 8, v1);
-            }
+            const float inv = 1.f / l;
+            float v[4] = {res[0] * inv, res[1] * inv, res[2] * inv, res[3] * inv};
+            store_f<T, 4>(reinterpret_cast<T *>(p.out) + (size_t)row * kDim + 4 * lane, v);
         } else {
             float *rec = p.parts + ((size_t)row * p.max_chunks + cur.k) * kPartFloats;
-            if (lane < 8) {
-                float4 *dst = reinterpret_cast<float4 *>(rec + 4 + 16 * lane);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_float4(res[4 * i], res[4 * i + 1], res[4 * i + 2], res[4 * i + 3]);
-            }
+            reinterpret_cast<float4 *>(rec + 4)[lane] = make_float4(res[0], res[1], res[2], res[3]);
             if (lane == 0) {
                 rec[0] = m_run;
                 rec[1] = l;
