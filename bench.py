@@ -19,6 +19,9 @@ Workloads (``--workload``):
               bytes per token.  Metric: GB/s (of the 8-bit bytes); the line also gives tokens/s.
   mixed_gqa   32 resumed conversations (history U{1024..16384}, new turn U{16..512}) + 32 decode
               sequences, GQA 32/8, d=128, bf16, block 32.  Metric: attention TFLOP/s (causal-exact).
+  mixed_gqa_fp8  the mixed_gqa batch with FP8 E4M3 K/V caches (scale 1/32): the resumed turns'
+              blocks widened to bf16 in workspace scratch, then the tcgen05 kernel; decode rows on
+              the CUDA-core E4M3 kernel.  Metric: TFLOP/s.
   longprefill 8 x (16384 cached + 2048 new), 40 MHA heads, d=128, bf16, block 16, ConvKV-style
               turn segments.  Metric: attention TFLOP/s.
   kvmove      40-layer 5120-hidden fp16 pool (8 layers resident), 64 sessions: append, 10%
@@ -223,7 +226,7 @@ def attn_accounting(batch, cow_frac=0.0, seed=0, kv8=False):
     Hq, Hkv, d = batch.num_q_heads, batch.num_kv_heads, batch.head_dim
     T = batch.total_q
     nb = (n + B - 1) // B
-    tc = tc_rows(batch) if not kv8 else np.zeros(batch.num_seqs, bool)
+    tc = tc_rows(batch)
     return {"pairs": pairs,
             "bytes_attn_tc": float(n[tc].sum() * Hkv * d * ek * 2 + 2 * batch.q_lens[tc].sum() * Hq * d * es
                                    + nb[tc].sum() * 4 + tc.sum() * 8),
@@ -260,7 +263,8 @@ def kitty_accounting(batch, R=None):
 
 
 # (copy-on-write fraction, seed of the fork draw) of the attention workloads
-ATTN_COW = {"decode13b": (0.1, 2), "decode13b_fp8": (0.1, 2), "mixed_gqa": (0.0, 3), "longprefill": (0.0, 4)}
+ATTN_COW = {"decode13b": (0.1, 2), "decode13b_fp8": (0.1, 2), "mixed_gqa": (0.0, 3), "mixed_gqa_fp8": (0.0, 3),
+            "longprefill": (0.0, 4)}
 
 
 def workload_batch(name, args):
@@ -270,7 +274,7 @@ def workload_batch(name, args):
         return W.decode13b(seed=2, num_seqs=seqs or 64, poison=False)
     if name == "decode13b_kitty":
         return W.decode13b_kitty(seed=2, num_seqs=seqs or 64)
-    if name in ("mixed_gqa", "swap_pipeline"):
+    if name in ("mixed_gqa", "mixed_gqa_fp8", "swap_pipeline"):
         half = (seqs or 64) // 2
         return W.mixed_gqa(seed=3, n_resume=half, n_decode=half, poison=False)
     if name == "longprefill":
@@ -386,9 +390,11 @@ class AttnStep:
         self.d2h_bytes = self.out.numel() * self.out.element_size()
         # block_copy (if any fork) + the planner (whose extra blocks write the new tokens; E4M3
         # caches take a quantising append launch of their own) + the decode kernel (which merges
-        # its own splits) (+ the tensor-core kernel when some turn takes it)
-        self.has_tc = bool(tc_rows(batch).any()) and not kv8
-        self.launches_per_step = (1 if len(pairs) else 0) + (1 if kv8 else 0) + 2 + (1 if self.has_tc else 0)
+        # its own splits) (+ the tensor-core kernel when some turn takes it, after the widening
+        # of its E4M3 blocks; the workspace holds scratch for all of them)
+        self.has_tc = bool(tc_rows(batch).any())
+        self.launches_per_step = ((1 if len(pairs) else 0) + (1 if kv8 else 0) + 2 + (1 if self.has_tc else 0)
+                                  + (1 if self.has_tc and kv8 else 0))
 
     def _copy(self, inp):
         if inp["pairs"].shape[0]:
@@ -752,6 +758,8 @@ WORKLOAD_TEXT = {
                        "appended token per sequence and one page quantised",
     "mixed_gqa": "mixed_gqa: 32 resumed turns (ctx U{1024..16384}, q U{16..512}) + 32 decode "
                  "(ctx U{256..8192}), GQA 32/8, head_dim 128, bf16, block 32",
+    "mixed_gqa_fp8": "mixed_gqa_fp8: the mixed_gqa batch with FP8 E4M3 K/V caches (scale 1/32 for K and V), "
+                     "bf16 queries and outputs",
     "longprefill": "longprefill: 8 seqs x (16384 cached + 2048 new), 40 MHA heads, head_dim 128, "
                    "bf16, block 16, ConvKV turn segments 64..1024 tokens",
     "layout": "layout: the decode13b batch on one layer of an 8-layer pool, block-first [blocks, layers, K|V, heads, "
@@ -930,6 +938,9 @@ def metric_for(name):
     if name == "decode13b_kitty":
         return ("paged-attn decode KV GB/s over 2-bit pages with promoted 4-bit key channels (algorithmic "
                 "HBM bytes per step / step time)", "GB/s", True)
+    if name == "mixed_gqa_fp8":
+        return ("paged-attn mixed-prefill TFLOP/s with FP8 E4M3 K/V caches (causal-exact attention FLOPs / "
+                "step time)", "TFLOP/s", True)
     if name == "layout":
         return ("paged-attn decode KV GB/s on a block-first pool (one layer of L; all layers of a block "
                 "contiguous)", "GB/s", True)
@@ -1122,8 +1133,12 @@ def measure_attn_workload(name, args, dev, dist, world, local, peaks, peak_src, 
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
                 "frac": achieved / pk, "traffic": traffic, "traffic_source": tsrc,
                 "algorithmic_flops": tflops, "kernel_ms": kern_ms,
-                "kernel": "tc_attention_kernel (tcgen05) on the turns it runs, between events the library "
-                          "records around its launch",
+                "kernel": ("tc_attention_kernel (tcgen05) on the turns it runs, between events the library "
+                           "records around its launch"
+                           + (" (on their E4M3 blocks widened to bf16 by a kernel before it, which the "
+                              "call's time includes)" if step_obj.kv8 else "")) if tc_ms else
+                          "the whole attention call (CUDA-core kernels: no turn of this batch takes the "
+                          "tcgen05 kernel)",
                 "call_ms": attn_ms, "call_flops": step_obj.flops,
                 "call_achieved": step_obj.flops / (attn_ms * 1e-3) / 1e12,
                 "decode_bracket_ms": cc_ms, "algorithmic_bytes": tbytes,

@@ -91,8 +91,15 @@ typedef enum { PA_KV_SAME = 0, PA_KV_E4M3 = 1 } pa_kv_dtype;
  * Supported: dtype f32 / bf16 / f16; d in {64, 128}; B in {16, 32, 64, 128}; Hq % Hkv == 0;
  * 16-byte aligned q, out and caches; kv_block_stride * element size a multiple of 16 bytes.
  * E4M3 caches (kv_dtype = PA_KV_E4M3): dtype bf16 or f16, d = 128, finite k_scale, v_scale > 0;
- * kv_block_stride counts codes (bytes); every sequence runs on the CUDA-core kernels (the
- * tensor-core kernel needs both MMA operands of one type).
+ * kv_block_stride counts codes (bytes).  Decode rows run on the CUDA-core kernels, which read the
+ * codes.  A tcgen05 MMA takes both operands in one 16-bit type, so the blocks of the sequences
+ * the tensor-core kernel takes (the rule below, with scale * k_scale > 0) are first widened,
+ * exactly, into scratch blocks of the query dtype in the workspace past its required part; the K
+ * scale joins the softmax scale and the V scale the output normalisation.  The scratch holds as
+ * many blocks as the caller's workspace has room for (pa_forward_widen_bytes: enough for every
+ * sequence the kernel may take); such sequences are admitted in sequence order while all of their
+ * blocks fit, and the others run on the CUDA-core kernels, so any workspace of at least
+ * pa_forward_workspace_size bytes is valid.  Their key ranges are not cut into chunks.
  * Sequences with q_len * g >= 16 query rows per KV head run on the tcgen05 tensor-core kernel when
  * the dtype is bf16/f16, d = 128, g divides 128 and scale > 0 (one work item per KV head and pair
  * of 128-row query tiles; when a call has fewer such items than SMs, each item's key range is
@@ -127,6 +134,14 @@ typedef struct {
 } pa_dims;
 
 size_t pa_forward_workspace_size(const pa_dims *dims);
+
+/* Extra workspace, past pa_forward_workspace_size(dims), that lets every sequence the tensor-core
+ * kernel may take of an E4M3 call (dims with total_q > num_seqs and a shape that kernel supports)
+ * run on it: a candidate-block prefix ([num_seqs + 1] int32) and a block table ([num_seqs,
+ * max_blocks_per_seq] int32), each padded to 256 bytes, then widened K and V blocks for min(num_seqs, total_q / ceil(16 / g)) * max_blocks_per_seq
+ * blocks.  0 for other dims or invalid dims.  The bound is from the dims alone; a smaller extra
+ * (down to none) is valid and sends the sequences that do not fit to the CUDA-core kernels. */
+size_t pa_forward_widen_bytes(const pa_dims *dims);
 
 pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
                      const int32_t *block_tables, const int32_t *ctx_lens, const int32_t *q_lens,

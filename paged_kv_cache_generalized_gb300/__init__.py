@@ -5,7 +5,7 @@ this package holds the in-tree build, a thin ctypes binding and the seeded workl
 Calls raise if the library has not been built: there is no CPU fallback.
 """
 from .pagedkv import (PA_KV_E4M3, PA_KV_SAME, PagedKVError, block_copy, device_status,  # noqa: F401
-                      forward_workspace_size, kitty_record_bytes, kitty_workspace_size, kv_append,
+                      forward_widen_bytes, forward_workspace_size, kitty_record_bytes, kitty_workspace_size, kv_append,
                       kv_quantize_pages,
                       library_path, load_library, pa_forward, pa_forward_kitty,
                       pa_forward_append, pa_forward_no_alloc, set_timing_events, status_names,

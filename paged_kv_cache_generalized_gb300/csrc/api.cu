@@ -194,6 +194,42 @@ WsLayout ws_layout(const pa_dims &d) {
 
 bool tc_supported(const pa_dims &d) { return tc_shape_supported(d); }
 
+bool widen_eligible(const pa_dims &d) {
+    // the tensor-core kernel's shapes, from the dims alone (the call also needs the driver's
+    // tensor-map encoder); the planner's prefix of candidate blocks is int32
+    const int g = d.num_kv_heads > 0 ? d.num_q_heads / d.num_kv_heads : 0;
+    return d.kv_dtype == PA_KV_E4M3 && d.total_q > d.num_seqs && (d.dtype == PA_BF16 || d.dtype == PA_F16) &&
+           d.head_dim == 128 && g >= 1 && g <= kTcTileRows && kTcTileRows % g == 0 && d.block_size >= 16 &&
+           d.block_size <= 128 && d.total_q < (int64_t(1) << 31) &&
+           (int64_t)d.num_seqs * d.max_blocks_per_seq < (int64_t(1) << 31) - 1;
+}
+
+int64_t widen_bound_blocks(const pa_dims &d) {
+    // a tensor-core sequence has q_len * g >= kTcMinRows, so at most total_q / ceil(16 / g) of them
+    const int g = d.num_q_heads / d.num_kv_heads;
+    const int64_t qmin = (kTcMinRows + g - 1) / g;
+    int64_t n = d.total_q / qmin;
+    if (n > d.num_seqs) n = d.num_seqs;
+    return n * d.max_blocks_per_seq;
+}
+
+WidenLayout widen_layout(const pa_dims &d, size_t base, size_t workspace_bytes) {
+    WidenLayout w;
+    const size_t S = (size_t)d.num_seqs;
+    const size_t blk = (size_t)d.num_kv_heads * d.block_size * d.head_dim * elem_bytes(d.dtype);
+    const int64_t bound = widen_bound_blocks(d);
+    w.cu = base;
+    w.bt = align_up(w.cu + (S + 1) * 4, 256);
+    w.k = align_up(w.bt + S * (size_t)d.max_blocks_per_seq * 4, 256);
+    w.end = w.k + (size_t)bound * 2 * blk;
+    int64_t cap = workspace_bytes > w.k ? (int64_t)((workspace_bytes - w.k) / (2 * blk)) : 0;
+    if (cap > bound) cap = bound;
+    if (cap >= (int64_t(1) << 31) - 1) cap = (int64_t(1) << 31) - 2;   // block ids of the tensor map
+    w.cap = cap;
+    w.v = w.k + (size_t)cap * blk;
+    return w;
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -217,6 +253,12 @@ const char *pa_status_string(pa_status s) {
 size_t pa_forward_workspace_size(const pa_dims *dims) {
     if (check_dims(dims) != PA_OK) return 0;
     return ws_layout(*dims).total;
+}
+
+size_t pa_forward_widen_bytes(const pa_dims *dims) {
+    if (check_dims(dims) != PA_OK || !widen_eligible(*dims)) return 0;
+    const size_t base = ws_layout(*dims).total;
+    return widen_layout(*dims, base, 0).end - base;
 }
 
 }  // extern "C"
@@ -272,6 +314,18 @@ pa_status forward_impl(const pa_dims *dims, const void *q, const void *k_cache, 
     if (!a.status || a.num_sms <= 0) return PA_ERR_CUDA;
     a.maybe_prefill = d.total_q > d.num_seqs;
     a.tc = a.maybe_prefill && scale > 0.f && d.kv_dtype == PA_KV_SAME && tc_supported(d);
+    if (a.maybe_prefill && scale * d.k_scale > 0.f && widen_eligible(d) && tc_supported(d)) {
+        // E4M3 caches: the tensor-core kernel reads widened copies of its sequences' blocks
+        const WidenLayout w = widen_layout(d, lay.total, workspace_bytes);
+        if (w.cap > 0) {
+            a.tc = true;
+            a.wid_cap = w.cap;
+            a.wid_cu = reinterpret_cast<int32_t *>(a.ws + w.cu);
+            a.wid_bt = reinterpret_cast<int32_t *>(a.ws + w.bt);
+            a.wid_k = a.ws + w.k;
+            a.wid_v = a.ws + w.v;
+        }
+    }
     AppendParams ap;
     if (append) {
         ap = *append;
@@ -280,6 +334,7 @@ pa_status forward_impl(const pa_dims *dims, const void *q, const void *k_cache, 
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (launch_plan(a, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (a.wid_cap > 0 && launch_widen(a, s) != cudaSuccess) return PA_ERR_CUDA;
     if (a.tc) {
         // the tensor-core kernel right after the planner on the caller's stream, so that its CTAs
         // (one per SM, each holding the SM's whole register file) are dispatched first; the decode

@@ -46,9 +46,11 @@ struct PlanParams {
     int32_t *cu_q, *simt_cu, *parts_cu, *comb_cu, *groups, *nchunk, *tc_cu, *tc_seq;
     uint32_t *unit_cnt;
     uint32_t *tc_arrive;               // chunk arrival counters (when the workspace holds them)
+    int32_t *wid_cu;                   // E4M3 widening: prefix of candidate sequences' blocks
     unsigned *status;
     int64_t total_q;
     int64_t max_parts;
+    int64_t wid_cap;                   // widened blocks the scratch holds; -1: no widening (16-bit caches)
     int num_seqs, kv_heads, group, block_size, max_blocks, rows, tc, total_warps, tc_chunk_ok;
 };
 
@@ -114,6 +116,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p, Append
     const bool packing_ok = (total == p.total_q);
     if (!packing_ok && tid == 0) report(p.status, PA_DEV_BAD_LENGTHS);
 
+    // pass B0 (E4M3 caches): the blocks each tensor-core candidate would widen, in sequence
+    // order; a candidate takes the tensor-core kernel when all of its blocks fit the scratch
+    if (p.wid_cap >= 0) {
+        for (int i = tid; i < S; i += kPlanThreads) {
+            const int c = p.ctx[i], q = p.qlen[i];
+            const int64_t n = (int64_t)c + q;
+            const int64_t nb = (n + p.block_size - 1) / p.block_size;
+            const bool valid = packing_ok && q >= 1 && c >= 0 && nb <= p.max_blocks && n <= kMaxSeqTokens;
+            p.wid_cu[i] = (valid && p.tc && (int64_t)q * p.group >= kTcMinRows) ? (int32_t)nb : 0;
+        }
+        __syncthreads();
+        const int64_t wtotal = block_exclusive_scan(p.wid_cu, S);
+        if (tid == 0) p.counters[kWidTotal] = (uint32_t)(wtotal < p.wid_cap ? wtotal : p.wid_cap);
+    }
+
     // pass B: classify sequences, total CUDA-core work (block-heads) for the split size
     int64_t work = 0;
     for (int i = tid; i < S; i += kPlanThreads) {
@@ -123,7 +140,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p, Append
         const bool valid = packing_ok && q >= 1 && c >= 0 && nb <= p.max_blocks && n <= kMaxSeqTokens;
         if (packing_ok && !valid) report(p.status, PA_DEV_BAD_LENGTHS);
         int path = 0;
-        if (valid) path = (p.tc && (int64_t)q * p.group >= kTcMinRows) ? 2 : 1;
+        if (valid) {
+            const bool fits = p.wid_cap < 0 || (int64_t)p.wid_cu[i] + nb <= p.wid_cap;
+            path = (p.tc && (int64_t)q * p.group >= kTcMinRows && fits) ? 2 : 1;
+        }
         const int64_t rows = (int64_t)q * p.group;
         const int G = path == 1 ? (int)((rows + p.rows - 1) / p.rows) : 0;
         p.groups[i] = path == 0 ? -1 : G;    // -1 marks an invalid sequence
@@ -1556,6 +1576,8 @@ cudaError_t launch_plan(const FwdArgs &a, cudaStream_t s) {
     p.tc = a.tc ? 1 : 0;
     p.tc_chunk_ok = a.lay.tc_chunks ? 1 : 0;
     p.tc_arrive = a.lay.tc_chunks ? reinterpret_cast<uint32_t *>(a.ws + L.tc_arrive) : nullptr;
+    p.wid_cu = a.wid_cu;
+    p.wid_cap = a.wid_cap > 0 ? a.wid_cap : -1;
     p.total_warps = a.num_sms * 8;
     AppendParams ap{};
     int64_t grid = 1;

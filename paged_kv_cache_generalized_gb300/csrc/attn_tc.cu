@@ -254,6 +254,7 @@ struct TcParams {
     unsigned *status;
     int64_t num_blocks;
     float scale_log2;
+    float v_scale;                // 1, or the V scale of E4M3 caches (their widened codes)
     int num_seqs, q_heads, kv_heads, group, block_size, max_blocks;
 };
 
@@ -357,7 +358,7 @@ __device__ __forceinline__ int tile_block(const TcParams &p, const int32_t *bt_r
 // m = -3e38, weight 0), and writes the row (orow, if stored).
 template <typename T>
 __device__ __noinline__ void chunk_epilogue(const TcParams &p, int it, const Item &t, int u, int quad, int row,
-                                            int lane, uint32_t o_tmem, float m, float l, T *orow) {
+                                            int lane, uint32_t o_tmem, float m, float l, float v_scale, T *orow) {
     float *mine = p.part + ((size_t)(it * 2 + u) * kRows + row) * kTcPartFloats;
     mine[0] = m;
     mine[1] = l;
@@ -388,7 +389,7 @@ __device__ __noinline__ void chunk_epilogue(const TcParams &p, int it, const Ite
         const float mc = __ldcg(slot(c));
         L += mc == -INFINITY ? 0.f : fast_exp2(mc - M) * __ldcg(slot(c) + 1);
     }
-    const float inv = 1.f / L;
+    const float inv = (1.f / L) * v_scale;
 #pragma unroll 1
     for (int b = 0; b < kDim / 32; ++b) {
         float acc[32];
@@ -855,11 +856,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t.nchunk > 1) {
                 // one chunk of the pair's key range: this row's (m, l, O) to the item's partial
                 // slot; the last of the pair's chunks to finish (per warp of rows) merges them
-                chunk_epilogue<T>(p, it, t, u, quad, row, lane, o_tmem, m, l, store ? orow : nullptr);
+                chunk_epilogue<T>(p, it, t, u, quad, row, lane, o_tmem, m, l, p.v_scale, store ? orow : nullptr);
                 tc_fence_before();
                 continue;
             }
-            const float inv = 1.f / l;
+            const float inv = (1.f / l) * p.v_scale;
 #pragma unroll 1
             for (int c = 0; c < kDim / 32; ++c) {
                 uint32_t r[32];
@@ -906,20 +907,24 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s) {
     const pa_dims &d = a.dims;
     const int g = d.num_q_heads / d.num_kv_heads;
     const uint64_t es = 2;
-    const int64_t bstride = d.kv_block_stride ? d.kv_block_stride
-                                              : (int64_t)d.num_kv_heads * d.block_size * d.head_dim;
+    // E4M3 caches: the widened scratch blocks (dense, `wid_cap` of them) and their block table
+    const bool wide = a.wid_cap > 0;
+    const int64_t dense = (int64_t)d.num_kv_heads * d.block_size * d.head_dim;
+    const int64_t bstride = wide ? dense : (d.kv_block_stride ? d.kv_block_stride : dense);
+    const int64_t nblocks = wide ? a.wid_cap : d.num_blocks;
+    const void *kbase = wide ? a.wid_k : a.k, *vbase = wide ? a.wid_v : a.v;
     CUtensorMap qmap, kmap, vmap;
     if (!make_map_3d(&qmap, d.dtype, a.q, kDim, d.num_q_heads, d.total_q, kDim * es,
                      (uint64_t)d.num_q_heads * kDim * es, 64, g, kRows / g) ||
-        !make_map_3d(&kmap, d.dtype, a.k, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
+        !make_map_3d(&kmap, d.dtype, kbase, kDim, (uint64_t)d.num_kv_heads * d.block_size, nblocks,
                      kDim * es, bstride * es, 64, d.block_size, 1) ||
-        !make_map_3d(&vmap, d.dtype, a.v, kDim, (uint64_t)d.num_kv_heads * d.block_size, d.num_blocks,
+        !make_map_3d(&vmap, d.dtype, vbase, kDim, (uint64_t)d.num_kv_heads * d.block_size, nblocks,
                      kDim * es, bstride * es, 64, d.block_size, 1))
         return cudaErrorInvalidValue;
     TcParams p;
     const WsLayout &L = a.lay;
     p.out = static_cast<char *>(a.out);
-    p.bt = a.bt;
+    p.bt = wide ? a.wid_bt : a.bt;
     p.ctx = a.ctx;
     p.qlen = a.qlen;
     p.cu_q = reinterpret_cast<const int32_t *>(a.ws + L.cu_q);
@@ -929,8 +934,9 @@ cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s) {
     p.part = L.tc_chunks ? reinterpret_cast<float *>(a.ws + L.tc_part) : nullptr;
     p.arrive = L.tc_chunks ? reinterpret_cast<uint32_t *>(a.ws + L.tc_arrive) : nullptr;
     p.status = a.status;
-    p.num_blocks = d.num_blocks;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.num_blocks = nblocks;
+    p.scale_log2 = a.scale * 1.4426950408889634f * (wide ? d.k_scale : 1.f);
+    p.v_scale = wide ? d.v_scale : 1.f;
     p.num_seqs = d.num_seqs;
     p.q_heads = d.num_q_heads;
     p.kv_heads = d.num_kv_heads;

@@ -71,6 +71,7 @@ enum Counter : int {
     kCombTotal = 4,   // number of split-KV rows to combine (row groups x rows)
     kChunkBlocks = 5, // KV blocks per CUDA-core split
     kTcChunk = 6,     // KV tiles per tensor-core chunk (0: pair items are not chunked)
+    kWidTotal = 7,    // widened blocks to write (E4M3 caches on the tensor-core kernel)
     kNumCounters = 16
 };
 
@@ -97,6 +98,24 @@ struct WsLayout {
 };
 
 WsLayout ws_layout(const pa_dims &d);
+
+// E4M3 caches on the tensor-core kernel.  The blocks of the sequences it takes are widened
+// (exactly) to the query dtype into scratch past the workspace layout: the candidate-block prefix,
+// a remapped block table, then `cap` widened K blocks and `cap` V blocks.  `cap` is what the
+// caller's workspace holds, at most the bound for the dims; sequences whose blocks do not fit run
+// on the CUDA-core kernels.
+struct WidenLayout {
+    size_t cu;         // int32 [S+1]  prefix of candidate sequences' blocks (planner)
+    size_t bt;         // int32 [S * max_blocks_per_seq]  block table of the widened blocks
+    size_t k, v;       // [cap, Hkv, B, d] in the query dtype
+    size_t end;        // first byte past the V blocks for the bound (the size to ask for)
+    int64_t cap;       // widened blocks the caller's workspace holds (0: no widening)
+};
+// Whether E4M3 dims may widen at all (total_q > num_seqs and a shape the tensor-core kernel takes).
+bool widen_eligible(const pa_dims &d);
+// Widened blocks that cover every sequence the tensor-core kernel may take for these dims.
+int64_t widen_bound_blocks(const pa_dims &d);
+WidenLayout widen_layout(const pa_dims &d, size_t base, size_t workspace_bytes);
 int rows_per_item(const pa_dims &d);
 bool tc_supported(const pa_dims &d);
 bool tc_shape_supported(const pa_dims &d);  // attn_tc.cu
@@ -120,11 +139,19 @@ struct FwdArgs {
     bool tc;            // tensor-core kernel available for this call
     bool maybe_prefill; // some sequence may have q_len > 1
     const AppendParams *append = nullptr;   // new tokens written by the planner's launch (or none)
+    // E4M3 caches on the tensor-core kernel (wid_cap > 0): the widening scratch
+    int64_t wid_cap = 0;
+    int32_t *wid_cu = nullptr;
+    int32_t *wid_bt = nullptr;
+    void *wid_k = nullptr;
+    void *wid_v = nullptr;
 };
 
 cudaError_t launch_plan(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_simt(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_tc(const FwdArgs &a, cudaStream_t s);
+// The widening of the planned sequences' E4M3 blocks (widen.cu), after the planner.
+cudaError_t launch_widen(const FwdArgs &a, cudaStream_t s);
 
 cudaError_t launch_kv_append(const kv_append_dims &d, const void *k_new, const void *v_new,
                              const int64_t *slots, void *k_cache, void *v_cache, unsigned *status,

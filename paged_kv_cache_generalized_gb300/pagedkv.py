@@ -31,7 +31,7 @@ PA_KV_SAME, PA_KV_E4M3 = 0, 1
 _E4M3 = tuple(t for t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if t is not None)
 _ELEM = {torch.float32: 4, torch.bfloat16: 2, torch.float16: 2}
 
-EXPORTED = ("pa_forward_workspace_size", "pa_forward", "pa_forward_no_alloc", "pa_forward_append", "pa_set_timing_events", "kv_append",
+EXPORTED = ("pa_forward_workspace_size", "pa_forward_widen_bytes", "pa_forward", "pa_forward_no_alloc", "pa_forward_append", "pa_set_timing_events", "kv_append",
             "block_copy", "pa_get_device_status", "pa_status_string", "pa_version",
             "pa_kitty_record_bytes", "pa_kitty_workspace_size", "kv_quantize_pages",
             "pa_forward_kitty")
@@ -94,6 +94,8 @@ def load_library(path: str | None = None):
     P, sz = ctypes.c_void_p, ctypes.c_size_t
     lib.pa_forward_workspace_size.restype = sz
     lib.pa_forward_workspace_size.argtypes = [ctypes.POINTER(PaDims)]
+    lib.pa_forward_widen_bytes.restype = sz
+    lib.pa_forward_widen_bytes.argtypes = [ctypes.POINTER(PaDims)]
     lib.pa_forward.restype = ctypes.c_int
     lib.pa_forward.argtypes = [ctypes.POINTER(PaDims), P, P, P, P, P, P, ctypes.c_float, P, P, sz, P]
     lib.pa_forward_no_alloc.restype = ctypes.c_int
@@ -194,8 +196,21 @@ def _forward_args(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, k_scale, 
 
 
 def forward_workspace_size(q, k_cache, block_tables, ctx_lens) -> int:
+    """Workspace bytes for pa_forward on these shapes: the required part, plus (E4M3 caches with
+    multi-token turns) the widening scratch that lets every tensor-core sequence widen."""
     dims = forward_dims(q, k_cache, block_tables, ctx_lens, 1.0, 1.0)
-    return int(load_library().pa_forward_workspace_size(ctypes.byref(dims)))
+    return _workspace_bytes(load_library(), dims)
+
+
+def forward_widen_bytes(q, k_cache, block_tables, ctx_lens) -> int:
+    """The widening scratch part of forward_workspace_size (0 unless the caches are E4M3)."""
+    dims = forward_dims(q, k_cache, block_tables, ctx_lens, 1.0, 1.0)
+    return int(load_library().pa_forward_widen_bytes(ctypes.byref(dims)))
+
+
+def _workspace_bytes(lib, dims) -> int:
+    base = int(lib.pa_forward_workspace_size(ctypes.byref(dims)))
+    return base + int(lib.pa_forward_widen_bytes(ctypes.byref(dims))) if base else 0
 
 
 def pa_forward(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale=None, out=None,
@@ -211,7 +226,7 @@ def pa_forward(q, k_cache, v_cache, block_tables, ctx_lens, q_lens, scale=None, 
         scale = 1.0 / float(dims.head_dim) ** 0.5
     if out is None:
         out = torch.empty_like(q)
-    need = int(lib.pa_forward_workspace_size(ctypes.byref(dims)))
+    need = _workspace_bytes(lib, dims)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     rc = lib.pa_forward(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache),
@@ -267,7 +282,7 @@ def pa_forward_append(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tab
         scale = 1.0 / float(dims.head_dim) ** 0.5
     if out is None:
         out = torch.empty_like(q)
-    need = int(lib.pa_forward_workspace_size(ctypes.byref(dims)))
+    need = _workspace_bytes(lib, dims)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     rc = lib.pa_forward_append(ctypes.byref(dims), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),

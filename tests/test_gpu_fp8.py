@@ -50,7 +50,7 @@ CASES = [
     ("decode_mha", [512, 1000, 37, 4096, 15], [1] * 5, 8, 8, 16, "bf16", 1 / 32, 1 / 16),
     ("decode_gqa4", [700, 33, 2000, 0], [1] * 4, 16, 4, 32, "bf16", 0.05, 0.02),
     ("decode_gqa2_f16", [300, 129, 64], [1] * 3, 8, 4, 16, "f16", 1 / 64, 1 / 64),
-    ("turns_on_cuda_cores", [300, 0, 129], [40, 33, 5], 8, 2, 16, "bf16", 0.03, 0.03),
+    ("turns_widened_gqa4", [300, 0, 129], [40, 33, 5], 8, 2, 16, "bf16", 0.03, 0.03),
     ("mha_turns", [100, 7], [20, 3], 4, 4, 64, "bf16", 1.0 / 8, 0.25),
     ("long_split", [16000, 9000], [1, 1], 8, 8, 32, "bf16", 1 / 32, 1 / 32),
 ]
@@ -152,3 +152,123 @@ def test_no_alloc_entry_point_on_e4m3_caches():
     assert torch.equal(a, c)
     ref = oracle.paged_attention_batch(b, threads=8, kv=(kc, vc, 1 / 16, 1 / 16))
     assert_close(as_f64(c), ref, "bf16", "no-alloc e4m3")
+
+
+# ---- multi-token turns on the tensor-core kernel: blocks widened into workspace scratch ----
+
+def _up(x):
+    return (x + 255) // 256 * 256
+
+
+def _dev_args(b, kc, vc):
+    return (to_dev(b.q, b.dtype), torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(),
+            to_dev(b.block_tables), to_dev(b.ctx_lens), to_dev(b.q_lens))
+
+
+def _forward_ws(b, kc, vc, ks, vs, extra=None):
+    """pa_forward with a workspace of the required size plus ``extra`` widening bytes (None: the
+    size the library asks for); returns (out, the planner's counters)."""
+    q, k, v, bt, ctx, ql = _dev_args(b, kc, vc)
+    full = pkg.forward_workspace_size(q, k, bt, ctx)
+    widen = pkg.forward_widen_bytes(q, k, bt, ctx)
+    nbytes = full if extra is None else full - widen + extra
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    out = pkg.pa_forward(q, k, v, bt, ctx, ql, b.scale, workspace=ws, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    return out, ws[:64].view(torch.int32).cpu().numpy()
+
+
+TC_CASES = [
+    # name, ctx, q, Hq, Hkv, B, dtype, k_scale, v_scale
+    ("gqa4_bf16", [300, 0, 1000, 77], [130, 40, 257, 1], 16, 4, 16, "bf16", 0.03, 0.05),
+    ("gqa8_f16_b32", [129, 513, 0], [64, 3, 300], 32, 4, 32, "f16", 1 / 64, 1 / 32),
+    ("mha_b128", [200, 5, 640], [17, 16, 70], 4, 4, 128, "bf16", 0.25, 0.125),
+    ("gqa2_b64_ragged", [1, 64, 127, 1500], [33, 100, 15, 9], 8, 4, 64, "bf16", 0.02, 0.02),
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=[c[0] for c in TC_CASES])
+def test_e4m3_turns_take_the_tensor_core_kernel(case):
+    name, ctx, ql, hq, hkv, B, dtype, ks, vs = case
+    b, kc, vc = _fp8_batch(name, ctx, ql, hq, hkv, B, dtype, ks, vs, seed=len(name) * 17)
+    out, counters = _forward_ws(b, kc, vc, ks, vs)
+    assert pkg.device_status() == 0
+    g = hq // hkv
+    cand = [i for i in range(len(ctx)) if ql[i] * g >= 16]
+    blocks = sum((ctx[i] + ql[i] + B - 1) // B for i in cand)
+    assert counters[7] == blocks, "widened blocks"
+    assert counters[3] > 0, "no tile went to the tensor-core kernel"
+    ref = oracle.paged_attention_batch(b, threads=8, kv=(kc, vc, ks, vs))
+    assert_close(as_f64(out), ref, dtype, name)
+
+
+def test_e4m3_scratch_capacity_decides_which_turns_widen():
+    """Scratch for the first candidate's blocks only: it takes the tensor-core kernel, the later
+    candidates run on CUDA cores; with no scratch every turn runs on CUDA cores.  Same results."""
+    ctx, ql, B, hq, hkv = [700, 300, 50], [60, 200, 20], 16, 16, 4
+    b, kc, vc = _fp8_batch("fp8cap", ctx, ql, hq, hkv, B, "bf16", 1 / 32, 1 / 16, seed=57)
+    ref = oracle.paged_attention_batch(b, threads=8, kv=(kc, vc, 1 / 32, 1 / 16))
+    S, mb = len(ctx), b.block_tables.shape[1]
+    nb0 = (ctx[0] + ql[0] + B - 1) // B
+    header = _up(4 * (S + 1)) + _up(4 * S * mb)
+    blk = hkv * B * 128 * 2
+    outs = []
+    for extra, widened in ((header + nb0 * 2 * blk, nb0), (header + nb0 * 2 * blk + 2 * blk - 1, nb0), (0, None)):
+        out, counters = _forward_ws(b, kc, vc, 1 / 32, 1 / 16, extra=extra)
+        assert pkg.device_status() == 0
+        if widened is None:
+            assert counters[3] == 0
+        else:
+            assert counters[7] == widened and counters[3] > 0
+        assert_close(as_f64(out), ref, "bf16", f"extra={extra}")
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_e4m3_widened_equals_bf16_caches_with_power_of_two_scales():
+    """With power-of-two scales, bf16 caches holding code * scale give the tensor-core kernel
+    operands that differ from the widened codes by exact powers of two, so the outputs agree bit
+    for bit.  20 sequences x 8 KV heads of one tile pair each: 160 pair items, more than the SMs,
+    so neither call cuts key ranges into chunks."""
+    S, hq, hkv, B = 20, 32, 8, 16
+    ctx = [int(x) for x in np.random.default_rng(5).integers(0, 700, S)]
+    ql = [int(x) for x in np.random.default_rng(6).integers(4, 64, S)]
+    ks, vs = 1 / 32, 1 / 8
+    b, kc, vc = _fp8_batch("fp8pow2", ctx, ql, hq, hkv, B, "bf16", ks, vs, seed=61)
+    out8, counters = _forward_ws(b, kc, vc, ks, vs)
+    assert pkg.device_status() == 0 and counters[3] == S * hkv and counters[6] == 0
+    k16 = (torch.from_numpy(kc).cuda().view(torch.float8_e4m3fn).float() * ks).to(torch.bfloat16)
+    v16 = (torch.from_numpy(vc).cuda().view(torch.float8_e4m3fn).float() * vs).to(torch.bfloat16)
+    q, _, _, bt, c, qlen = _dev_args(b, kc, vc)
+    ws = torch.zeros(pkg.forward_workspace_size(q, k16, bt, c), dtype=torch.uint8, device="cuda")
+    out16 = pkg.pa_forward(q, k16, v16, bt, c, qlen, b.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkg.device_status() == 0
+    assert ws[:64].view(torch.int32)[6].item() == 0, "the bf16 call was chunked"
+    assert torch.equal(out8, out16)
+
+
+def test_e4m3_widening_flags_a_bad_block_id():
+    """A bad id in a widened sequence's table is flagged; the other sequences' rows are unharmed."""
+    b, kc, vc = _fp8_batch("fp8bad", [400, 90, 1000], [50, 30, 1], 16, 4, 16, "bf16", 1 / 32, 1 / 32, seed=67)
+    ref = oracle.paged_attention_batch(b, threads=8, kv=(kc, vc, 1 / 32, 1 / 32))
+    b.block_tables[0, 3] = b.k_cache.shape[0] + 5
+    out, counters = _forward_ws(b, kc, vc, 1 / 32, 1 / 32)
+    assert pkg.device_status() & 0x1                   # PA_DEV_BAD_BLOCK_ID
+    assert counters[3] > 0
+    keep = slice(int(b.q_lens[0]), int(b.q_lens.sum()))
+    assert_close(as_f64(out)[keep], ref[keep], "bf16", "other sequences")
+
+
+def test_e4m3_mixed_gqa_full_size():
+    """The mixed GQA batch (32 resumed turns of 16-512 new tokens over 1K-16K histories + 32
+    decodes) on E4M3 caches: turns widened onto the tensor-core kernel, sampled rows."""
+    b = W.mixed_gqa(poison=False)
+    ks, vs = 1 / 512, 1 / 256
+    kc, vc = _uniform_codes(b.k_cache.shape, 73), _uniform_codes(b.v_cache.shape, 74)
+    out, counters = _forward_ws(b, kc, vc, ks, vs)
+    assert pkg.device_status() == 0
+    assert counters[3] > 0 and counters[7] > 0
+    rows = sample_rows(b, 192, seed=5)
+    ref = oracle.paged_attention_batch(b, rows=rows, threads=16, kv=(kc, vc, ks, vs))
+    assert_close(gather_rows(out, b, rows), ref, b.dtype, "mixed_gqa e4m3")
