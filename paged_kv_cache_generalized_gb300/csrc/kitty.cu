@@ -592,7 +592,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
 #pragma unroll
         for (int e = 0; e < 4; ++e) qs[e] *= p.scale_log2;
         float m_run = -INFINITY, l_l = 0.f, bv_l = 0.f;
-        float o[4] = {0.f, 0.f, 0.f, 0.f};         // channels 4 lane .. 4 lane + 3, units of 2^-F
+        // o[c]: channel 4 lane + ((c + vrot) & 3), units of 2^-F
+        float o[4] = {0.f, 0.f, 0.f, 0.f};
+        const int vrot = (lane >> 1) & 3;
         int F_cur = 0;
         bool have_F = false;
         float b = 0.f, zmul = 0.f;                  // of the current page, set by its first half
@@ -638,10 +640,83 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
                         __syncwarp();
                         zmul = pow2f(-E);
                     }
-                    // V: F puts this half's largest token scale in [2^13, 2^14); o is kept in units of 2^-F
                     const float *vsc = reinterpret_cast<const float *>(st + kHsVs);
                     const float *vmn = reinterpret_cast<const float *>(st + kHsVm);
-                    const float vmax = warp_max(fmaxf(vsc[lane], vsc[lane + 32]));
+                    const uint32_t wlo_a = smem_addr(s_wlo), whi_a = smem_addr(s_whi);
+
+                    float z0, z1;                           // keys lane and 32 + lane of the half
+                    {
+                        // QK^T, two keys per lane (lane, 32 + lane) in one pass, so each weight pair
+                        // loaded serves both keys: the codes unpacked to bytes (field j of a word
+                        // holds channels j, 4 + j, 8 + j, 12 + j) meet the weight pairs in dp2a
+                        // (exact int32).  Field j is masked in place, leaving bytes code * 4^j (<=
+                        // 192), one accumulator per field and key; the 4^j is divided out exactly
+                        // at the end
+                        const uint4 *kl0 = reinterpret_cast<const uint4 *>(st + kHsKlo + lane * 32);
+                        const uint4 *kl1 = reinterpret_cast<const uint4 *>(st + kHsKlo + (32 + lane) * 32);
+                        int a0[4] = {0, 0, 0, 0}, a1[4] = {0, 0, 0, 0};
+#pragma unroll
+                        for (int hw4 = 0; hw4 < 2; ++hw4) {
+                            const uint4 x0 = kl0[hw4], x1 = kl1[hw4];
+                            const uint32_t k0w[4] = {x0.x, x0.y, x0.z, x0.w}, k1w[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int wd = hw4 * 4 + q;
+                                uint32_t wp[8];
+                                lds128(wlo_a + wd * 32, wp[0], wp[1], wp[2], wp[3]);
+                                lds128(wlo_a + wd * 32 + 16, wp[4], wp[5], wp[6], wp[7]);
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const uint32_t m = 0x03030303u << (2 * j);
+                                    const uint32_t u0 = k0w[q] & m, u1 = k1w[q] & m;
+                                    a0[j] = dp2a_lo(wp[2 * j], u0, a0[j]);
+                                    a1[j] = dp2a_lo(wp[2 * j], u1, a1[j]);
+                                    a0[j] = dp2a_hi(wp[2 * j + 1], u0, a0[j]);
+                                    a1[j] = dp2a_hi(wp[2 * j + 1], u1, a1[j]);
+                                }
+                            }
+                        }
+                        int h0[4] = {0, 0, 0, 0}, h1[4] = {0, 0, 0, 0};
+                        uint32_t hv0[P / 16], hv1[P / 16];
+                        if constexpr (P == 32) {
+                            const uint2 y0 = *reinterpret_cast<const uint2 *>(st + kHsKhi + lane * 8);
+                            const uint2 y1 = *reinterpret_cast<const uint2 *>(st + kHsKhi + (32 + lane) * 8);
+                            hv0[0] = y0.x; hv0[1] = y0.y; hv1[0] = y1.x; hv1[1] = y1.y;
+                        } else {
+                            hv0[0] = *reinterpret_cast<const uint32_t *>(st + kHsKhi + lane * 4);
+                            hv1[0] = *reinterpret_cast<const uint32_t *>(st + kHsKhi + (32 + lane) * 4);
+                        }
+#pragma unroll
+                        for (int wd = 0; wd < P / 16; ++wd) {
+                            uint32_t wp[8];
+                            lds128(whi_a + wd * 32, wp[0], wp[1], wp[2], wp[3]);
+                            lds128(whi_a + wd * 32 + 16, wp[4], wp[5], wp[6], wp[7]);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t m = 0x03030303u << (2 * j);
+                                const uint32_t u0 = hv0[wd] & m, u1 = hv1[wd] & m;
+                                h0[j] = dp2a_lo(wp[2 * j], u0, h0[j]);
+                                h1[j] = dp2a_lo(wp[2 * j], u1, h1[j]);
+                                h0[j] = dp2a_hi(wp[2 * j + 1], u0, h0[j]);
+                                h1[j] = dp2a_hi(wp[2 * j + 1], u1, h1[j]);
+                            }
+                        }
+                        const int d0 = (a0[0] + (a0[1] >> 2)) + ((a0[2] >> 4) + (a0[3] >> 6)) +
+                                       4 * ((h0[0] + (h0[1] >> 2)) + ((h0[2] >> 4) + (h0[3] >> 6)));
+                        const int d1 = (a1[0] + (a1[1] >> 2)) + ((a1[2] >> 4) + (a1[3] >> 6)) +
+                                       4 * ((h1[0] + (h1[1] >> 2)) + ((h1[2] >> 4) + (h1[3] >> 6)));
+                        z0 = fmaf((float)d0, zmul, b);
+                        z1 = fmaf((float)d1, zmul, b);
+                    }
+                    // online softmax over the half's 64 keys (one max, so every P of the half
+                    // refers to the same m_run), reduced together with the half's largest V
+                    // token scale: F puts it in [2^13, 2^14); o is kept in units of 2^-F
+                    float mloc = fmaxf(z0, z1), vmax = fmaxf(vsc[lane], vsc[lane + 32]);
+#pragma unroll
+                    for (int sh = 16; sh > 0; sh >>= 1) {
+                        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, sh));
+                        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, sh));
+                    }
                     const int F = vmax > 0.f ? max(-60, min(60, 13 - exponent_of(vmax))) : 0;
                     if (!have_F) {
                         F_cur = F;
@@ -653,61 +728,6 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
                         F_cur = F;
                     }
                     const float psc = pow2f(F_cur);
-                    const uint32_t wlo_a = smem_addr(s_wlo), whi_a = smem_addr(s_whi);
-
-                    float z0 = 0.f, z1 = 0.f;               // keys lane and 32 + lane of the half
-#pragma unroll 1
-                    for (int pass = 0; pass < 2; ++pass) {
-                        const int t = pass * 32 + lane;
-                        // QK^T, one key per lane: the codes unpacked to bytes (field j of a word holds
-                        // channels j, 4 + j, 8 + j, 12 + j) meet the weight pairs in dp2a (exact int32)
-                        const uint4 *kl = reinterpret_cast<const uint4 *>(st + kHsKlo + t * 32);
-                        const uint4 w0 = kl[0], w1 = kl[1];
-                        const uint32_t kw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                        // field j masked in place: bytes code * 4^j (<= 192), one accumulator per field,
-                        // the 4^j divided out exactly at the end
-                        int acc[4] = {0, 0, 0, 0}, acch[4] = {0, 0, 0, 0};
-#pragma unroll
-                        for (int wd = 0; wd < 8; ++wd) {
-                            uint32_t wp[8];
-                            lds128(wlo_a + wd * 32, wp[0], wp[1], wp[2], wp[3]);
-                            lds128(wlo_a + wd * 32 + 16, wp[4], wp[5], wp[6], wp[7]);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const uint32_t u = kw[wd] & (0x03030303u << (2 * j));
-                                acc[j] = dp2a_lo(wp[2 * j], u, acc[j]);
-                                acc[j] = dp2a_hi(wp[2 * j + 1], u, acc[j]);
-                            }
-                        }
-                        uint32_t hw[P / 16];
-                        if constexpr (P == 32) {
-                            const uint2 h2 = *reinterpret_cast<const uint2 *>(st + kHsKhi + t * 8);
-                            hw[0] = h2.x;
-                            hw[1] = h2.y;
-                        } else {
-                            hw[0] = *reinterpret_cast<const uint32_t *>(st + kHsKhi + t * 4);
-                        }
-#pragma unroll
-                        for (int wd = 0; wd < P / 16; ++wd) {
-                            uint32_t wp[8];
-                            lds128(whi_a + wd * 32, wp[0], wp[1], wp[2], wp[3]);
-                            lds128(whi_a + wd * 32 + 16, wp[4], wp[5], wp[6], wp[7]);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const uint32_t u = hw[wd] & (0x03030303u << (2 * j));
-                                acch[j] = dp2a_lo(wp[2 * j], u, acch[j]);
-                                acch[j] = dp2a_hi(wp[2 * j + 1], u, acch[j]);
-                            }
-                        }
-                        const int dot = (acc[0] + (acc[1] >> 2)) + ((acc[2] >> 4) + (acc[3] >> 6)) +
-                                        4 * ((acch[0] + (acch[1] >> 2)) + ((acch[2] >> 4) + (acch[3] >> 6)));
-                        const float z = fmaf((float)dot, zmul, b);
-                        if (pass == 0) z0 = z;
-                        else z1 = z;
-                    }
-                    // online softmax over the half's 64 keys (one max, so every P of the half
-                    // refers to the same m_run)
-                    const float mloc = warp_max(fmaxf(z0, z1));
                     if (mloc > m_run) {
                         const float al = fast_exp2(m_run - mloc);
                         l_l *= al;
@@ -739,7 +759,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
                         for (int i = 0; i < 8; ++i) lds128(p_a + 16 * i, pp[4 * i], pp[4 * i + 1], pp[4 * i + 2], pp[4 * i + 3]);
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            const uint4 v = vc[c];
+                            // the lane's c-th load is its word (c + vrot) & 3: neighbouring lanes
+                            // start on different 16-byte words, so a load touches every bank
+                            // four times instead of half the banks sixteen times
+                            const uint4 v = vc[(c + vrot) & 3];
                             const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
                             int af[4] = {0, 0, 0, 0};       // per field j, in units of 4^j
 #pragma unroll
@@ -766,7 +789,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) kitty_decode_kernel(DecPara
         const float f = pow2f(-F_cur);
         float res[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) res[i] = fmaf(o[i], f, bv);
+        for (int i = 0; i < 4; ++i) {
+            const int c = (i - vrot) & 3;
+            const float oc = c == 0 ? o[0] : c == 1 ? o[1] : c == 2 ? o[2] : o[3];
+            res[i] = fmaf(oc, f, bv);
+        }
         if (cur.nch == 1) {
             const float inv = 1.f / l;
             float v[4] = {res[0] * inv, res[1] * inv, res[2] * inv, res[3] * inv};
