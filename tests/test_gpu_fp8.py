@@ -272,3 +272,40 @@ def test_e4m3_mixed_gqa_full_size():
     rows = sample_rows(b, 192, seed=5)
     ref = oracle.paged_attention_batch(b, rows=rows, threads=16, kv=(kc, vc, ks, vs))
     assert_close(gather_rows(out, b, rows), ref, b.dtype, "mixed_gqa e4m3")
+
+
+def test_e4m3_turns_on_a_block_first_pool():
+    """Every layer of a block-first pool of E4M3 codes ([num_blocks, L, K|V, Hkv, B, d]): the
+    widening reads each layer's blocks through the pool's block stride."""
+    ctx, ql, ks, vs = [700, 90, 1500, 33], [40, 3, 130, 1], 1 / 32, 1 / 16
+    b = W.make_attn_batch("fp8blockfirst", ctx, ql, 8, 2, 128, 16, "bf16", seed=81, poison=False)
+    L = 3
+    codes = [(_codes(b.k_cache.shape, ks, 82 + 2 * l), _codes(b.v_cache.shape, vs, 83 + 2 * l)) for l in range(L)]
+    pool = torch.stack([torch.stack([torch.from_numpy(k), torch.from_numpy(v)], 1) for k, v in codes], 1).cuda()
+    q, bt, c, qlen = to_dev(b.q, "bf16"), to_dev(b.block_tables), to_dev(b.ctx_lens), to_dev(b.q_lens)
+    for layer, (k, v) in enumerate(codes):
+        kc, vc = pool[:, layer, 0], pool[:, layer, 1]
+        assert kc.stride(0) == L * 2 * kc[0].numel()
+        ws = torch.zeros(pkg.forward_workspace_size(q, kc, bt, c), dtype=torch.uint8, device="cuda")
+        out = pkg.pa_forward(q, kc, vc, bt, c, qlen, b.scale, workspace=ws, k_scale=ks, v_scale=vs)
+        torch.cuda.synchronize()
+        assert pkg.device_status() == 0
+        assert ws[:64].view(torch.int32)[7].item() > 0, "no block was widened"
+        ref = oracle.paged_attention_batch(b, threads=8, kv=(k, v, ks, vs))
+        assert_close(as_f64(out), ref, "bf16", f"block-first e4m3 layer {layer}")
+
+
+def test_no_alloc_entry_point_widens_e4m3_turns():
+    """pa_forward_no_alloc on E4M3 turns: its fixed scratch past the required workspace holds this
+    batch's widened blocks, so it runs the same kernels as pa_forward with the full widening
+    workspace and returns the same bits."""
+    ks, vs = 1 / 16, 1 / 32
+    b, kc, vc = _fp8_batch("fp8noalloc_turns", [600, 31, 2000], [50, 1, 70], 16, 4, 32, "f16", ks, vs, seed=43)
+    args = _dev_args(b, kc, vc) + (b.scale,)
+    a = pkg.pa_forward(*args, k_scale=ks, v_scale=vs)
+    c = pkg.pa_forward_no_alloc(*args, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pkg.device_status() == 0
+    assert torch.equal(a, c)
+    ref = oracle.paged_attention_batch(b, threads=8, kv=(kc, vc, ks, vs))
+    assert_close(as_f64(c), ref, "f16", "no-alloc e4m3 turns")
