@@ -99,7 +99,8 @@ typedef enum { PA_KV_SAME = 0, PA_KV_E4M3 = 1 } pa_kv_dtype;
  * many blocks as the caller's workspace has room for (pa_forward_widen_bytes: enough for every
  * sequence the kernel may take); such sequences are admitted in sequence order while all of their
  * blocks fit, and the others run on the CUDA-core kernels, so any workspace of at least
- * pa_forward_workspace_size bytes is valid.  Their key ranges are not cut into chunks.
+ * pa_forward_workspace_size bytes is valid.  Their key ranges are cut into chunks (as below) only
+ * when the workspace holds all of pa_forward_widen_bytes, whose last 16 MB hold the chunks.
  * Sequences with q_len * g >= 16 query rows per KV head run on the tcgen05 tensor-core kernel when
  * the dtype is bf16/f16, d = 128, g divides 128 and scale > 0 (one work item per KV head and pair
  * of 128-row query tiles; when a call has fewer such items than SMs, each item's key range is
@@ -138,9 +139,12 @@ size_t pa_forward_workspace_size(const pa_dims *dims);
 /* Extra workspace, past pa_forward_workspace_size(dims), that lets every sequence the tensor-core
  * kernel may take of an E4M3 call (dims with total_q > num_seqs and a shape that kernel supports)
  * run on it: a candidate-block prefix ([num_seqs + 1] int32) and a block table ([num_seqs,
- * max_blocks_per_seq] int32), each padded to 256 bytes, then widened K and V blocks for min(num_seqs, total_q / ceil(16 / g)) * max_blocks_per_seq
- * blocks.  0 for other dims or invalid dims.  The bound is from the dims alone; a smaller extra
- * (down to none) is valid and sends the sequences that do not fit to the CUDA-core kernels. */
+ * max_blocks_per_seq] int32), each padded to 256 bytes; widened K and V blocks for
+ * min(num_seqs, total_q / ceil(16 / g)) * max_blocks_per_seq blocks; then the tensor-core
+ * kernel's chunk counters and partial rows (3840 and 120 * 2 * 128 * 528 bytes).  0 for other
+ * dims or invalid dims.  The bound is from the dims alone; a smaller extra (down to none) is valid:
+ * it holds fewer widened blocks (the sequences that do not fit run on the CUDA-core kernels) and
+ * no chunk regions. */
 size_t pa_forward_widen_bytes(const pa_dims *dims);
 
 pa_status pa_forward(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,

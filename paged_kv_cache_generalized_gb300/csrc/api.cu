@@ -221,10 +221,17 @@ WidenLayout widen_layout(const pa_dims &d, size_t base, size_t workspace_bytes) 
     w.cu = base;
     w.bt = align_up(w.cu + (S + 1) * 4, 256);
     w.k = align_up(w.bt + S * (size_t)d.max_blocks_per_seq * 4, 256);
-    w.end = w.k + (size_t)bound * 2 * blk;
-    int64_t cap = workspace_bytes > w.k ? (int64_t)((workspace_bytes - w.k) / (2 * blk)) : 0;
+    w.arrive = align_up(w.k + (size_t)bound * 2 * blk, 256);
+    w.part = align_up(w.arrive + (size_t)kMaxTcChunkItems * 8 * sizeof(uint32_t), 256);
+    w.end = w.part + (size_t)kMaxTcChunkItems * 2 * kTcTileRows * kTcPartFloats * sizeof(float);
+    // the bound's blocks and the chunk regions, else as many blocks as fit and no chunks
+    w.chunks = workspace_bytes >= w.end;
+    int64_t cap = w.chunks ? bound : (workspace_bytes > w.k ? (int64_t)((workspace_bytes - w.k) / (2 * blk)) : 0);
     if (cap > bound) cap = bound;
-    if (cap >= (int64_t(1) << 31) - 1) cap = (int64_t(1) << 31) - 2;   // block ids of the tensor map
+    if (cap >= (int64_t(1) << 31) - 1) {   // block ids of the tensor map
+        cap = (int64_t(1) << 31) - 2;
+        w.chunks = false;
+    }
     w.cap = cap;
     w.v = w.k + (size_t)cap * blk;
     return w;
@@ -324,6 +331,11 @@ pa_status forward_impl(const pa_dims *dims, const void *q, const void *k_cache, 
             a.wid_bt = reinterpret_cast<int32_t *>(a.ws + w.bt);
             a.wid_k = a.ws + w.k;
             a.wid_v = a.ws + w.v;
+            if (w.chunks) {   // few pair items: their key ranges may run as chunks
+                a.lay.tc_chunks = true;
+                a.lay.tc_arrive = w.arrive;
+                a.lay.tc_part = w.part;
+            }
         }
     }
     AppendParams ap;

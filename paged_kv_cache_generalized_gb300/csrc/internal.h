@@ -103,13 +103,17 @@ WsLayout ws_layout(const pa_dims &d);
 // (exactly) to the query dtype into scratch past the workspace layout: the candidate-block prefix,
 // a remapped block table, then `cap` widened K blocks and `cap` V blocks.  `cap` is what the
 // caller's workspace holds, at most the bound for the dims; sequences whose blocks do not fit run
-// on the CUDA-core kernels.
+// on the CUDA-core kernels.  A workspace that holds the bound's blocks also holds, after them, the
+// tensor-core kernel's chunk regions (16-bit caches keep those in the required layout).
 struct WidenLayout {
     size_t cu;         // int32 [S+1]  prefix of candidate sequences' blocks (planner)
     size_t bt;         // int32 [S * max_blocks_per_seq]  block table of the widened blocks
     size_t k, v;       // [cap, Hkv, B, d] in the query dtype
-    size_t end;        // first byte past the V blocks for the bound (the size to ask for)
+    size_t arrive;     // chunk arrival counters, as WsLayout::tc_arrive (when `chunks`)
+    size_t part;       // chunk partial rows, as WsLayout::tc_part (when `chunks`)
+    size_t end;        // first byte past the chunk regions for the bound (the size to ask for)
     int64_t cap;       // widened blocks the caller's workspace holds (0: no widening)
+    bool chunks;       // the workspace holds the bound's blocks and the chunk regions
 };
 // Whether E4M3 dims may widen at all (total_q > num_seqs and a shape the tensor-core kernel takes).
 bool widen_eligible(const pa_dims &d);

@@ -69,8 +69,9 @@ def test_workspace_size_is_host_only(lib):
 
 def test_widen_bytes_cover_every_tensor_core_candidate(lib):
     """E4M3 dims with multi-token turns: a 256-byte-aligned candidate prefix (S + 1 int32) and block
-    table (S x max_blocks int32), then K and V blocks of the query dtype for every sequence that may
-    take the tensor-core kernel (q_len * g >= 16, so at most total_q // ceil(16 / g) sequences)."""
+    table (S x max_blocks int32), K and V blocks of the query dtype for every sequence that may take
+    the tensor-core kernel (q_len * g >= 16, so at most total_q // ceil(16 / g) sequences), then the
+    chunk counters and partial rows."""
     def w(**kw):
         return lib.pa_forward_widen_bytes(ctypes.byref(_dims(**kw)))
 
@@ -78,15 +79,16 @@ def test_widen_bytes_cover_every_tensor_core_candidate(lib):
         return (x + 255) // 256 * 256
 
     e4 = dict(kv_dtype=1, k_scale=0.5, v_scale=0.25)
+    chunks = 120 * 8 * 4 + 120 * 2 * 128 * 132 * 4       # chunk counters and partial rows
     # 8 sequences, 100 query tokens, GQA 4 (at least 4 tokens each): all 8 may take the kernel
     got = w(num_seqs=8, total_q=100, max_blocks_per_seq=40, **e4)
-    assert got == up(9 * 4) + up(8 * 40 * 4) + 8 * 40 * 2 * (2 * 16 * 128 * 2)
+    assert got == up(9 * 4) + up(8 * 40 * 4) + 8 * 40 * 2 * (2 * 16 * 128 * 2) + chunks
     # 40 query tokens over 30 sequences: at most 10 of them have 4 tokens
     got = w(num_seqs=30, total_q=40, max_blocks_per_seq=7, **e4)
-    assert got == up(31 * 4) + up(30 * 7 * 4) + 10 * 7 * 2 * (2 * 16 * 128 * 2)
+    assert got == up(31 * 4) + up(30 * 7 * 4) + 10 * 7 * 2 * (2 * 16 * 128 * 2) + chunks
     # MHA (g = 1): 16 tokens per candidate
     got = w(num_seqs=4, total_q=50, num_q_heads=2, max_blocks_per_seq=5, **e4)
-    assert got == up(5 * 4) + up(4 * 5 * 4) + 3 * 5 * 2 * (2 * 16 * 128 * 2)
+    assert got == up(5 * 4) + up(4 * 5 * 4) + 3 * 5 * 2 * (2 * 16 * 128 * 2) + chunks
     assert w(num_seqs=4, total_q=4, **e4) == 0                  # decode only
     assert w(num_seqs=2, total_q=30) == 0                      # 16-bit caches need no widening
     assert w(num_seqs=2, total_q=30, head_dim=64, **e4) == 0   # unsupported E4M3 shape

@@ -309,3 +309,29 @@ def test_no_alloc_entry_point_widens_e4m3_turns():
     assert torch.equal(a, c)
     ref = oracle.paged_attention_batch(b, threads=8, kv=(kc, vc, ks, vs))
     assert_close(as_f64(c), ref, "f16", "no-alloc e4m3 turns")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_e4m3_few_turns_run_as_key_range_chunks(dtype):
+    """One 64-token turn over a 20K-token history beside a decode row (GQA 16/2): 2 pair items,
+    so with the whole widening workspace the key ranges run as chunks.  Within the oracle's bar,
+    and (power-of-two scales) bit for bit the result of 16-bit caches holding code * scale, which
+    chunk the same way."""
+    ks, vs = 1 / 32, 1 / 16
+    b, kc, vc = _fp8_batch("fp8chunks", [20000, 300], [64, 1], 16, 2, 16, dtype, ks, vs, seed=91)
+    out8, counters = _forward_ws(b, kc, vc, ks, vs)
+    assert pkg.device_status() == 0
+    assert counters[3] > 0 and counters[6] > 0, "the pairs were not chunked"
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    k16 = (torch.from_numpy(kc).cuda().view(torch.float8_e4m3fn).float() * ks).to(tdt)
+    v16 = (torch.from_numpy(vc).cuda().view(torch.float8_e4m3fn).float() * vs).to(tdt)
+    q, _, _, bt, c, qlen = _dev_args(b, kc, vc)
+    ws = torch.zeros(pkg.forward_workspace_size(q, k16, bt, c), dtype=torch.uint8, device="cuda")
+    out16 = pkg.pa_forward(q, k16, v16, bt, c, qlen, b.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkg.device_status() == 0
+    assert ws[:64].view(torch.int32)[6].item() == counters[6]
+    # the decode row runs on different CUDA-core kernels for the two cache types: compare the turn
+    assert torch.equal(out8[:64], out16[:64])
+    ref = oracle.paged_attention_batch(b, threads=16, kv=(kc, vc, ks, vs))
+    assert_close(as_f64(out8), ref, dtype, f"e4m3 chunks {dtype}")
