@@ -187,6 +187,9 @@ pa_status pa_set_timing_events(void *tc_start, void *tc_stop, void *cc_start, vo
  *    cudaMalloc, cudaFree or allocating library routine).
  *  - Dims whose pa_forward_workspace_size exceeds PA_NO_ALLOC_WORKSPACE_BYTES are rejected with
  *    PA_ERR_WORKSPACE before any device work (use pa_forward with your own workspace instead).
+ *  - E4M3 calls widen their tensor-core turns into the part of the array past
+ *    pa_forward_workspace_size (see pa_forward): turns that do not fit there run on the CUDA-core
+ *    kernels.
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
  *    that device current); make that first call before any stream capture.
  *  - Every call on a device shares the one array, which keeps the last call's contents (nothing
