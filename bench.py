@@ -421,6 +421,42 @@ class AttnStep:
         self.step()
         self.out_host.copy_(self.out, non_blocking=True)
 
+    def decode_alone_ms(self, warmup=3, reps=20):
+        """Median time of pa_forward over the sequences that do not take the tensor-core kernel
+        alone (same device caches, their rows of q), outside the timed steps: the decode part's
+        own rate, which the mixed call's bracket cannot give (there the decode kernel waits for the
+        SMs the tensor-core kernel holds).  None when every sequence takes the tensor-core kernel."""
+        torch = self.torch
+        dec = np.flatnonzero(~tc_rows(self.b))
+        if not self.has_tc or len(dec) == 0:
+            return None
+        cu = np.concatenate([[0], np.cumsum(self.b.q_lens.astype(np.int64))])
+        rows = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in dec])
+        sel = torch.from_numpy(dec).to(self.dev)
+        q = self.dev_in["q"][torch.from_numpy(rows).to(self.dev)].contiguous()
+        bt = self.dev_in["bt"][sel].contiguous()
+        ctx, ql = self.dev_in["ctx"][sel].contiguous(), self.dev_in["ql"][sel].contiguous()
+        ws = torch.empty(max(256, self.pkg.forward_workspace_size(q, self.k_cache, bt, ctx)),
+                         dtype=torch.uint8, device=self.dev)
+        out = torch.empty_like(q)
+
+        def call():
+            self.pkg.pa_forward(q, self.k_cache, self.v_cache, bt, ctx, ql, self.b.scale, out=out,
+                                workspace=ws, k_scale=self.ks, v_scale=self.vs)
+
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e[0].record()
+            call()
+            e[1].record()
+            torch.cuda.synchronize()
+            ts.append(e[0].elapsed_time(e[1]))
+        return float(np.median(ts))
+
 
 class KittyStep:
     """kv_append + kv_quantize_pages + pa_forward_kitty over one KittyBatch (2-bit pages with
@@ -1094,6 +1130,7 @@ def measure_attn_workload(name, args, dev, dist, world, local, peaks, peak_src, 
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev) / Ke
     e2e_val = work * world / (e2e_ms * 1e-3) / scale_u
+    dec_alone_ms = step_obj.decode_alone_ms() if kernel_events and unit != "GB/s" else None
     flags = step_obj.pkg.device_status()
 
     res = {"metric": metric, "unit": unit, "higher_is_better": hib, "value": value, "ms_per_step": ms_step,
@@ -1150,6 +1187,11 @@ def measure_attn_workload(name, args, dev, dist, world, local, peaks, peak_src, 
             roof["decode_part"] = {"algorithmic_bytes": dec_bytes, "bracket_ms": cc_ms,
                                    "achieved_gbs": dec_bytes / (cc_ms * 1e-3) / 1e9,
                                    "note": "bracket includes waiting for SMs held by the tensor-core kernel"}
+            if dec_alone_ms:
+                # the same rows in a call of their own (planner + decode kernel), after the steps
+                a_gbs = dec_bytes / (dec_alone_ms * 1e-3) / 1e9
+                roof["decode_part"].update({"alone_ms": dec_alone_ms, "alone_achieved_gbs": a_gbs,
+                                            "alone_frac_hbm": a_gbs / peaks["hbm_gbs"]})
     res["roofline"] = roof
     del step_obj
     torch.cuda.synchronize()
